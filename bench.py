@@ -1,0 +1,393 @@
+"""Decode-step benchmark of the IceCache select + sparse-attention path on GB300.
+
+One step = ice_select + ice_sparse_attn for every unit (layer x KV head) of a
+Llama-3.1-8B-shaped decode step at a 36,864-token context (32 layers, 8 KV
+heads, 4 query heads per KV head, d = 128, bf16, page_size 16, token budget
+256, 8 projections x 2 composite indices). Inputs are synthetic clustered
+Gaussian keys (512 centres per unit) and N(0, 1) values, resident in HBM.
+L2 is flushed (256 MiB write) between timed steps, outside the events.
+
+Prints one JSON line. Metric: select+attn latency in us per layer (lower is
+better), with the achieved HBM bandwidth of the dominant kernel against the
+measured copy bandwidth of the GPU.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ice|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-step select+attn latency (µs/layer) & achieved HBM GB/s vs peak, 1 GB300"
+UNIT = "us/layer"
+WORKLOAD = "llama8b_36k"
+FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _workload(name):
+    from semantic_paged_kv_head_gb300 import synth
+    return synth.WORKLOADS[name]
+
+
+def _config(w):
+    return {"workload": w.name, "n_layers": w.n_layers, "n_kv_heads": w.n_kv_heads,
+            "group": w.group, "d": w.d, "n_tokens": w.n_tokens, "batch": w.batch,
+            "page_size": w.page_size, "token_budget": w.budget, "n_proj": w.n_proj,
+            "n_composite": w.n_composite, "n_centers": w.n_centers,
+            "l2": "flushed between steps (256 MiB write, outside the timed events)"}
+
+
+# --------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0, out_path=None):
+        self.proc = None
+        self.path = out_path or os.path.join(ROOT, "gpurun_out", "clocks.csv")
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------------------
+# the oracle (CPU) on a bounded sample: cpu_baseline leg and the reference arm
+# --------------------------------------------------------------------------------------
+def oracle_time_units(w, keys_u, values_u, q_u, budget_s=10.0):
+    """Time oracle select+attn over the given units (lists of CPU tensors).
+    Returns (us per unit, repetitions, per-unit (page_ids, n_pages, trace))."""
+    from oracle.oracle import OracleIndex
+    idx = []
+    for k, v in zip(keys_u, values_u):
+        ix = OracleIndex(w.d, w.n_proj, w.n_composite, w.page_size, w.seed)
+        ix.build(k, v)
+        idx.append(ix)
+    results = []
+    for ix, q in zip(idx, q_u):
+        ids, npg, tr = ix.select(q, w.budget)
+        ix.attn(q, ids, npg)
+        results.append((ids, npg, tr))
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        for ix, q in zip(idx, q_u):
+            ids, npg, _ = ix.select(q, w.budget)
+            ix.attn(q, ids, npg)
+            reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return dt / reps * 1e6, reps, results
+
+
+def run_reference(args):
+    """--impl reference: the oracle as it stands, on the host cores, one layer
+    (8 KV-head units) of the same workload shape per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from semantic_paged_kv_head_gb300 import synth
+    w = _workload(args.workload)
+    ws = synth.scaled(w, n_layers=1, batch=1)
+    keys, values, centers = synth.make_kv(ws)
+    q = synth.make_queries(ws, centers)
+    from oracle.oracle import OracleIndex
+    idx, qs = [], []
+    for h in range(ws.n_kv_heads):
+        ix = OracleIndex(w.d, w.n_proj, w.n_composite, w.page_size, w.seed)
+        ix.build(keys[0, 0, h], values[0, 0, h])
+        idx.append(ix)
+        qs.append(q[0, 0, h * w.group:(h + 1) * w.group])
+
+    def step():
+        for ix, qq in zip(idx, qs):
+            ids, npg, _ = ix.select(qq, w.budget)
+            ix.attn(qq, ids, npg)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    us_layer = dt * 1e6  # one step = one layer (all KV heads)
+    sample = (f"one layer ({ws.n_kv_heads} KV-head units, {w.n_tokens} tokens each) of the "
+              f"{w.name} shape per step; oracle build untimed")
+    line = {"impl": "reference", "metric": METRIC, "value": round(us_layer, 3), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 4), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 select (fixed-order fp32 dot), f64 attention",
+            "data": "synthetic", "config": _config(w),
+            "cpu_baseline": {"value": round(us_layer, 3), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(us_layer, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------------------
+def _traffic_for(kernel, src_file):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    with open(os.path.join(ROOT, "semantic_paged_kv_head_gb300", "csrc", src_file), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if ent.get("source_sha") != h:
+        return None
+    return ent.get("dram_bytes_per_launch_full")
+
+
+def run_ice(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from semantic_paged_kv_head_gb300 import build as ice_build
+    ice_build.build_lib()
+    from semantic_paged_kv_head_gb300 import ice, synth
+
+    w = _workload(args.workload)
+    dev = torch.device("cuda", local)
+    keys, values, centers = synth.make_kv(w, device=dev)
+    q = synth.make_queries(w, centers)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ix = ice.IceIndex.build(keys, values, page_size=w.page_size, n_q_heads=w.n_q_heads,
+                            n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed)
+    torch.cuda.synchronize()
+    build_ms = (time.perf_counter() - t0) * 1e3
+    U = ix.n_units
+    n_sel = w.budget // w.page_size
+    page_ids = torch.empty((U, n_sel), dtype=torch.int32, device=dev)
+    n_pages = torch.empty((U,), dtype=torch.int32, device=dev)
+    stats = torch.zeros((U, 4), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # algorithmic bytes (counters verified against the oracle trace by the tests)
+    ix.select(q, w.budget, page_ids, n_pages, stats)
+    ix.sparse_attn(q, page_ids, n_pages, out)
+    torch.cuda.synchronize()
+    ix.check()
+    st = stats.double().sum(0).tolist()
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    qo = U * w.group * w.d * es
+    ids_b = U * (n_sel + 1) * 4
+    sel_bytes = st[0] * (2 * w.n_proj + 4) + st[1] * (w.d * es + 4) + qo + ids_b
+    attn_bytes = st[2] * 2 * w.d * es + 2 * qo + ids_b
+    step_bytes = sel_bytes + attn_bytes
+
+    def one_step():
+        ix.select(q, w.budget, page_ids, n_pages)
+        ix.sparse_attn(q, page_ids, n_pages, out)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        one_step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            ix.select(q, w.budget, page_ids, n_pages)
+            ev[k][1].record(stream)
+            ix.sparse_attn(q, page_ids, n_pages, out)
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    t_sel = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
+    t_att = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    t_step = [a + b for a, b in zip(t_sel, t_att)]
+    ms_step = sum(t_step) / len(t_step)
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    ix.check()
+    ms_sel = sum(t_sel) / len(t_sel)
+    ms_att = sum(t_att) / len(t_att)
+
+    # end to end through the public API: pinned host q in, host out back, every step
+    q_host = q.cpu().pin_memory()
+    out_host = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    q_in = torch.empty_like(q)
+    n_e2e = max(10, args.steps // 4)
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
+    for _ in range(3):
+        q_in.copy_(q_host, non_blocking=True)
+        ix.select(q_in, w.budget, page_ids, n_pages)
+        ix.sparse_attn(q_in, page_ids, n_pages, out)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    for k in range(n_e2e):
+        flush.zero_()
+        ev2[k][0].record(stream)
+        q_in.copy_(q_host, non_blocking=True)
+        ix.select(q_in, w.budget, page_ids, n_pages)
+        ix.sparse_attn(q_in, page_ids, n_pages, out)
+        out_host.copy_(out, non_blocking=True)
+        ev2[k][1].record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = sum(e[0].elapsed_time(e[1]) for e in ev2) / n_e2e
+
+    peak, peak_kind = _peaks()
+    sel_gbs = sel_bytes / (ms_sel * 1e-3) / 1e9
+    att_gbs = attn_bytes / (ms_att * 1e-3) / 1e9
+    if ms_sel >= ms_att:
+        dom, dom_bytes, dom_ms, dom_gbs, src = "select_kernel", sel_bytes, ms_sel, sel_gbs, "ice_select.cu"
+    else:
+        dom, dom_bytes, dom_ms, dom_gbs, src = "attn_kernel", attn_bytes, ms_att, att_gbs, "ice_attn.cu"
+    us_layer = ms_step * 1e3 / (w.n_layers * w.batch)
+    line = {
+        "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": _config(w),
+        "step_bytes": int(step_bytes),
+        "step_gbs": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
+        "step_frac_of_peak": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "kernels": {"select_kernel": {"us": round(ms_sel * 1e3, 3), "bytes": int(sel_bytes),
+                                      "gbs": round(sel_gbs, 1)},
+                    "attn_kernel": {"us": round(ms_att * 1e3, 3), "bytes": int(attn_bytes),
+                                    "gbs": round(att_gbs, 1)}},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                     "traffic": _traffic_for(dom, src), "algorithmic_bytes": int(dom_bytes)},
+        "e2e": {"value": round(ms_e2e * 1e3 / (w.n_layers * w.batch), 4), "unit": UNIT,
+                "h2d_bytes_per_step": int(q.numel() * q.element_size()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+        "gpu_launches": 2 * args.steps,
+        "build_ms": round(build_ms, 1),
+        "wall_s_timed_region": round(wall, 3),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample_units = [0, 85, 170, 255][: max(1, min(4, U))]
+        ku = [keys.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]
+        vu = [values.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]
+        qu = [q.view(U, w.group, w.d)[u].cpu() for u in sample_units]
+        us_unit, reps, res = oracle_time_units(w, ku, vu, qu, budget_s=args.cpu_seconds)
+        units_per_layer = U // (w.n_layers * w.batch)
+        ids_cpu = page_ids.cpu().numpy()
+        same = all(res[i][1] == int(n_pages[u]) and
+                   (ids_cpu[u][:n_sel] == res[i][0]).all() for i, u in enumerate(sample_units))
+        st_cpu = stats.cpu().numpy()
+        stats_same = all(st_cpu[u][0] == res[i][2]["leaves"] and st_cpu[u][1] == res[i][2]["cands"]
+                         and st_cpu[u][2] == res[i][2]["sel_tokens"]
+                         for i, u in enumerate(sample_units))
+        line["cpu_baseline"] = {
+            "value": round(us_unit * units_per_layer, 2), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": (f"units {sample_units} of this workload, select+attn repeated {reps} times "
+                       f"(~{args.cpu_seconds:.0f} s, single thread); oracle build untimed; "
+                       f"us/layer = us/unit x {units_per_layer} KV heads")}
+        line["parity_sampled"] = {"units": sample_units, "page_ids_equal": bool(same),
+                                  "byte_counters_equal": bool(stats_same)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ice", "reference"], default="ice")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ice(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

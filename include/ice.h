@@ -1,0 +1,211 @@
+/*
+ * ice.h - C ABI of the GB300-native IceCache decode-time library (libice.so).
+ *
+ * IceCache ("IceCache", arXiv 2604.10539) keeps the KV cache of each attention
+ * head in pages that are the leaves of a DCI-tree built over the keys in a
+ * transformed key space (Figure 2 step 1; Figure 3 maps tree nodes to physical
+ * pages). Generated tokens are inserted without a rebuild (abstract:
+ * "dynamically updatable"). At each decode step a prioritised tree search
+ * finds the query's top keys, the pages holding them are selected (Figure 2
+ * steps 2-3), and attention runs over every token of those pages.
+ *
+ * This library runs all of it on one GPU with its own CUDA kernels. The four
+ * calls of the method are ice_build, ice_insert, ice_select and
+ * ice_sparse_attn; they work on a grid of independent UNITS, one unit being
+ * one (sequence b, layer l, KV head h), unit index u = (b * n_layers + l) *
+ * n_kv_heads + h. Query head g of unit u is q_head = h * G + g with
+ * G = n_q_heads / n_kv_heads (grouped-query attention).
+ *
+ * Conventions for every call:
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current CUDA device; the caller owns them. Host pointers are named so.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls enqueue work on it and return without waiting, except where stated.
+ *  - Return value: ICE_OK (0) or a negative ICE_ERR_* code. Argument errors
+ *    are found on the host before anything is launched. Errors that only the
+ *    GPU can see (a page id out of range, an exhausted capacity, a timed-out
+ *    wait) are recorded in a per-index device status word that
+ *    ice_get_error() returns; kernels never trap.
+ *  - Element type of keys, values, queries and outputs is the index's dtype
+ *    (ICE_BF16 or ICE_F32); rows of d elements are contiguous.
+ */
+#ifndef ICE_H_
+#define ICE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define ICE_OK 0
+#define ICE_ERR_INVALID_ARG (-1) /* bad argument; nothing was launched          */
+#define ICE_ERR_CAPACITY (-2)    /* token / page / leaf capacity exhausted        */
+#define ICE_ERR_CUDA (-3)        /* a CUDA runtime call failed                    */
+#define ICE_ERR_TIMEOUT (-4)     /* a bounded device wait ran out                 */
+#define ICE_ERR_BOUNDS (-5)      /* a page id or count given to a kernel is bad   */
+#define ICE_ERR_UNSUPPORTED (-6) /* valid request this build does not implement  */
+
+/* ---- element types ----------------------------------------------------- */
+#define ICE_F32 0
+#define ICE_BF16 1
+
+typedef struct ice_index ice_index; /* opaque; owns the page pool and the index */
+
+/* Shape and method parameters of an index. */
+typedef struct ice_params {
+    int32_t d;           /* head dimension; this build supports 128                  */
+    int32_t n_kv_heads;  /* KV heads per layer (>= 1)                                */
+    int32_t n_q_heads;   /* query heads per layer, a multiple of n_kv_heads; G <= 8  */
+    int32_t n_layers;    /* layers (>= 1)                                            */
+    int32_t batch;       /* sequences (>= 1)                                         */
+    int32_t page_size;   /* P: tokens per page = leaf capacity, 1..64                */
+    int32_t n_proj;      /* m: projections per composite index; must be 8            */
+    int32_t n_composite; /* L: composite indices, 1..2                               */
+    int32_t n_cand;      /* candidates taken per composite; 0 = the token budget     */
+    int32_t dtype;       /* ICE_BF16 or ICE_F32                                      */
+    int64_t max_tokens;  /* token capacity per unit (>= n_tokens of ice_build)       */
+    uint64_t seed;       /* seed of the random projection directions (splitmix64)    */
+} ice_params;
+
+/*
+ * ice_build - index the prefill keys and values (Figure 2 step 1, Figure 3).
+ *
+ * keys, values: device, [batch][n_layers][n_kv_heads][n_tokens][d], dtype.
+ * For each unit: squared key norms set the scale c = 2^e (smallest power of
+ * two with c^2 >= max ||k||^2, frozen for later inserts); each key is mapped to
+ * k~ = [k / c, sqrt(1 - ||k||^2 / c^2)] and projected on the L*m random +-1/16
+ * directions; the 8-bit codes are Morton-interleaved into a 64-bit key, the
+ * token index breaks ties, and the keys are sorted. A binary trie over these
+ * 96-bit keys splits every node that holds more than P tokens; its non-empty
+ * leaves are the leaves of each composite, and the leaves of composite 0 are
+ * the physical pages (ids 0.. left to right), into which K and V are copied.
+ * The library keeps its own copy of K and V; the inputs may be reused as soon
+ * as the call returns.
+ *
+ * This call waits for its stream once (to size the page pool from the leaf
+ * counts) and returns with the build complete. On success *out receives a new
+ * handle that the caller releases with ice_destroy.
+ */
+int ice_build(const ice_params* params, const void* keys, const void* values, int64_t n_tokens,
+              void* stream, ice_index** out);
+
+/*
+ * ice_insert - add one generated token to every unit without a rebuild
+ * (abstract: "dynamically updatable").
+ *
+ * k, v: device, [batch][n_layers][n_kv_heads][d], dtype. The token gets index
+ * n (the unit's current token count). Its key is transformed with the frozen
+ * scale, then in each composite it is appended to the leaf whose prefix it
+ * carries; a leaf that would exceed P splits in two (the left part keeps the
+ * page id, the right part takes the next free id); a key that falls where no
+ * leaf exists opens a new leaf with the next free id. The result equals a
+ * fresh build of all tokens with the same scale.
+ * Returns ICE_ERR_CAPACITY if the units already hold max_tokens tokens.
+ */
+int ice_insert(ice_index* ix, const void* k, const void* v, void* stream);
+
+/*
+ * ice_select - the prioritised query: pages holding the query's top keys
+ * (Figure 2 steps 2-3).
+ *
+ * q: device, [batch][n_layers][n_q_heads][d], dtype.
+ * token_budget: T, a multiple of page_size with T >= page_size; n_sel = T / P
+ *   pages are selected per unit.
+ * page_ids: device int32 [units][n_sel]; receives the selected page ids in
+ *   selection order, -1 after the last one.
+ * n_pages: device int32 [units]; receives the number of pages selected (< n_sel
+ *   only when the candidates span fewer pages).
+ * stats: device int32 [units][4] or NULL. When given: [0] leaf records scanned
+ *   (all composites), [1] distinct candidate keys rescored, [2] tokens in the
+ *   selected pages, [3] candidate tokens taken before de-duplication.
+ *
+ * Per unit: the group's query heads are summed in fp32 (q_sel), normalised and
+ * projected to codes; in each composite the leaves are taken in increasing
+ * (L-infinity code distance to the leaf's cell, position) order until n_cand
+ * tokens are collected; the union of those tokens is rescored exactly with a
+ * fixed-order fp32 dot q_sel . k, ranked by (score desc, token asc), and the
+ * pages of the ranked tokens are taken in first-occurrence order.
+ */
+int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
+               int32_t* n_pages, int32_t* stats, void* stream);
+
+/*
+ * ice_sparse_attn - attention of each query head over every token of the
+ * selected pages (Figure 2 step 3).
+ *
+ * q: device, [batch][n_layers][n_q_heads][d], dtype.
+ * page_ids: device int32 [units][page_stride]; n_pages: device int32 [units],
+ *   0 <= n_pages[u] <= page_stride (as written by ice_select).
+ * out: device, [batch][n_layers][n_q_heads][d], dtype. For query head g of
+ *   unit u: out = sum_t softmax_t(q . k_t / sqrt(d)) v_t over the tokens t of
+ *   the pages (fp32 accumulation). A unit with no pages gets zeros.
+ * Page ids outside the unit's allocated range are skipped and reported as
+ * ICE_ERR_BOUNDS through ice_get_error().
+ */
+int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const int32_t* n_pages,
+                    int32_t page_stride, void* out, void* stream);
+
+/*
+ * ice_get_error - waits for `stream`, then returns and clears the index's
+ * device status word (ICE_OK if no kernel reported an error).
+ */
+int ice_get_error(ice_index* ix, void* stream);
+
+/* ice_destroy - waits for the device, then frees everything the handle owns. */
+void ice_destroy(ice_index* ix);
+
+/* ice_status_string - static text for a status code. */
+const char* ice_status_string(int status);
+
+/* Host-side facts about an index. */
+typedef struct ice_info {
+    int64_t n_units;       /* batch * n_layers * n_kv_heads                     */
+    int64_t n_tokens;      /* tokens per unit (build + inserts)                 */
+    int64_t max_tokens;    /* token capacity per unit                           */
+    int64_t list_capacity; /* leaf / page capacity per unit and composite       */
+    int64_t pool_bytes;    /* device bytes held by the handle                   */
+    int32_t group;         /* G                                                 */
+    int32_t n_composite;   /* L                                                 */
+    int32_t page_size;     /* P                                                 */
+    int32_t dtype;         /* ICE_BF16 / ICE_F32                                */
+} ice_info;
+
+int ice_get_info(const ice_index* ix, ice_info* info);
+
+/*
+ * Debug views (tests only). ice_debug_dump copies the index of one unit to
+ * host memory and waits for the copy. Layout of host_buf, little endian:
+ *   int64 header[16]: L, P, list_capacity C, n_tokens n, e, n_leaf[0..3],
+ *                     next_id[0..3], reserved
+ *   per composite l (repeated L times):
+ *     leaf key   [C] x {uint64 morton_prefix, uint32 token_prefix, uint32 t}
+ *     leaf cell  [C] x {uint8 lo[8], uint8 hi[8]}
+ *     leaf meta  [C] x uint32 (list id << 8 | token count)
+ *     list count [C] x int32 (tokens in list/page id)
+ *     slot token [C][P] x int32 (token of each slot of list/page id)
+ *     slot key   [C][P] x uint64 (Morton key of that token)
+ *   token location [max_tokens] x int32 (page id * P + slot, composite 0)
+ * Only the first n_leaf[l] leaf records and the first next_id[l] lists are
+ * meaningful. Returns the byte size required when host_buf is NULL or cap is
+ * too small (as a positive number), ICE_OK after a copy, or an error.
+ */
+int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap, void* stream);
+
+/* Copies page `page_id` of unit `unit` (P rows of K and of V, dtype) to host
+ * buffers of P*d elements each and waits for the copy. */
+int ice_debug_page(ice_index* ix, int32_t unit, int32_t page_id, void* host_k, void* host_v,
+                   void* stream);
+
+/* Test hook: flag bit 0 makes ice_sparse_attn wait on a barrier nothing
+ * signals, so that its bounded wait runs out and ICE_ERR_TIMEOUT is reported.
+ * 0 restores normal operation. */
+int ice_debug_set_flags(ice_index* ix, int32_t flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ICE_H_ */

@@ -1,0 +1,354 @@
+// C ABI of libice.so: argument checks, memory ownership and launch order.
+// See include/ice.h for the contract of each call.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "ice_internal.cuh"
+
+
+using namespace ice;
+
+struct ice_index {
+    ice_params p;
+    int U = 0, G = 0;
+    long long C = 0;
+    long long n_tok = 0;
+    size_t bytes = 0;
+    int device = 0;
+    std::vector<void*> owned;
+    IndexView v;
+};
+
+namespace {
+
+// splitmix64 (Steele, Lea & Flood 2014), the generator of the directions.
+uint64_t sm64(uint64_t& s) {
+    s += 0x9E3779B97F4A7C15ULL;
+    uint64_t z = s;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+int check_params(const ice_params* p) {
+    if (!p) return ICE_ERR_INVALID_ARG;
+    if (p->d != kD || p->n_proj != kM) return ICE_ERR_UNSUPPORTED;
+    if (p->n_kv_heads < 1 || p->n_layers < 1 || p->batch < 1) return ICE_ERR_INVALID_ARG;
+    if (p->n_q_heads < p->n_kv_heads || p->n_q_heads % p->n_kv_heads) return ICE_ERR_INVALID_ARG;
+    const int G = p->n_q_heads / p->n_kv_heads;
+    if (!(G == 1 || G == 2 || G == 4 || G == 8)) return ICE_ERR_UNSUPPORTED;
+    if (p->page_size < 1 || p->page_size > kMaxP) return ICE_ERR_INVALID_ARG;
+    if (p->n_composite < 1 || p->n_composite > kMaxL) return ICE_ERR_INVALID_ARG;
+    if (p->n_cand < 0) return ICE_ERR_INVALID_ARG;
+    if (p->dtype != ICE_F32 && p->dtype != ICE_BF16) return ICE_ERR_INVALID_ARG;
+    if (p->max_tokens < 0 || p->max_tokens > (1LL << 30)) return ICE_ERR_INVALID_ARG;
+    const long long units = (long long)p->batch * p->n_layers * p->n_kv_heads;
+    if (units > (1LL << 24)) return ICE_ERR_INVALID_ARG;
+    return ICE_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+template <typename T>
+cudaError_t dev_alloc(ice_index* ix, T** out, size_t count) {
+    void* p = nullptr;
+    const size_t bytes = std::max<size_t>(count * sizeof(T), 16);
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) return e;
+    ix->owned.push_back(p);
+    ix->bytes += bytes;
+    *out = reinterpret_cast<T*>(p);
+    return cudaSuccess;
+}
+
+void free_all(ice_index* ix) {
+    for (void* p : ix->owned) cudaFree(p);
+    ix->owned.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ice_status_string(int s) {
+    switch (s) {
+        case ICE_OK: return "ok";
+        case ICE_ERR_INVALID_ARG: return "invalid argument";
+        case ICE_ERR_CAPACITY: return "capacity exhausted";
+        case ICE_ERR_CUDA: return "CUDA runtime error";
+        case ICE_ERR_TIMEOUT: return "bounded device wait timed out";
+        case ICE_ERR_BOUNDS: return "page id or page count out of range";
+        case ICE_ERR_UNSUPPORTED: return "unsupported parameters";
+        default: return "unknown status";
+    }
+}
+
+int ice_build(const ice_params* params, const void* keys, const void* values, int64_t n_tokens,
+              void* stream, ice_index** out) {
+    if (!out) return ICE_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = check_params(params);
+    if (rc) return rc;
+    if (n_tokens < 0 || n_tokens > params->max_tokens || n_tokens > (1LL << 30))
+        return ICE_ERR_INVALID_ARG;
+    if (n_tokens > 0 && (!keys || !values || !aligned16(keys) || !aligned16(values)))
+        return ICE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    ice_index* ix = new (std::nothrow) ice_index();
+    if (!ix) return ICE_ERR_CUDA;
+    ix->p = *params;
+    if (ix->p.n_cand == 0) ix->p.n_cand = 0;  // resolved per select call (budget)
+    ix->U = params->batch * params->n_layers * params->n_kv_heads;
+    ix->G = params->n_q_heads / params->n_kv_heads;
+    ix->n_tok = n_tokens;
+    cudaGetDevice(&ix->device);
+    const int U = ix->U, L = params->n_composite, P = params->page_size;
+    const long long n = n_tokens;
+    IndexView& v = ix->v;
+    std::memset(&v, 0, sizeof(v));
+    v.U = U;
+    v.L = L;
+    v.P = P;
+    v.G = ix->G;
+    v.dtype = params->dtype;
+    v.max_tokens = std::max<long long>(1, params->max_tokens);
+
+    // directions, on the host from splitmix64(seed): sign bit -> -1/16, else +1/16
+    std::vector<float> dirs((size_t)L * kM * kDirStride, 0.0f);
+    {
+        uint64_t s = params->seed;
+        for (int l = 0; l < L; ++l)
+            for (int j = 0; j < kM; ++j)
+                for (int i = 0; i <= kD; ++i)
+                    dirs[((size_t)l * kM + j) * kDirStride + i] = (sm64(s) >> 63) ? -0.0625f : 0.0625f;
+    }
+    cudaError_t e = cudaSuccess;
+    float* d_dirs = nullptr;
+    int* d_status = nullptr;
+    int* d_e = nullptr;
+    if ((e = dev_alloc(ix, &d_dirs, dirs.size())) != cudaSuccess) goto fail;
+    if ((e = dev_alloc(ix, &d_status, 1)) != cudaSuccess) goto fail;
+    if ((e = dev_alloc(ix, &d_e, (size_t)U)) != cudaSuccess) goto fail;
+    if ((e = cudaMemcpyAsync(d_dirs, dirs.data(), dirs.size() * sizeof(float),
+                             cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        goto fail;
+    if ((e = cudaMemsetAsync(d_status, 0, sizeof(int), st)) != cudaSuccess) goto fail;
+    if ((e = cudaMemsetAsync(d_e, 0, sizeof(int) * U, st)) != cudaSuccess) goto fail;
+    v.dirs = d_dirs;
+    v.status = d_status;
+    v.e_unit = d_e;
+    {
+        BuildScratch s;
+        std::vector<int> nleaf((size_t)L * U, 0);
+        int cur = 0;
+        if (n > 0) {
+            if ((e = scratch_alloc(s, U, L, n, st)) != cudaSuccess) {
+                scratch_free(s, st);
+                goto fail;
+            }
+            e = build_phase1(params->dtype, keys, U, L, P, n, d_dirs, d_e, s, st, &cur);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(nleaf.data(), s.nleaf, sizeof(int) * L * U,
+                                    cudaMemcpyDeviceToHost, st);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) {
+                scratch_free(s, st);
+                goto fail;
+            }
+        }
+        // list capacity: the largest leaf count plus one new leaf per future insert
+        long long mx = 0;
+        for (int x : nleaf) mx = std::max<long long>(mx, x);
+        ix->C = std::max<long long>(1, mx + (v.max_tokens - n));
+        if (ix->C >= (1LL << 24) || ix->C * P > (1LL << 31) - 1) {
+            scratch_free(s, st);
+            free_all(ix);
+            delete ix;
+            return ICE_ERR_CAPACITY;
+        }
+        v.C = ix->C;
+        const long long C = ix->C;
+        const size_t es = params->dtype == ICE_BF16 ? 2 : 4;
+        bool okc = true;
+        okc = okc && dev_alloc(ix, &v.leaf_key, (size_t)U * L * C) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.leaf_cell, (size_t)U * L * C) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.leaf_meta, (size_t)U * L * C) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.n_leaf, (size_t)U * L) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.next_id, (size_t)U * L) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.list_cnt, (size_t)U * L * C) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.slot_tok, (size_t)U * L * C * P) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.slot_key, (size_t)U * L * C * P) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.tok_loc, (size_t)U * v.max_tokens) == cudaSuccess;
+        unsigned char* pk = nullptr;
+        unsigned char* pv = nullptr;
+        okc = okc && dev_alloc(ix, &pk, (size_t)U * C * P * kD * es) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &pv, (size_t)U * C * P * kD * es) == cudaSuccess;
+        if (!okc) {
+            scratch_free(s, st);
+            cudaGetLastError();
+            free_all(ix);
+            delete ix;
+            return ICE_ERR_CAPACITY;
+        }
+        v.page_k = pk;
+        v.page_v = pv;
+        e = cudaMemsetAsync(v.n_leaf, 0, sizeof(int) * U * L, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(v.next_id, 0, sizeof(int) * U * L, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(v.list_cnt, 0, sizeof(int) * U * L * C, st);
+        if (e == cudaSuccess)  // -1: token not placed yet
+            e = cudaMemsetAsync(v.tok_loc, 0xFF, sizeof(int) * U * v.max_tokens, st);
+        if (e == cudaSuccess && n > 0) e = build_phase2(v, keys, values, n, s, cur, st);
+        scratch_free(s, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) goto fail;
+    }
+    *out = ix;
+    return ICE_OK;
+fail:
+    cudaGetLastError();
+    free_all(ix);
+    delete ix;
+    return ICE_ERR_CUDA;
+}
+
+int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
+    if (!ix || !k || !v || !aligned16(k) || !aligned16(v)) return ICE_ERR_INVALID_ARG;
+    if (ix->n_tok >= ix->v.max_tokens) return ICE_ERR_CAPACITY;
+    cudaError_t e = launch_insert(ix->v, k, v, ix->n_tok, (cudaStream_t)stream);
+    if (e != cudaSuccess) return ICE_ERR_CUDA;
+    ix->n_tok += 1;
+    return ICE_OK;
+}
+
+int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
+               int32_t* n_pages, int32_t* stats, void* stream) {
+    if (!ix || !q || !page_ids || !n_pages || !aligned16(q)) return ICE_ERR_INVALID_ARG;
+    const int P = ix->p.page_size;
+    if (token_budget < P || token_budget % P) return ICE_ERR_INVALID_ARG;
+    const int n_sel = token_budget / P;
+    if (n_sel > 512) return ICE_ERR_UNSUPPORTED;
+    const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
+    if (n_cand > (1 << 16)) return ICE_ERR_UNSUPPORTED;
+    if (select_smem_bytes(ix->C, ix->p.n_composite, P, n_cand) > 200 * 1024)
+        return ICE_ERR_UNSUPPORTED;
+    cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, stats,
+                                  (cudaStream_t)stream);
+    return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
+}
+
+int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const int32_t* n_pages,
+                    int32_t page_stride, void* out, void* stream) {
+    if (!ix || !q || !page_ids || !n_pages || !out || !aligned16(q) || !aligned16(out))
+        return ICE_ERR_INVALID_ARG;
+    if (page_stride < 1 || page_stride > 512) return ICE_ERR_INVALID_ARG;
+    const size_t es = ix->p.dtype == ICE_BF16 ? 2 : 4;
+    const int ppc = attn_pages_per_cta(page_stride);
+    if ((size_t)2 * ppc * ix->p.page_size * kD * es > 200 * 1024) return ICE_ERR_UNSUPPORTED;
+    cudaError_t e = launch_attn(ix->v, q, page_ids, n_pages, page_stride, out, (cudaStream_t)stream);
+    return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
+}
+
+int ice_get_error(ice_index* ix, void* stream) {
+    if (!ix) return ICE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return ICE_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, ix->v.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ICE_ERR_CUDA;
+    if (h != 0 && cudaMemset(ix->v.status, 0, sizeof(int)) != cudaSuccess) return ICE_ERR_CUDA;
+    return h;
+}
+
+void ice_destroy(ice_index* ix) {
+    if (!ix) return;
+    cudaDeviceSynchronize();
+    free_all(ix);
+    delete ix;
+}
+
+int ice_get_info(const ice_index* ix, ice_info* info) {
+    if (!ix || !info) return ICE_ERR_INVALID_ARG;
+    info->n_units = ix->U;
+    info->n_tokens = ix->n_tok;
+    info->max_tokens = ix->v.max_tokens;
+    info->list_capacity = ix->C;
+    info->pool_bytes = (int64_t)ix->bytes;
+    info->group = ix->G;
+    info->n_composite = ix->p.n_composite;
+    info->page_size = ix->p.page_size;
+    info->dtype = ix->p.dtype;
+    return ICE_OK;
+}
+
+int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap, void* stream) {
+    if (!ix || unit < 0 || unit >= ix->U) return ICE_ERR_INVALID_ARG;
+    const int L = ix->p.n_composite, P = ix->p.page_size;
+    const long long C = ix->C;
+    const int64_t per_l = C * 16 + C * 16 + C * 4 + C * 4 + C * P * 4 + C * P * 8;
+    const int64_t need = 16 * 8 + L * per_l + ix->v.max_tokens * 4;
+    if (!host_buf || cap < need) return need;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return ICE_ERR_CUDA;
+    const IndexView& v = ix->v;
+    int64_t hdr[16] = {0};
+    hdr[0] = L;
+    hdr[1] = P;
+    hdr[2] = C;
+    hdr[3] = ix->n_tok;
+    int e = 0, nl[kMaxL] = {0, 0}, ni[kMaxL] = {0, 0};
+    bool ok = cudaMemcpy(&e, v.e_unit + unit, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess;
+    ok = ok && cudaMemcpy(nl, v.n_leaf + (long long)unit * L, sizeof(int) * L,
+                          cudaMemcpyDeviceToHost) == cudaSuccess;
+    ok = ok && cudaMemcpy(ni, v.next_id + (long long)unit * L, sizeof(int) * L,
+                          cudaMemcpyDeviceToHost) == cudaSuccess;
+    hdr[4] = e;
+    for (int l = 0; l < L; ++l) {
+        hdr[5 + l] = nl[l];
+        hdr[9 + l] = ni[l];
+    }
+    char* o = (char*)host_buf;
+    std::memcpy(o, hdr, sizeof(hdr));
+    o += sizeof(hdr);
+    for (int l = 0; l < L && ok; ++l) {
+        const long long lb = v.leaf_base(unit, l), sb = v.slot_base(unit, l);
+        ok = ok && cudaMemcpy(o, v.leaf_key + lb, C * 16, cudaMemcpyDeviceToHost) == cudaSuccess;
+        o += C * 16;
+        ok = ok && cudaMemcpy(o, v.leaf_cell + lb, C * 16, cudaMemcpyDeviceToHost) == cudaSuccess;
+        o += C * 16;
+        ok = ok && cudaMemcpy(o, v.leaf_meta + lb, C * 4, cudaMemcpyDeviceToHost) == cudaSuccess;
+        o += C * 4;
+        ok = ok && cudaMemcpy(o, v.list_cnt + lb, C * 4, cudaMemcpyDeviceToHost) == cudaSuccess;
+        o += C * 4;
+        ok = ok && cudaMemcpy(o, v.slot_tok + sb, C * P * 4, cudaMemcpyDeviceToHost) == cudaSuccess;
+        o += C * P * 4;
+        ok = ok && cudaMemcpy(o, v.slot_key + sb, C * P * 8, cudaMemcpyDeviceToHost) == cudaSuccess;
+        o += C * P * 8;
+    }
+    ok = ok && cudaMemcpy(o, v.tok_loc + (long long)unit * v.max_tokens, v.max_tokens * 4,
+                          cudaMemcpyDeviceToHost) == cudaSuccess;
+    return ok ? ICE_OK : ICE_ERR_CUDA;
+}
+
+int ice_debug_page(ice_index* ix, int32_t unit, int32_t page_id, void* host_k, void* host_v,
+                   void* stream) {
+    if (!ix || unit < 0 || unit >= ix->U || page_id < 0 || page_id >= ix->C || !host_k || !host_v)
+        return ICE_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ICE_ERR_CUDA;
+    const size_t es = ix->p.dtype == ICE_BF16 ? 2 : 4;
+    const size_t bytes = (size_t)ix->p.page_size * kD * es;
+    const size_t off = (size_t)ix->v.page_row(unit, page_id, 0) * kD * es;
+    bool ok = cudaMemcpy(host_k, (char*)ix->v.page_k + off, bytes, cudaMemcpyDeviceToHost) == cudaSuccess;
+    ok = ok && cudaMemcpy(host_v, (char*)ix->v.page_v + off, bytes, cudaMemcpyDeviceToHost) == cudaSuccess;
+    return ok ? ICE_OK : ICE_ERR_CUDA;
+}
+
+int ice_debug_set_flags(ice_index* ix, int32_t flags) {
+    if (!ix) return ICE_ERR_INVALID_ARG;
+    ix->v.debug_flags = flags;
+    return ICE_OK;
+}
+
+}  // extern "C"

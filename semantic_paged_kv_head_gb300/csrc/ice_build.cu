@@ -1,0 +1,521 @@
+// Prefill build of the DCI-tree page index ("IceCache", Figure 2 step 1 and
+// Figure 3): transform + projection + quantisation of every key, a segmented
+// radix sort of the 96-bit keys, the trie leaves (split while a node holds
+// more than P tokens), and the packing of K/V rows into the physical pages.
+//
+// Every unit (sequence, layer, KV head) is an independent segment; all units
+// are processed by the same launches.
+#include <algorithm>
+#include <vector>
+
+#include "ice_internal.cuh"
+
+namespace ice {
+
+// ---------------------------------------------------------------------------
+// K1a: squared norm of every key with the fixed-order dot, and the per-unit
+// maximum (non-negative floats order like their bit patterns).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) norms_kernel(const T* __restrict__ keys, long long total,
+                                                   long long n, float* __restrict__ nrm2,
+                                                   unsigned int* __restrict__ umax) {
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    float r = 0.0f;
+    if (i < total) {
+        const T* row = keys + i * kD;
+        float acc[32];
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+            float v[4];
+            load4_nc(row + 4 * l, v);
+            float s = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) s = __fmaf_rn(v[k], v[k], s);
+            acc[l] = s;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+            for (int l = 0; l < o; ++l) acc[l] = __fadd_rn(acc[l], acc[l + o]);
+        r = acc[0];
+        nrm2[i] = r;
+    }
+    // one atomic per warp and unit: lanes of a warp may straddle two units
+    long long u = i < total ? i / n : -1;
+    long long u0 = __shfl_sync(0xffffffffu, u, 0);
+    bool same = __all_sync(0xffffffffu, u == u0);
+    if (same) {
+        float m = r;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0 && u0 >= 0) atomicMax(&umax[u0], __float_as_uint(m));
+    } else if (i < total) {
+        atomicMax(&umax[u], __float_as_uint(r));
+    }
+}
+
+// Smallest e with 4^e >= maxn (e >= -60); 0 when maxn == 0.
+__device__ __forceinline__ int scale_exponent_dev(float maxn) {
+    if (!(maxn > 0.0f)) return 0;
+    int x;
+    float f = frexpf(maxn, &x);  // maxn = f * 2^x, f in [0.5, 1)
+    int need = (f == 0.5f) ? x - 1 : x;  // 2e >= need
+    int e = need >= 0 ? (need + 1) / 2 : -((-need) / 2);
+    return e < -60 ? -60 : e;
+}
+
+__global__ void exponent_kernel(const unsigned int* __restrict__ umax, int* __restrict__ e_unit,
+                                int U) {
+    int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u < U) e_unit[u] = scale_exponent_dev(__uint_as_float(umax[u]));
+}
+
+// ---------------------------------------------------------------------------
+// K1b: transformed key k~ = [k 2^-e, sqrt(max(0, 1 - |k|^2 2^-2e))], its
+// projections p = fma(u[d], tail, D(u[0:d], k~[0:d])) on the L*8 directions,
+// 8-bit codes and the Morton key per composite. One thread per (token,
+// direction); the token rows are staged in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kProjThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kProjThreads) project_kernel(
+    const T* __restrict__ keys, const float* __restrict__ nrm2, const int* __restrict__ e_unit,
+    const float* __restrict__ dirs, int L, long long n, int tiles_per_unit,
+    unsigned long long* __restrict__ mk_out, int* __restrict__ tok_out, int U) {
+    const int ndir = L * kM;
+    const int tpb = kProjThreads / ndir;  // tokens per block
+    __shared__ __align__(16) float kt[kProjThreads / kM][kD + 4];
+    __shared__ float tail[kProjThreads / kM];
+    __shared__ int codes[kProjThreads / kM][kMaxL * kM];
+    const int u = blockIdx.x / tiles_per_unit;
+    const long long t0 = (long long)(blockIdx.x % tiles_per_unit) * tpb;
+    const int e = e_unit[u];
+    const float sc = ldexpf(1.0f, -e);
+    const float sc2 = ldexpf(1.0f, -2 * e);
+    // stage k~ rows: 4 elements per thread per step
+    for (int idx = threadIdx.x; idx < tpb * (kD / 4); idx += blockDim.x) {
+        int r = idx / (kD / 4), c = (idx % (kD / 4)) * 4;
+        long long t = t0 + r;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < n) load4_nc(keys + ((long long)u * n + t) * kD + c, v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) kt[r][c + k] = __fmul_rn(v[k], sc);
+    }
+    if (threadIdx.x < tpb) {
+        long long t = t0 + threadIdx.x;
+        float r = 0.0f;
+        if (t < n) {
+            r = __fsub_rn(1.0f, __fmul_rn(nrm2[(long long)u * n + t], sc2));
+            r = r > 0.0f ? r : 0.0f;
+        }
+        tail[threadIdx.x] = __fsqrt_rn(r);
+    }
+    __syncthreads();
+    const int r = threadIdx.x / ndir, dir = threadIdx.x % ndir;
+    if (r < tpb) {
+        const float* ud = dirs + (long long)dir * kDirStride;
+        float acc[32];
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+            float4 x = *reinterpret_cast<const float4*>(&kt[r][4 * l]);
+            float4 w = __ldg(reinterpret_cast<const float4*>(ud + 4 * l));
+            float s = 0.0f;
+            s = __fmaf_rn(w.x, x.x, s);
+            s = __fmaf_rn(w.y, x.y, s);
+            s = __fmaf_rn(w.z, x.z, s);
+            s = __fmaf_rn(w.w, x.w, s);
+            acc[l] = s;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+            for (int l = 0; l < o; ++l) acc[l] = __fadd_rn(acc[l], acc[l + o]);
+        float p = __fmaf_rn(ud[kD], tail[r], acc[0]);
+        codes[r][dir] = quantise_code(p);
+    }
+    __syncthreads();
+    if (threadIdx.x < tpb * L) {
+        int rr = threadIdx.x / L, l = threadIdx.x % L;
+        long long t = t0 + rr;
+        if (t < n) {
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = codes[rr][l * kM + j];
+            long long o = ((long long)l * U + u) * n + t;
+            mk_out[o] = morton8(c);
+            tok_out[o] = (int)t;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K2: stable LSD radix sort of (Morton key, token) within each segment
+// (composite, unit), 8 bits per pass. Input order is ascending token, so equal
+// Morton keys stay in token order and the result is sorted by the 96-bit key.
+// ---------------------------------------------------------------------------
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 8;
+constexpr int kSortTile = kSortThreads * kSortItems;
+
+__global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(
+    const unsigned long long* __restrict__ keys, long long n, int tiles, int shift,
+    int* __restrict__ hist) {
+    __shared__ int h[256];
+    const int seg = blockIdx.x / tiles, tile = blockIdx.x % tiles;
+    h[threadIdx.x] = 0;
+    __syncthreads();
+    const long long base = (long long)seg * n + (long long)tile * kSortTile;
+    const long long lim = min((long long)kSortTile, n - (long long)tile * kSortTile);
+    for (int i = threadIdx.x; i < lim; i += kSortThreads)
+        atomicAdd(&h[(int)((keys[base + i] >> shift) & 0xFF)], 1);
+    __syncthreads();
+    hist[((long long)seg * 256 + threadIdx.x) * tiles + tile] = h[threadIdx.x];
+}
+
+// Per segment: offsets[seg][digit][tile] = segment start + (all smaller
+// digits) + (same digit in earlier tiles).
+__global__ void __launch_bounds__(256) radix_scan_kernel(int* __restrict__ hist, long long n,
+                                                         int tiles) {
+    __shared__ int tot[256];
+    const int seg = blockIdx.x, dgt = threadIdx.x;
+    int* row = hist + ((long long)seg * 256 + dgt) * tiles;
+    int s = 0;
+    for (int t = 0; t < tiles; ++t) s += row[t];
+    tot[dgt] = s;
+    __syncthreads();
+    if (dgt == 0) {
+        int run = 0;
+        for (int k = 0; k < 256; ++k) {
+            int x = tot[k];
+            tot[k] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    int run = tot[dgt];
+    for (int t = 0; t < tiles; ++t) {
+        int x = row[t];
+        row[t] = run;
+        run += x;
+    }
+}
+
+__global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
+    const unsigned long long* __restrict__ kin, const int* __restrict__ vin,
+    unsigned long long* __restrict__ kout, int* __restrict__ vout, long long n, int tiles,
+    int shift, const int* __restrict__ offs) {
+    constexpr int W = kSortThreads / 32;
+    __shared__ int running[256];
+    __shared__ int base_off[256];
+    __shared__ int wcnt[W][256];
+    const int seg = blockIdx.x / tiles, tile = blockIdx.x % tiles;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    running[threadIdx.x] = 0;
+    base_off[threadIdx.x] = offs[((long long)seg * 256 + threadIdx.x) * tiles + tile];
+    const long long seg0 = (long long)seg * n;
+    const long long base = seg0 + (long long)tile * kSortTile;
+    const long long lim = min((long long)kSortTile, n - (long long)tile * kSortTile);
+    const unsigned int lt = (1u << lane) - 1u;
+    // Items are taken in tile order, one round of kSortThreads at a time; within
+    // a round, warp w precedes warp w+1 and lane order is kept by match_any.
+    for (int r = 0; r < kSortItems; ++r) {
+        for (int w = 0; w < W; ++w) wcnt[w][threadIdx.x] = 0;
+        __syncthreads();
+        const int i = r * kSortThreads + threadIdx.x;
+        const bool ok = i < lim;
+        const unsigned long long k = ok ? kin[base + i] : 0ull;
+        const int val = ok ? vin[base + i] : 0;
+        const int dgt = ok ? (int)((k >> shift) & 0xFF) : 256;
+        const unsigned int peers = __match_any_sync(0xffffffffu, dgt);
+        const int rank = __popc(peers & lt);
+        if (ok && rank == 0) wcnt[warp][dgt] = __popc(peers);
+        __syncthreads();
+        int round_total = 0;  // items of digit threadIdx.x in this round
+        for (int w = 0; w < W; ++w) {
+            int x = wcnt[w][threadIdx.x];
+            wcnt[w][threadIdx.x] = round_total;
+            round_total += x;
+        }
+        __syncthreads();
+        if (ok) {
+            long long pos = seg0 + base_off[dgt] + running[dgt] + wcnt[warp][dgt] + rank;
+            kout[pos] = k;
+            vout[pos] = val;
+        }
+        __syncthreads();
+        running[threadIdx.x] += round_total;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K3a: trie leaves of each sorted segment. With a_j = lcp(key_j, key_{j+1}),
+// the node of depth t around position i holds <= P keys iff every window of
+// P+1 consecutive keys containing i has lcp < t, so the leaf depth of i is
+// t_i = 1 + max over such windows of min(a_s .. a_{s+P-1}) (0 when n <= P),
+// and i starts a leaf iff i == 0 or a_{i-1} < t_i.
+// One block per segment walks it in chunks and numbers the leaves.
+// ---------------------------------------------------------------------------
+constexpr int kLeafThreads = 512;
+
+__global__ void __launch_bounds__(kLeafThreads) leaf_scan_kernel(
+    const unsigned long long* __restrict__ mk, const int* __restrict__ tok, long long n, int P,
+    int* __restrict__ leaf_of, int* __restrict__ leaf_start, unsigned char* __restrict__ tdepth,
+    int* __restrict__ nleaf_out) {
+    constexpr int B = kLeafThreads;
+    __shared__ unsigned char a[B + 2 * kMaxP + 2];   // adjacent lcps around the chunk
+    __shared__ unsigned char wmin[B + kMaxP + 2];    // window minima
+    __shared__ int scan[B / 32];
+    __shared__ int carry;
+    const int seg = blockIdx.x;
+    const long long s0 = (long long)seg * n;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (long long c0 = 0; c0 < n; c0 += B) {
+        // adjacent lcps a_j for j in [c0 - P - 1, c0 + B + P)
+        const long long j0 = c0 - P - 1;
+        const int na = B + 2 * P + 1;
+        for (int x = threadIdx.x; x < na; x += B) {
+            long long j = j0 + x;
+            unsigned char v = 0;
+            if (j >= 0 && j + 1 < n)
+                v = (unsigned char)lcp96(mk[s0 + j], (unsigned)tok[s0 + j], mk[s0 + j + 1],
+                                         (unsigned)tok[s0 + j + 1]);
+            a[x] = v;
+        }
+        __syncthreads();
+        // window minima W_s = min(a_s .. a_{s+P-1}) for s in [c0 - P, c0 + B)
+        const long long w0 = c0 - P;
+        for (int x = threadIdx.x; x < B + P; x += B) {
+            long long s = w0 + x;
+            unsigned char v = 0;
+            if (s >= 0 && s + P <= n - 1) {
+                v = 255;
+                for (int k = 0; k < P; ++k) v = min(v, a[(int)(s + k - j0)]);
+            } else {
+                v = 0;  // window not inside the segment: contributes nothing
+            }
+            wmin[x] = v;
+        }
+        __syncthreads();
+        const long long i = c0 + threadIdx.x;
+        int flag = 0, t = 0;
+        if (i < n) {
+            if (n > P) {
+                int best = -1;
+                for (int k = 0; k <= P; ++k) {
+                    long long s = i - k;
+                    if (s >= 0 && s + P <= n - 1) best = max(best, (int)wmin[(int)(s - w0)]);
+                }
+                t = best + 1;
+            }
+            flag = (i == 0) || ((int)a[(int)(i - 1 - j0)] < t);
+            tdepth[s0 + i] = (unsigned char)t;
+        }
+        // block-wide inclusive scan of flags
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int x = flag;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) scan[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int v = lane < B / 32 ? scan[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            if (lane < B / 32) scan[lane] = v;
+        }
+        __syncthreads();
+        int incl = x + (warp > 0 ? scan[warp - 1] : 0) + carry;
+        if (i < n) {
+            int leaf = incl - 1;
+            leaf_of[s0 + i] = leaf;
+            if (flag) leaf_start[s0 + leaf] = (int)i;
+        }
+        __syncthreads();
+        if (threadIdx.x == B - 1) carry = incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) nleaf_out[seg] = carry;
+}
+
+// ---------------------------------------------------------------------------
+// K3b: leaf records, slot lists and token locations, one thread per sorted
+// position of every segment.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) leaf_write_kernel(
+    IndexView v, const unsigned long long* __restrict__ mk, const int* __restrict__ tok,
+    long long n, const int* __restrict__ leaf_of, const int* __restrict__ leaf_start,
+    const unsigned char* __restrict__ tdepth, const int* __restrict__ nleaf) {
+    long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    long long total = (long long)v.L * v.U * n;
+    if (g >= total) return;
+    const int seg = (int)(g / n);
+    const long long i = g % n;
+    const int l = seg / v.U, u = seg % v.U;
+    const long long s0 = (long long)seg * n;
+    const int leaf = leaf_of[g];
+    const int nl = nleaf[seg];
+    if (leaf >= v.C) {
+        set_status(v.status, ICE_ERR_CAPACITY);
+        return;
+    }
+    const int start = leaf_start[s0 + leaf];
+    const int end = leaf + 1 < nl ? leaf_start[s0 + leaf + 1] : (int)n;
+    const int slot = (int)i - start;
+    if (slot < 0 || slot >= v.P || end - start > v.P) {  // a leaf never exceeds P tokens
+        set_status(v.status, ICE_ERR_BOUNDS);
+        return;
+    }
+    const unsigned long long m = mk[g];
+    const int t = tok[g];
+    const long long sb = v.slot_base(u, l) + (long long)leaf * v.P + slot;
+    v.slot_tok[sb] = t;
+    v.slot_key[sb] = m;
+    if (l == 0) v.tok_loc[(long long)u * v.max_tokens + t] = leaf * v.P + slot;
+    if (slot == 0) {
+        const int depth = tdepth[g];
+        unsigned long long pm;
+        unsigned int pt;
+        prefix96(m, (unsigned)t, depth, pm, pt);
+        const long long lb = v.leaf_base(u, l) + leaf;
+        LeafKey k;
+        k.pm = pm;
+        k.pt = pt;
+        k.t = (unsigned)depth;
+        v.leaf_key[lb] = k;
+        v.leaf_cell[lb] = cell_of_prefix(pm, (unsigned)depth);
+        v.leaf_meta[lb] = ((unsigned)leaf << 8) | (unsigned)(end - start);
+        v.list_cnt[v.leaf_base(u, l) + leaf] = end - start;
+    }
+    if (i == 0) {
+        v.n_leaf[v.ul(u, l)] = nl;
+        v.next_id[v.ul(u, l)] = nl;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K4: copy each token's K and V row into its page slot (16 B per thread).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) pack_kernel(IndexView v, const T* __restrict__ keys,
+                                                   const T* __restrict__ values, long long n) {
+    constexpr int VPR = kD * (int)sizeof(T) / 16;  // 16-byte vectors per row
+    long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    long long total = (long long)v.U * n * VPR;
+    if (g >= total) return;
+    const int c = (int)(g % VPR);
+    const long long row = g / VPR;  // u * n + t
+    const int u = (int)(row / n);
+    const long long t = row % n;
+    const int loc = v.tok_loc[(long long)u * v.max_tokens + t];
+    if (loc < 0 || (long long)loc >= v.C * v.P) return;  // token not placed (reported earlier)
+    const long long dst = ((long long)u * v.C * v.P + loc) * VPR + c;
+    reinterpret_cast<uint4*>(v.page_k)[dst] = __ldg(reinterpret_cast<const uint4*>(keys) + g);
+    reinterpret_cast<uint4*>(v.page_v)[dst] = __ldg(reinterpret_cast<const uint4*>(values) + g);
+}
+
+// ---------------------------------------------------------------------------
+// Host side of the build. Scratch is stream-ordered and released before return.
+// ---------------------------------------------------------------------------
+
+#define ICE_TRY(x)                          \
+    do {                                    \
+        cudaError_t e_ = (x);               \
+        if (e_ != cudaSuccess) return e_;   \
+    } while (0)
+
+// Phase 1: keys -> sorted 96-bit keys and leaf numbering in scratch.
+cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long long n,
+                         const float* dirs, int* e_unit, BuildScratch& s, cudaStream_t st,
+                         int* final_buf) {
+    const long long total = (long long)U * n;
+    const int S = L * U;
+    ICE_TRY(cudaMemsetAsync(s.umax, 0, sizeof(unsigned) * U, st));
+    const int nb = (int)((total + 255) / 256);
+    if (dtype == ICE_BF16)
+        norms_kernel<__nv_bfloat16><<<nb, 256, 0, st>>>((const __nv_bfloat16*)keys, total, n,
+                                                         s.nrm2, s.umax);
+    else
+        norms_kernel<float><<<nb, 256, 0, st>>>((const float*)keys, total, n, s.nrm2, s.umax);
+    ICE_TRY(cudaGetLastError());
+    exponent_kernel<<<(U + 127) / 128, 128, 0, st>>>(s.umax, e_unit, U);
+    ICE_TRY(cudaGetLastError());
+    const int tpb = kProjThreads / (L * kM);
+    const int tiles_u = (int)((n + tpb - 1) / tpb);
+    if (dtype == ICE_BF16)
+        project_kernel<__nv_bfloat16><<<U * tiles_u, kProjThreads, 0, st>>>(
+            (const __nv_bfloat16*)keys, s.nrm2, e_unit, dirs, L, n, tiles_u, s.mk[0], s.tk[0], U);
+    else
+        project_kernel<float><<<U * tiles_u, kProjThreads, 0, st>>>(
+            (const float*)keys, s.nrm2, e_unit, dirs, L, n, tiles_u, s.mk[0], s.tk[0], U);
+    ICE_TRY(cudaGetLastError());
+    const int tiles = (int)((n + kSortTile - 1) / kSortTile);
+    int cur = 0;
+    for (int shift = 0; shift < 64; shift += 8) {
+        radix_hist_kernel<<<S * tiles, kSortThreads, 0, st>>>(s.mk[cur], n, tiles, shift, s.hist);
+        ICE_TRY(cudaGetLastError());
+        radix_scan_kernel<<<S, 256, 0, st>>>(s.hist, n, tiles);
+        ICE_TRY(cudaGetLastError());
+        radix_scatter_kernel<<<S * tiles, kSortThreads, 0, st>>>(s.mk[cur], s.tk[cur], s.mk[cur ^ 1],
+                                                                 s.tk[cur ^ 1], n, tiles, shift,
+                                                                 s.hist);
+        ICE_TRY(cudaGetLastError());
+        cur ^= 1;
+    }
+    *final_buf = cur;
+    leaf_scan_kernel<<<S, kLeafThreads, 0, st>>>(s.mk[cur], s.tk[cur], n, P, s.leaf_of,
+                                                 s.leaf_start, s.tdepth, s.nleaf);
+    return cudaGetLastError();
+}
+
+cudaError_t build_phase2(const IndexView& v, const void* keys, const void* values, long long n,
+                         BuildScratch& s, int cur, cudaStream_t st) {
+    const long long total = (long long)v.L * v.U * n;
+    leaf_write_kernel<<<(int)((total + 255) / 256), 256, 0, st>>>(
+        v, s.mk[cur], s.tk[cur], n, s.leaf_of, s.leaf_start, s.tdepth, s.nleaf);
+    ICE_TRY(cudaGetLastError());
+    const int es = v.dtype == ICE_BF16 ? 2 : 4;
+    const long long vec = (long long)v.U * n * (kD * es / 16);
+    const int nb = (int)((vec + 255) / 256);
+    if (v.dtype == ICE_BF16)
+        pack_kernel<__nv_bfloat16><<<nb, 256, 0, st>>>(v, (const __nv_bfloat16*)keys,
+                                                       (const __nv_bfloat16*)values, n);
+    else
+        pack_kernel<float><<<nb, 256, 0, st>>>(v, (const float*)keys, (const float*)values, n);
+    return cudaGetLastError();
+}
+
+cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st) {
+    const long long SN = (long long)L * U * n;
+    const long long tiles = (n + kSortTile - 1) / kSortTile;
+    ICE_TRY(cudaMallocAsync((void**)&s.nrm2, sizeof(float) * U * n, st));
+    ICE_TRY(cudaMallocAsync((void**)&s.umax, sizeof(unsigned) * U, st));
+    for (int b = 0; b < 2; ++b) {
+        ICE_TRY(cudaMallocAsync((void**)&s.mk[b], sizeof(unsigned long long) * SN, st));
+        ICE_TRY(cudaMallocAsync((void**)&s.tk[b], sizeof(int) * SN, st));
+    }
+    ICE_TRY(cudaMallocAsync((void**)&s.hist, sizeof(int) * L * U * 256 * tiles, st));
+    ICE_TRY(cudaMallocAsync((void**)&s.leaf_of, sizeof(int) * SN, st));
+    ICE_TRY(cudaMallocAsync((void**)&s.leaf_start, sizeof(int) * SN, st));
+    ICE_TRY(cudaMallocAsync((void**)&s.tdepth, SN, st));
+    ICE_TRY(cudaMallocAsync((void**)&s.nleaf, sizeof(int) * L * U, st));
+    return cudaSuccess;
+}
+
+void scratch_free(BuildScratch& s, cudaStream_t st) {
+    void* ptrs[] = {s.nrm2, s.umax, s.mk[0], s.mk[1], s.tk[0], s.tk[1], s.hist, s.leaf_of,
+                    s.leaf_start, s.tdepth, s.nleaf};
+    for (void* p : ptrs)
+        if (p) cudaFreeAsync(p, st);
+    s = BuildScratch();
+}
+
+}  // namespace ice

@@ -1,0 +1,351 @@
+// Dynamic insertion of one generated token per unit ("IceCache" abstract: a
+// hierarchical, dynamically updatable structure; the blog: no rebuild when a
+// new token appears).
+//
+// The trie over 96-bit keys is history independent: a node is a leaf iff its
+// parent holds more than P keys. Adding key x therefore changes only the leaf
+// on x's path:
+//  * x carries the prefix of an existing leaf holding < P tokens: append;
+//  * that leaf holds P tokens: its P+1 keys share exactly lambda = lcp(min, max)
+//    bits, so it splits into the two children at bit lambda (left keeps the
+//    page id, right takes the next free id);
+//  * x carries no leaf prefix: x opens a new leaf one bit below its longest
+//    common prefix with any existing key (its neighbours in key order).
+// One block per unit; composites are handled one after the other.
+#include "ice_internal.cuh"
+
+namespace ice {
+
+constexpr int kInsThreads = 128;
+
+struct InsKey {
+    unsigned long long m;
+    unsigned int t;
+};
+
+// Shift leaf records [from, N) one place to the right (backwards, in chunks).
+__device__ void shift_right(LeafKey* key, uint4* cell, unsigned int* meta, int from, int N) {
+    for (int end = N; end > from; end -= kInsThreads) {
+        const int start = max(from, end - kInsThreads);
+        const int i = start + (int)threadIdx.x;
+        LeafKey k;
+        uint4 c;
+        unsigned int mt = 0;
+        const bool act = i < end;
+        if (act) {
+            k = key[i];
+            c = cell[i];
+            mt = meta[i];
+        }
+        __syncthreads();
+        if (act) {
+            key[i + 1] = k;
+            cell[i + 1] = c;
+            meta[i + 1] = mt;
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const T* __restrict__ knew,
+                                                            const T* __restrict__ vnew, int tok) {
+    constexpr int ROW = kD;  // elements per row
+    extern __shared__ __align__(16) unsigned char smem[];
+    T* rows_k = reinterpret_cast<T*>(smem);                      // [P+1][D]
+    T* rows_v = rows_k + (size_t)(v.P + 1) * ROW;                // [P+1][D]
+    __shared__ unsigned long long s_mk[kMaxL];
+    __shared__ unsigned long long e_m[kMaxP + 1];
+    __shared__ unsigned int e_t[kMaxP + 1];
+    __shared__ int e_slot[kMaxP + 1];  // original slot (P = the new token)
+    __shared__ int s_sorted[kMaxP + 1];
+    __shared__ int s_lo, s_hi, s_cnt, s_abort;
+
+    const int u = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = v.P;
+    const T* kin = knew + (long long)u * kD;
+    const T* vin = vnew + (long long)u * kD;
+
+    // ---- key of the new token: frozen scale, projections, codes (warp 0) ----------
+    if (warp == 0) {
+        float k4[4];
+        load4(kin + 4 * lane, k4);
+        const float nrm2 = warp_dot_fixed(k4, k4);
+        const int e = v.e_unit[u];
+        const float sc = ldexpf(1.0f, -e), sc2 = ldexpf(1.0f, -2 * e);
+        float kt[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kt[i] = __fmul_rn(k4[i], sc);
+        float r = __fsub_rn(1.0f, __fmul_rn(nrm2, sc2));
+        r = r > 0.0f ? r : 0.0f;
+        const float tail = __fsqrt_rn(r);
+        for (int l = 0; l < v.L; ++l) {
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float* ud = v.dirs + (long long)(l * kM + j) * kDirStride;
+                float w[4];
+                load4(ud + 4 * lane, w);
+                const float p = __fmaf_rn(ud[kD], tail, warp_dot_fixed(w, kt));
+                c[j] = quantise_code(p);
+            }
+            if (lane == 0) s_mk[l] = morton8(c);
+        }
+    }
+    if (tid == 0) s_abort = 0;
+    __syncthreads();
+
+    for (int l = 0; l < v.L; ++l) {
+        const unsigned long long xm = s_mk[l];
+        const unsigned int xt = (unsigned)tok;
+        LeafKey* lk = v.leaf_key + v.leaf_base(u, l);
+        uint4* lc = v.leaf_cell + v.leaf_base(u, l);
+        unsigned int* lm = v.leaf_meta + v.leaf_base(u, l);
+        int* cntl = v.list_cnt + v.leaf_base(u, l);
+        int* stok = v.slot_tok + v.slot_base(u, l);
+        unsigned long long* skey = v.slot_key + v.slot_base(u, l);
+        const int N = v.n_leaf[v.ul(u, l)];
+        const int nid = v.next_id[v.ul(u, l)];
+
+        // ---- a = number of leaves whose prefix <= x (k-ary search) --------------------
+        if (tid == 0) {
+            s_lo = 0;
+            s_hi = N;
+        }
+        __syncthreads();
+        int a = -1;
+        while (a < 0) {
+            const int lo = s_lo, hi = s_hi;
+            if (hi - lo <= kInsThreads) {
+                const int i = lo + tid;
+                bool le = false;
+                if (i < hi) {
+                    const LeafKey k = lk[i];
+                    le = !key_less(xm, xt, k.pm, k.pt);
+                }
+                a = lo + __syncthreads_count(le);
+                break;
+            }
+            const int step = (hi - lo + kInsThreads - 1) / kInsThreads;
+            const int i = lo + tid * step;
+            bool le = false;
+            if (i < hi) {
+                const LeafKey k = lk[i];
+                le = !key_less(xm, xt, k.pm, k.pt);
+            }
+            const int c = __syncthreads_count(le);
+            if (c == 0) {
+                a = lo;
+                break;
+            }
+            if (tid == 0) {
+                const int pc = lo + (c - 1) * step;
+                s_lo = pc + 1;
+                s_hi = min(hi, pc + step);
+            }
+            __syncthreads();
+        }
+        const int pos = a - 1;  // last leaf with prefix <= x, or -1
+        bool member = false;
+        unsigned int mt = 0;
+        if (pos >= 0) {
+            const LeafKey k = lk[pos];
+            unsigned long long pm;
+            unsigned int pt;
+            prefix96(xm, xt, (int)k.t, pm, pt);
+            member = pm == k.pm && pt == k.pt;
+            mt = lm[pos];
+        }
+        const int id = (int)(mt >> 8), cnt = (int)(mt & 0xFFu);
+        const bool split = member && cnt >= P;
+        // capacity: a split or a new leaf needs one more leaf record and list id
+        if (!(member && !split) && (N + 1 > v.C || nid + 1 > v.C)) {
+            if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
+            __syncthreads();
+            break;
+        }
+
+        if (member && !split) {
+            // ---- append to the leaf ---------------------------------------------------
+            if (tid == 0) {
+                const long long sb = (long long)id * P + cnt;
+                stok[sb] = tok;
+                skey[sb] = xm;
+                cntl[id] = cnt + 1;
+                lm[pos] = ((unsigned)id << 8) | (unsigned)(cnt + 1);
+                if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = id * P + cnt;
+            }
+            if (l == 0) {
+                T* pk = reinterpret_cast<T*>(v.page_k) + v.page_row(u, id, cnt) * kD;
+                T* pv = reinterpret_cast<T*>(v.page_v) + v.page_row(u, id, cnt) * kD;
+                for (int i = tid; i < kD; i += kInsThreads) {
+                    pk[i] = kin[i];
+                    pv[i] = vin[i];
+                }
+            }
+            __syncthreads();
+            continue;
+        }
+
+        if (split) {
+            // ---- split the full leaf in two ---------------------------------------------
+            for (int j = tid; j <= P; j += kInsThreads) {
+                if (j < P) {
+                    e_m[j] = skey[(long long)id * P + j];
+                    e_t[j] = (unsigned)stok[(long long)id * P + j];
+                } else {
+                    e_m[j] = xm;
+                    e_t[j] = xt;
+                }
+                e_slot[j] = j;
+            }
+            if (l == 0) {  // stage the P old rows and the new row, K and V
+                const T* pk = reinterpret_cast<const T*>(v.page_k) + v.page_row(u, id, 0) * kD;
+                const T* pv = reinterpret_cast<const T*>(v.page_v) + v.page_row(u, id, 0) * kD;
+                for (int i = tid; i < (P + 1) * kD; i += kInsThreads) {
+                    const int r = i / kD, c = i % kD;
+                    rows_k[i] = r < P ? pk[(long long)r * kD + c] : kin[c];
+                    rows_v[i] = r < P ? pv[(long long)r * kD + c] : vin[c];
+                }
+            }
+            __syncthreads();
+            // rank of each key among the P+1 (keys are distinct)
+            for (int j = tid; j <= P; j += kInsThreads) {
+                int r = 0;
+                for (int k = 0; k <= P; ++k) r += key_less(e_m[k], e_t[k], e_m[j], e_t[j]);
+                s_sorted[r] = j;
+            }
+            __syncthreads();
+            const int f = s_sorted[0], g = s_sorted[P];
+            const int lam = lcp96(e_m[f], e_t[f], e_m[g], e_t[g]);
+            if (tid == 0) {
+                int nl = 0;
+                for (int r = 0; r <= P; ++r) nl += key_bit96(e_m[s_sorted[r]], e_t[s_sorted[r]], lam) == 0;
+                s_cnt = nl;
+            }
+            __syncthreads();
+            const int nl = s_cnt, nr = P + 1 - nl;
+            const int rid = nid;  // right child takes the next free id
+            for (int r = tid; r <= P; r += kInsThreads) {
+                const int j = s_sorted[r];
+                const int dst = r < nl ? id : rid;
+                const int slot = r < nl ? r : r - nl;
+                stok[(long long)dst * P + slot] = (int)e_t[j];
+                skey[(long long)dst * P + slot] = e_m[j];
+                if (l == 0) v.tok_loc[(long long)u * v.max_tokens + e_t[j]] = dst * P + slot;
+            }
+            if (l == 0) {
+                for (int i = tid; i < (P + 1) * kD; i += kInsThreads) {
+                    const int r = i / kD, c = i % kD;
+                    const int j = s_sorted[r];
+                    const int dst = r < nl ? id : rid;
+                    const int slot = r < nl ? r : r - nl;
+                    const long long o = v.page_row(u, dst, slot) * kD + c;
+                    reinterpret_cast<T*>(v.page_k)[o] = rows_k[(long long)j * kD + c];
+                    reinterpret_cast<T*>(v.page_v)[o] = rows_v[(long long)j * kD + c];
+                }
+            }
+            __syncthreads();
+            shift_right(lk, lc, lm, pos + 1, N);
+            if (tid == 0) {
+                cntl[id] = nl;
+                cntl[rid] = nr;
+                const int t = lam + 1;
+                LeafKey kl, kr;
+                prefix96(e_m[f], e_t[f], t, kl.pm, kl.pt);
+                prefix96(e_m[g], e_t[g], t, kr.pm, kr.pt);
+                kl.t = kr.t = (unsigned)t;
+                lk[pos] = kl;
+                lc[pos] = cell_of_prefix(kl.pm, (unsigned)t);
+                lm[pos] = ((unsigned)id << 8) | (unsigned)nl;
+                lk[pos + 1] = kr;
+                lc[pos + 1] = cell_of_prefix(kr.pm, (unsigned)t);
+                lm[pos + 1] = ((unsigned)rid << 8) | (unsigned)nr;
+                v.n_leaf[v.ul(u, l)] = N + 1;
+                v.next_id[v.ul(u, l)] = nid + 1;
+            }
+            __syncthreads();
+            continue;
+        }
+
+        // ---- x lies where no leaf exists: a new leaf below its longest common
+        //      prefix with the neighbouring keys -------------------------------------------
+        {
+            int best = -1;
+            // predecessor leaf `pos` and successor leaf `pos + 1`: all their keys
+            for (int side = 0; side < 2; ++side) {
+                const int li = pos + side;
+                if (li < 0 || li >= N) continue;
+                const unsigned int m2 = lm[li];
+                const int id2 = (int)(m2 >> 8), c2 = (int)(m2 & 0xFFu);
+                int bl = -1;
+                if (tid < c2) {
+                    const unsigned long long km = skey[(long long)id2 * P + tid];
+                    const unsigned int kt = (unsigned)stok[(long long)id2 * P + tid];
+                    bl = lcp96(xm, xt, km, kt);
+                }
+                for (int o = 16; o >= 1; o >>= 1) bl = max(bl, __shfl_xor_sync(0xffffffffu, bl, o));
+                best = max(best, bl);
+            }
+            // combine the warps (P <= 64 keys live in warps 0 and 1)
+            __shared__ int s_best[kInsThreads / 32];
+            if (lane == 0) s_best[warp] = best;
+            __syncthreads();
+            if (tid == 0) {
+                int b = -1;
+                for (int w = 0; w < kInsThreads / 32; ++w) b = max(b, s_best[w]);
+                s_cnt = b + 1;  // depth of the new leaf
+            }
+            __syncthreads();
+            const int t = s_cnt;
+            const int nidl = nid;
+            if (l == 0) {
+                T* pk = reinterpret_cast<T*>(v.page_k) + v.page_row(u, nidl, 0) * kD;
+                T* pv = reinterpret_cast<T*>(v.page_v) + v.page_row(u, nidl, 0) * kD;
+                for (int i = tid; i < kD; i += kInsThreads) {
+                    pk[i] = kin[i];
+                    pv[i] = vin[i];
+                }
+            }
+            shift_right(lk, lc, lm, pos + 1, N);
+            if (tid == 0) {
+                stok[(long long)nidl * P] = tok;
+                skey[(long long)nidl * P] = xm;
+                cntl[nidl] = 1;
+                if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = nidl * P;
+                LeafKey k;
+                prefix96(xm, xt, t, k.pm, k.pt);
+                k.t = (unsigned)t;
+                lk[pos + 1] = k;
+                lc[pos + 1] = cell_of_prefix(k.pm, (unsigned)t);
+                lm[pos + 1] = ((unsigned)nidl << 8) | 1u;
+                v.n_leaf[v.ul(u, l)] = N + 1;
+                v.next_id[v.ul(u, l)] = nid + 1;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, long long tok,
+                          cudaStream_t s) {
+    const size_t es = v.dtype == ICE_BF16 ? 2 : 4;
+    const size_t bytes = (size_t)2 * (v.P + 1) * kD * es;
+    if (v.dtype == ICE_BF16) {
+        cudaError_t e = cudaFuncSetAttribute(insert_kernel<__nv_bfloat16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        insert_kernel<__nv_bfloat16><<<v.U, kInsThreads, bytes, s>>>(
+            v, (const __nv_bfloat16*)k, (const __nv_bfloat16*)val, (int)tok);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(insert_kernel<float>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        insert_kernel<float><<<v.U, kInsThreads, bytes, s>>>(v, (const float*)k, (const float*)val,
+                                                            (int)tok);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ice
