@@ -222,6 +222,8 @@ def run_ice(args):
     from semantic_paged_kv_head_gb300 import ice, synth
 
     w = _workload(args.workload)
+    if args.layers:
+        w = synth.scaled(w, n_layers=args.layers)
     dev = torch.device("cuda", local)
     keys, values, centers = synth.make_kv(w, device=dev)
     q = synth.make_queries(w, centers)
@@ -383,6 +385,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -23,9 +23,9 @@
  *    Calls enqueue work on it and return without waiting, except where stated.
  *  - Return value: ICE_OK (0) or a negative ICE_ERR_* code. Argument errors
  *    are found on the host before anything is launched. Errors that only the
- *    GPU can see (a page id out of range, an exhausted capacity, a timed-out
- *    wait) are recorded in a per-index device status word that
- *    ice_get_error() returns; kernels never trap.
+ *    GPU can see (a page id out of range, an exhausted capacity) are recorded
+ *    in a per-index device status word that ice_get_error() returns; kernels
+ *    never trap and never wait on other blocks.
  *  - Element type of keys, values, queries and outputs is the index's dtype
  *    (ICE_BF16 or ICE_F32); rows of d elements are contiguous.
  */
@@ -44,7 +44,7 @@ extern "C" {
 #define ICE_ERR_INVALID_ARG (-1) /* bad argument; nothing was launched          */
 #define ICE_ERR_CAPACITY (-2)    /* token / page / leaf capacity exhausted        */
 #define ICE_ERR_CUDA (-3)        /* a CUDA runtime call failed                    */
-#define ICE_ERR_TIMEOUT (-4)     /* a bounded device wait ran out                 */
+#define ICE_ERR_TIMEOUT (-4)     /* reserved: a bounded device wait ran out       */
 #define ICE_ERR_BOUNDS (-5)      /* a page id or count given to a kernel is bad   */
 #define ICE_ERR_UNSUPPORTED (-6) /* valid request this build does not implement  */
 
@@ -199,10 +199,6 @@ int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap,
 int ice_debug_page(ice_index* ix, int32_t unit, int32_t page_id, void* host_k, void* host_v,
                    void* stream);
 
-/* Test hook: flag bit 0 makes ice_sparse_attn wait on a barrier nothing
- * signals, so that its bounded wait runs out and ICE_ERR_TIMEOUT is reported.
- * 0 restores normal operation. */
-int ice_debug_set_flags(ice_index* ix, int32_t flags);
 
 #ifdef __cplusplus
 }

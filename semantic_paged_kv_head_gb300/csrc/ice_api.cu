@@ -244,9 +244,6 @@ int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const
     if (!ix || !q || !page_ids || !n_pages || !out || !aligned16(q) || !aligned16(out))
         return ICE_ERR_INVALID_ARG;
     if (page_stride < 1 || page_stride > 512) return ICE_ERR_INVALID_ARG;
-    const size_t es = ix->p.dtype == ICE_BF16 ? 2 : 4;
-    const int ppc = attn_pages_per_cta(page_stride);
-    if ((size_t)2 * ppc * ix->p.page_size * kD * es > 200 * 1024) return ICE_ERR_UNSUPPORTED;
     cudaError_t e = launch_attn(ix->v, q, page_ids, n_pages, page_stride, out, (cudaStream_t)stream);
     return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
 }
@@ -345,10 +342,5 @@ int ice_debug_page(ice_index* ix, int32_t unit, int32_t page_id, void* host_k, v
     return ok ? ICE_OK : ICE_ERR_CUDA;
 }
 
-int ice_debug_set_flags(ice_index* ix, int32_t flags) {
-    if (!ix) return ICE_ERR_INVALID_ARG;
-    ix->v.debug_flags = flags;
-    return ICE_OK;
-}
 
 }  // extern "C"

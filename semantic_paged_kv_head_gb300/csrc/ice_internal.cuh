@@ -59,7 +59,6 @@ struct IndexView {
     void* page_k;
     void* page_v;
     int* status;
-    int debug_flags;
 
     __host__ __device__ long long ul(int u, int l) const { return (long long)u * L + l; }
     __host__ __device__ long long leaf_base(int u, int l) const { return ul(u, l) * C; }
@@ -254,7 +253,6 @@ cudaError_t build_phase2(const IndexView& v, const void* keys, const void* value
 cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st);
 void scratch_free(BuildScratch& s, cudaStream_t st);
 int select_smem_bytes(long long C, int L, int P, int n_cand);
-int attn_pages_per_cta(int page_stride);
 
 // ---- launchers (implemented in the .cu files) --------------------------------------
 cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, long long tok,

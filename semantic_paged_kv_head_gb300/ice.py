@@ -34,8 +34,7 @@ ICE_BF16 = 1
 
 # every symbol include/ice.h declares
 EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_sparse_attn", "ice_get_error",
-           "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page",
-           "ice_debug_set_flags"]
+           "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page"]
 
 
 class ice_params(ctypes.Structure):
@@ -88,8 +87,6 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_debug_dump.restype = i64
     lib.ice_debug_page.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.ice_debug_page.restype = ctypes.c_int
-    lib.ice_debug_set_flags.argtypes = [vp, i32]
-    lib.ice_debug_set_flags.restype = ctypes.c_int
     return lib
 
 
@@ -217,9 +214,6 @@ class IceIndex:
             self.destroy()
         except Exception:
             pass
-
-    def set_debug_flags(self, flags: int):
-        _check(_lib.ice_debug_set_flags(self._h, int(flags)), "ice_debug_set_flags")
 
     # -- debug views --------------------------------------------------------------------
     def dump(self, unit: int, stream=None) -> dict:
