@@ -182,8 +182,9 @@ int ice_get_info(const ice_index* ix, ice_info* info);
  *                     next_id[0..3], reserved
  *   per composite l (repeated L times):
  *     leaf key   [C] x {uint64 morton_prefix, uint32 token_prefix, uint32 t}
- *     leaf cell  [C] x {uint8 lo[8], uint8 hi[8]}
- *     leaf meta  [C] x uint32 (list id << 8 | token count)
+ *     leaf rec   [C] x {uint8 lo[8], uint32 list id << 8 | token count, uint32 t}
+ *                (lo = lower corner of the leaf's code cell; the upper corner
+ *                 is lo_j | (2^(8 - b_j) - 1), b_j the known bits of code j)
  *     list count [C] x int32 (tokens in list/page id)
  *     slot token [C][P] x int32 (token of each slot of list/page id)
  *     slot key   [C][P] x uint64 (Morton key of that token)

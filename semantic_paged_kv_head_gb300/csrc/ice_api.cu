@@ -174,8 +174,7 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         const size_t es = params->dtype == ICE_BF16 ? 2 : 4;
         bool okc = true;
         okc = okc && dev_alloc(ix, &v.leaf_key, (size_t)U * L * C) == cudaSuccess;
-        okc = okc && dev_alloc(ix, &v.leaf_cell, (size_t)U * L * C) == cudaSuccess;
-        okc = okc && dev_alloc(ix, &v.leaf_meta, (size_t)U * L * C) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.leaf_rec, (size_t)U * L * C) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.n_leaf, (size_t)U * L) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.next_id, (size_t)U * L) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.list_cnt, (size_t)U * L * C) == cudaSuccess;
@@ -195,6 +194,13 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         }
         v.page_k = pk;
         v.page_v = pv;
+        if (select_prepare() != cudaSuccess) {
+            scratch_free(s, st);
+            cudaGetLastError();
+            free_all(ix);
+            delete ix;
+            return ICE_ERR_CUDA;
+        }
         e = cudaMemsetAsync(v.n_leaf, 0, sizeof(int) * U * L, st);
         if (e == cudaSuccess) e = cudaMemsetAsync(v.next_id, 0, sizeof(int) * U * L, st);
         if (e == cudaSuccess) e = cudaMemsetAsync(v.list_cnt, 0, sizeof(int) * U * L * C, st);
@@ -284,7 +290,7 @@ int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap,
     if (!ix || unit < 0 || unit >= ix->U) return ICE_ERR_INVALID_ARG;
     const int L = ix->p.n_composite, P = ix->p.page_size;
     const long long C = ix->C;
-    const int64_t per_l = C * 16 + C * 16 + C * 4 + C * 4 + C * P * 4 + C * P * 8;
+    const int64_t per_l = C * 16 + C * 16 + C * 4 + C * P * 4 + C * P * 8;
     const int64_t need = 16 * 8 + L * per_l + ix->v.max_tokens * 4;
     if (!host_buf || cap < need) return need;
     cudaStream_t st = (cudaStream_t)stream;
@@ -313,10 +319,8 @@ int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap,
         const long long lb = v.leaf_base(unit, l), sb = v.slot_base(unit, l);
         ok = ok && cudaMemcpy(o, v.leaf_key + lb, C * 16, cudaMemcpyDeviceToHost) == cudaSuccess;
         o += C * 16;
-        ok = ok && cudaMemcpy(o, v.leaf_cell + lb, C * 16, cudaMemcpyDeviceToHost) == cudaSuccess;
+        ok = ok && cudaMemcpy(o, v.leaf_rec + lb, C * 16, cudaMemcpyDeviceToHost) == cudaSuccess;
         o += C * 16;
-        ok = ok && cudaMemcpy(o, v.leaf_meta + lb, C * 4, cudaMemcpyDeviceToHost) == cudaSuccess;
-        o += C * 4;
         ok = ok && cudaMemcpy(o, v.list_cnt + lb, C * 4, cudaMemcpyDeviceToHost) == cudaSuccess;
         o += C * 4;
         ok = ok && cudaMemcpy(o, v.slot_tok + sb, C * P * 4, cudaMemcpyDeviceToHost) == cudaSuccess;

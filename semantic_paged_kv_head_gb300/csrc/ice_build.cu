@@ -391,8 +391,7 @@ __global__ void __launch_bounds__(256) leaf_write_kernel(
         k.pt = pt;
         k.t = (unsigned)depth;
         v.leaf_key[lb] = k;
-        v.leaf_cell[lb] = cell_of_prefix(pm, (unsigned)depth);
-        v.leaf_meta[lb] = ((unsigned)leaf << 8) | (unsigned)(end - start);
+        v.leaf_rec[lb] = make_leaf_rec(pm, (unsigned)depth, leaf, end - start);
         v.list_cnt[v.leaf_base(u, l) + leaf] = end - start;
     }
     if (i == 0) {

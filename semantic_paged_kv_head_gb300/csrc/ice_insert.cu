@@ -23,25 +23,23 @@ struct InsKey {
     unsigned int t;
 };
 
-// Shift leaf records [from, N) one place to the right (backwards, in chunks).
-__device__ void shift_right(LeafKey* key, uint4* cell, unsigned int* meta, int from, int N) {
+// Shift leaf keys and records [from, N) one place to the right (backwards, in
+// chunks of one element per thread).
+__device__ void shift_right(LeafKey* key, uint4* rec, int from, int N) {
     for (int end = N; end > from; end -= kInsThreads) {
         const int start = max(from, end - kInsThreads);
         const int i = start + (int)threadIdx.x;
         LeafKey k;
-        uint4 c;
-        unsigned int mt = 0;
+        uint4 r;
         const bool act = i < end;
         if (act) {
             k = key[i];
-            c = cell[i];
-            mt = meta[i];
+            r = rec[i];
         }
         __syncthreads();
         if (act) {
             key[i + 1] = k;
-            cell[i + 1] = c;
-            meta[i + 1] = mt;
+            rec[i + 1] = r;
         }
         __syncthreads();
     }
@@ -100,8 +98,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
         const unsigned long long xm = s_mk[l];
         const unsigned int xt = (unsigned)tok;
         LeafKey* lk = v.leaf_key + v.leaf_base(u, l);
-        uint4* lc = v.leaf_cell + v.leaf_base(u, l);
-        unsigned int* lm = v.leaf_meta + v.leaf_base(u, l);
+        uint4* lr = v.leaf_rec + v.leaf_base(u, l);
         int* cntl = v.list_cnt + v.leaf_base(u, l);
         int* stok = v.slot_tok + v.slot_base(u, l);
         unsigned long long* skey = v.slot_key + v.slot_base(u, l);
@@ -148,17 +145,18 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
         }
         const int pos = a - 1;  // last leaf with prefix <= x, or -1
         bool member = false;
-        unsigned int mt = 0;
+        uint4 rc = make_uint4(0u, 0u, 0u, 0u);
         if (pos >= 0) {
             const LeafKey k = lk[pos];
             unsigned long long pm;
             unsigned int pt;
             prefix96(xm, xt, (int)k.t, pm, pt);
             member = pm == k.pm && pt == k.pt;
-            mt = lm[pos];
+            rc = lr[pos];
         }
-        const int id = (int)(mt >> 8), cnt = (int)(mt & 0xFFu);
+        const int id = rec_id(rc), cnt = rec_cnt(rc);
         const bool split = member && cnt >= P;
+        __syncthreads();  // every thread has read the record before any thread updates it
         // capacity: a split or a new leaf needs one more leaf record and list id
         if (!(member && !split) && (N + 1 > v.C || nid + 1 > v.C)) {
             if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
@@ -173,7 +171,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 stok[sb] = tok;
                 skey[sb] = xm;
                 cntl[id] = cnt + 1;
-                lm[pos] = ((unsigned)id << 8) | (unsigned)(cnt + 1);
+                lr[pos].z = ((unsigned)id << 8) | (unsigned)(cnt + 1);
                 if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = id * P + cnt;
             }
             if (l == 0) {
@@ -247,7 +245,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 }
             }
             __syncthreads();
-            shift_right(lk, lc, lm, pos + 1, N);
+            shift_right(lk, lr, pos + 1, N);
             if (tid == 0) {
                 cntl[id] = nl;
                 cntl[rid] = nr;
@@ -257,11 +255,9 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 prefix96(e_m[g], e_t[g], t, kr.pm, kr.pt);
                 kl.t = kr.t = (unsigned)t;
                 lk[pos] = kl;
-                lc[pos] = cell_of_prefix(kl.pm, (unsigned)t);
-                lm[pos] = ((unsigned)id << 8) | (unsigned)nl;
+                lr[pos] = make_leaf_rec(kl.pm, (unsigned)t, id, nl);
                 lk[pos + 1] = kr;
-                lc[pos + 1] = cell_of_prefix(kr.pm, (unsigned)t);
-                lm[pos + 1] = ((unsigned)rid << 8) | (unsigned)nr;
+                lr[pos + 1] = make_leaf_rec(kr.pm, (unsigned)t, rid, nr);
                 v.n_leaf[v.ul(u, l)] = N + 1;
                 v.next_id[v.ul(u, l)] = nid + 1;
             }
@@ -277,8 +273,8 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
             for (int side = 0; side < 2; ++side) {
                 const int li = pos + side;
                 if (li < 0 || li >= N) continue;
-                const unsigned int m2 = lm[li];
-                const int id2 = (int)(m2 >> 8), c2 = (int)(m2 & 0xFFu);
+                const uint4 r2 = lr[li];
+                const int id2 = rec_id(r2), c2 = rec_cnt(r2);
                 int bl = -1;
                 if (tid < c2) {
                     const unsigned long long km = skey[(long long)id2 * P + tid];
@@ -308,7 +304,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                     pv[i] = vin[i];
                 }
             }
-            shift_right(lk, lc, lm, pos + 1, N);
+            shift_right(lk, lr, pos + 1, N);
             if (tid == 0) {
                 stok[(long long)nidl * P] = tok;
                 skey[(long long)nidl * P] = xm;
@@ -318,8 +314,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 prefix96(xm, xt, t, k.pm, k.pt);
                 k.t = (unsigned)t;
                 lk[pos + 1] = k;
-                lc[pos + 1] = cell_of_prefix(k.pm, (unsigned)t);
-                lm[pos + 1] = ((unsigned)nidl << 8) | 1u;
+                lr[pos + 1] = make_leaf_rec(k.pm, (unsigned)t, nidl, 1);
                 v.n_leaf[v.ul(u, l)] = N + 1;
                 v.next_id[v.ul(u, l)] = nid + 1;
             }

@@ -6,16 +6,18 @@
 //                                   rows padded to 132 floats for 16-byte loads
 //   e_unit     [U] i32              frozen scale exponent, c = 2^e
 //   leaf_key   [U][L][C] LeafKey    96-bit prefix + length, sorted (left to right)
-//   leaf_cell  [U][L][C] uint4      code cell lo[8], hi[8] of each leaf
-//   leaf_meta  [U][L][C] u32        list id << 8 | token count
+//   leaf_rec   [U][L][C] uint4      leaf record: x, y = lower cell corner lo[8]
+//                                   (one byte per direction), z = list id << 8 |
+//                                   token count, w = prefix length t (the upper
+//                                   corner is lo | (2^(8 - known bits(t, j)) - 1))
 //   n_leaf     [U][L] i32, next_id [U][L] i32
 //   list_cnt   [U][L][C] i32        tokens held by list / page id
 //   slot_tok   [U][L][C][P] i32     token of each slot
 //   slot_key   [U][L][C][P] u64     Morton key of each slot's token
 //   tok_loc    [U][max_tokens] i32  page * P + slot of each token (composite 0)
 //   page_k/v   [U][C][P][D] T       the physical pages (composite-0 lists)
-// The select kernel streams leaf_cell + leaf_meta (20 B per leaf); insert is
-// the only reader of leaf_key and slot_key.
+// The select kernel streams leaf_rec (16 B per leaf); insert is the only
+// reader of leaf_key and slot_key.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -48,8 +50,7 @@ struct IndexView {
     const float* dirs;
     int* e_unit;
     LeafKey* leaf_key;
-    uint4* leaf_cell;
-    unsigned int* leaf_meta;
+    uint4* leaf_rec;
     int* n_leaf;
     int* next_id;
     int* list_cnt;
@@ -191,6 +192,14 @@ __device__ __forceinline__ uint4 cell_of_prefix(unsigned long long pm, unsigned 
     return r;
 }
 
+// Leaf record: lower cell corner of a prefix, list id, count, prefix length.
+__device__ __forceinline__ uint4 make_leaf_rec(unsigned long long pm, unsigned t, int id, int cnt) {
+    const uint4 cell = cell_of_prefix(pm, t);
+    return make_uint4(cell.x, cell.y, ((unsigned)id << 8) | (unsigned)cnt, t);
+}
+__device__ __forceinline__ int rec_id(const uint4& r) { return (int)(r.z >> 8); }
+__device__ __forceinline__ int rec_cnt(const uint4& r) { return (int)(r.z & 0xFFu); }
+
 // Length of the common prefix of two 96-bit keys.
 __device__ __forceinline__ int lcp96(unsigned long long am, unsigned int at, unsigned long long bm,
                                      unsigned int bt) {
@@ -253,6 +262,7 @@ cudaError_t build_phase2(const IndexView& v, const void* keys, const void* value
 cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st);
 void scratch_free(BuildScratch& s, cudaStream_t st);
 int select_smem_bytes(long long C, int L, int P, int n_cand);
+cudaError_t select_prepare();
 
 // ---- launchers (implemented in the .cu files) --------------------------------------
 cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, long long tok,

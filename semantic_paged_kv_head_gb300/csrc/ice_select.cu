@@ -2,77 +2,169 @@
 // mechanism section: P-DCI, the prioritised DCI search, picks the pages most
 // relevant to the current query).
 //
-// One 512-thread block per unit, organised for memory-level parallelism (the
-// work per unit is a chain of dependent phases, so the latency of each phase
-// is what the block must hide):
-//  1. the first batch of leaf records is requested before the query prep:
-//     q_sel = sum of the group's heads (fp32, head order), its normalisation
-//     and the 8-bit codes of its projections per composite;
-//  2. all composites are scanned in one pass: priority of every leaf = the
+// One 512-thread block per unit. The work of a unit is a chain of dependent
+// phases, so each phase is organised to keep many requests in flight and to
+// spend few instructions per element:
+//  1. the unit's leaf counts, the group's query heads and the projection
+//     directions are requested together; the first batch of leaf records is
+//     requested before the query prep (q_sel = sum of the heads in head order,
+//     normalised, projected and quantised per composite) is computed;
+//  2. all composites are scanned in one pass: the priority of a leaf is the
 //     L-infinity distance in code units between the query codes and the leaf's
-//     cell, and token counts by priority go to sub-histograms shared by two
-//     warps each;
-//  3. per composite, the threshold priority pi* is the smallest with
-//     cumulative count >= n_cand; leaves with priority < pi* are taken, and
-//     those at pi* in left-to-right order while the tokens taken before them at
-//     pi* are fewer than needed (the order a best-first tree search visits
-//     leaves in);
-//  4. every slot of every taken leaf is expanded in one parallel round into a
-//     candidate (token, row); a composite-1 token whose page was taken in
-//     composite 0 is a duplicate and dropped;
-//  5. every candidate is rescored with the fixed-order fp32 dot q_sel . k, four
-//     rows per warp instruction (8 lanes per row, each lane evaluating four of
-//     the 32 lane partials of the fixed order);
-//  6. candidates are sorted by (score desc, token asc) and walked; the page of
-//     each is taken on first occurrence until n_sel pages are taken.
+//     cell, evaluated two directions per instruction on fp16x2 (codes are
+//     exact small integers there); token counts by priority go to
+//     sub-histograms shared by two warps;
+//  3. per composite, pi* is the smallest priority whose cumulative count
+//     reaches n_cand; leaves below pi* are taken, and leaves at pi* in
+//     left-to-right order while the tokens taken before them at pi* are fewer
+//     than needed (the order a best-first tree search visits leaves in);
+//  4. every slot of every taken leaf becomes a candidate (token, row) in one
+//     parallel round; a composite-1 token whose page composite 0 already took
+//     is a duplicate and dropped;
+//  5. every candidate is rescored with the fixed-order fp32 dot q_sel . k
+//     (8 lanes per row, each lane evaluating four of the 32 lane partials of
+//     the fixed order), and its (score desc, token asc) key is min-reduced
+//     into its page's slot of a shared-memory hash table: a page's first
+//     occurrence in the ranked candidate list is its smallest key;
+//  6. the n_sel pages with the smallest keys, in key order, are the selection
+//     (warp-level bitonic top-32 and a fixed-order merge of the warps' lists;
+//     a block-wide bitonic sort when n_sel > 32).
 #include "ice_internal.cuh"
+
+#include <cuda_fp16.h>
 
 namespace ice {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSubH = 8;     // sub-histograms per composite (two warps each)
-constexpr int kScanUnr = 8;  // leaf records in flight per thread
-constexpr int kRowUnr = 2;   // candidate rows per lane group per round
+constexpr int kSubH = 8;      // sub-histograms per composite (two warps each)
+constexpr int kScanUnr = 8;   // leaf records in flight per thread
+constexpr int kRowUnr = 2;    // candidate rows per lane group per round
+constexpr int kTieCap = 256;  // leaves at pi* ordered by rank counting; more -> range scan
+constexpr int kTopK = 32;     // warp top-k width
 
 struct SelSmem {
-    int prio, cnt, hist, chosen, cmeta, coff, bm0, bm_taken, keys, vals, end;
+    int prio, hist, chosen, cmeta, coff, tie, bm0, keys, vals, hpage, hkey, top, end;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
 
-__host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, int sort_cap) {
+__host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, int sort_cap,
+                                              int hcap) {
     SelSmem s;
     int o = 0;
     s.prio = o; o = align16(o + L * (int)C);
-    s.cnt = o; o = align16(o + L * (int)C);
     s.hist = o; o = align16(o + L * kSubH * 256 * 4);
     s.chosen = o; o = align16(o + L * n_cand * 4);
     s.cmeta = o; o = align16(o + L * n_cand * 4);
     s.coff = o; o = align16(o + L * (n_cand + 1) * 4);
+    s.tie = o; o = align16(o + L * kTieCap * 4);
     s.bm0 = o; o = align16(o + (int)((C + 31) / 32) * 4);
-    s.bm_taken = o; o = align16(o + (int)((C + 31) / 32) * 4);
     s.keys = o; o = align16(o + sort_cap * 8);
     s.vals = o; o = align16(o + sort_cap * 4);
+    s.hpage = o; o = align16(o + hcap * 4);
+    s.hkey = o; o = align16(o + hcap * 8);
+    s.top = o; o = align16(o + kSelWarps * kTopK * 12);
     s.end = o;
     return s;
 }
 
-__device__ __forceinline__ int cell_dist(uint4 cell, const int (&qc)[8]) {
-    const unsigned lo[2] = {cell.x, cell.y}, hi[2] = {cell.z, cell.w};
-    int best = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int l = (int)((lo[j >> 2] >> (8 * (j & 3))) & 0xFF);
-        const int h = (int)((hi[j >> 2] >> (8 * (j & 3))) & 0xFF);
-        const int c = qc[j];
-        const int dj = c < l ? l - c : (c > h ? c - h : 0);
-        best = max(best, dj);
-    }
-    return best;
+// Two bytes of x (selector s) as two fp16 values 1024 + byte (exact). The bit
+// pattern is moved with memcpy: reading the word through a __half2 lvalue would
+// break type-based aliasing rules.
+__device__ __forceinline__ __half2 bytes_to_h2(unsigned x, unsigned s) {
+    const unsigned w = __byte_perm(x, 0x64646464u, s);
+    __half2 h;
+    memcpy(&h, &w, sizeof(h));
+    return h;
 }
 
-// Raw row chunk of 4 elements (8 B for bf16, 16 B for f32) and its widening.
+// Widths hi - lo of the 8 code intervals of a prefix of length t, as fp16x2.
+__device__ __forceinline__ void cell_widths(int t, __half2 (&w)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float a[2];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+            const int j = 2 * k + z;
+            int b = t >= 64 ? 8 : ((t + 7 - j) >> 3);
+            b = b > 8 ? 8 : b;
+            a[z] = (float)((1 << (8 - b)) - 1);
+        }
+        w[k] = __floats2half2_rn(a[0], a[1]);
+    }
+}
+
+// L-infinity distance (code units) between the query codes q (biased fp16x2,
+// directions 2k, 2k+1 in word k) and the cell of a leaf record.
+__device__ __forceinline__ int leaf_priority(const uint4& rec, const __half2 (&q)[4],
+                                             const __half2* widths /* [97][4] */) {
+    const __half2 lo[4] = {bytes_to_h2(rec.x, 0x4140u), bytes_to_h2(rec.x, 0x4342u),
+                           bytes_to_h2(rec.y, 0x4140u), bytes_to_h2(rec.y, 0x4342u)};
+    const int t = (int)min(rec.w, 96u);
+    __half2 m[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __half2 hi = __hadd2(lo[k], widths[t * 4 + k]);
+        m[k] = __hmax2(__hsub2(lo[k], q[k]), __hsub2(q[k], hi));  // one of them is <= 0
+    }
+    const __half2 r = __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
+    const __half d = __hmax(__hmax(__low2half(r), __high2half(r)), __float2half(0.0f));
+    const __half b = __hadd(d, __float2half(1024.0f));  // 1024 + d, d in [0, 255]
+    return (int)(__half_as_ushort(b) & 0x3FFu);
+}
+
+// Byte store to shared memory through an explicit st.shared.u8. With a plain
+// C++ byte store of the fp16-derived priority, the priority table did not
+// receive the values in builds of this kernel for sm_103a with nvcc 13.0 (the
+// bytes read back unchanged after the block barrier); the explicit store does.
+__device__ __forceinline__ void st_shared_u8(unsigned char* p, int v) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"((unsigned)v & 0xFFu) : "memory");
+}
+
+// Ascending bitonic sort of one (key, value) per lane across the warp.
+__device__ __forceinline__ void warp_sort32(unsigned long long& k, int& v, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned long long ok = __shfl_xor_sync(0xffffffffu, k, stride);
+            const int ov = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool up = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            const bool keep_min = lower == up;
+            const bool take = keep_min ? (ok < k) : (ok > k);
+            if (take) {
+                k = ok;
+                v = ov;
+            }
+        }
+    }
+}
+
+// a (sorted ascending across lanes) := the 32 smallest of a and b (b sorted).
+__device__ __forceinline__ void warp_merge32(unsigned long long& ka, int& va, unsigned long long kb,
+                                             int vb, int lane) {
+    const unsigned long long rk = __shfl_sync(0xffffffffu, kb, 31 - lane);
+    const int rv = __shfl_sync(0xffffffffu, vb, 31 - lane);
+    if (rk < ka) {
+        ka = rk;
+        va = rv;
+    }
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const unsigned long long ok = __shfl_xor_sync(0xffffffffu, ka, stride);
+        const int ov = __shfl_xor_sync(0xffffffffu, va, stride);
+        const bool lower = (lane & stride) == 0;
+        const bool take = lower ? (ok < ka) : (ok > ka);
+        if (take) {
+            ka = ok;
+            va = ov;
+        }
+    }
+}
+
 template <typename T> struct Chunk;
 template <> struct Chunk<__nv_bfloat16> {
     uint2 r;
@@ -92,69 +184,75 @@ template <> struct Chunk<float> {
     }
 };
 
-template <typename T>
+template <typename T, int G>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
-    IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap,
+    IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
     int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out, int32_t* __restrict__ stats) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
-    __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL];
-    __shared__ int s_ncand, s_nraw;
+    __shared__ __align__(16) __half2 s_width[97 * 4];
+    __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL], s_ntie[kMaxL];
+    __shared__ int s_ncand, s_nraw, s_npg;
     __shared__ int s_wsum[kMaxL][kSelWarps];
 
     const int u = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = v.L, P = v.P;
     const long long C = v.C;
-    const SelSmem lay = sel_layout(C, L, n_cand, sort_cap);
+    const SelSmem lay = sel_layout(C, L, n_cand, sort_cap, hcap);
     unsigned char* prio = smem + lay.prio;                            // [L][C]
-    unsigned char* cnts = smem + lay.cnt;                             // [L][C]
     int* hist = reinterpret_cast<int*>(smem + lay.hist);              // [L][kSubH][256]
     int* chosen = reinterpret_cast<int*>(smem + lay.chosen);          // [L][n_cand] leaf index
-    unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);  // [L][n_cand] leaf meta
+    unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);  // [L][n_cand] id|count
     int* coff = reinterpret_cast<int*>(smem + lay.coff);              // [L][n_cand + 1]
+    int* tie = reinterpret_cast<int*>(smem + lay.tie);                // [L][kTieCap]
     unsigned* bm0 = reinterpret_cast<unsigned*>(smem + lay.bm0);
-    unsigned* bm_taken = reinterpret_cast<unsigned*>(smem + lay.bm_taken);
     unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.keys);
     int* sval = reinterpret_cast<int*>(smem + lay.vals);
+    int* hpage = reinterpret_cast<int*>(smem + lay.hpage);
+    unsigned long long* hkey = reinterpret_cast<unsigned long long*>(smem + lay.hkey);
+    unsigned long long* topk = reinterpret_cast<unsigned long long*>(smem + lay.top);
+    int* topv = reinterpret_cast<int*>(smem + lay.top + kSelWarps * kTopK * 8);
     const int nwords = (int)((C + 31) / 32);
+    const uint4* recs = v.leaf_rec;
 
+    // ---- 1. leaf counts, query heads and directions requested together -------------------
     int N[kMaxL] = {0, 0};
-    for (int l = 0; l < L; ++l) {
-        const int x = v.n_leaf[v.ul(u, l)];
-        N[l] = x < 0 ? 0 : (x > C ? (int)C : x);
+    for (int l = 0; l < L; ++l) N[l] = v.n_leaf[v.ul(u, l)];
+    float qh[G][4];
+    const T* qu = q + (long long)u * G * kD;
+#pragma unroll
+    for (int h = 0; h < G; ++h) load4(qu + (long long)h * kD + 4 * lane, qh[h]);
+    float wdir[4] = {0.f, 0.f, 0.f, 0.f};
+    float wlast = 0.f;
+    if (warp < L * kM) {
+        const float* ud = v.dirs + (long long)warp * kDirStride;
+        load4(ud + 4 * lane, wdir);
+        wlast = ud[kD];
     }
+    for (int l = 0; l < L; ++l) N[l] = N[l] < 0 ? 0 : (N[l] > C ? (int)C : N[l]);
     const int Ntot = N[0] + N[1];
-
-    // ---- 1a. request the first batch of leaf records --------------------------------
-    uint4 c4[kScanUnr];
-    unsigned m4[kScanUnr];
+    uint4 rb[kScanUnr];
     auto load_batch = [&](int base) {
 #pragma unroll
         for (int k = 0; k < kScanUnr; ++k) {
             const int i = base + k * kSelThreads + tid;
             if (i < Ntot) {
                 const int l = i < N[0] ? 0 : 1;
-                const long long o = v.leaf_base(u, l) + (i - (l ? N[0] : 0));
-                c4[k] = __ldg(v.leaf_cell + o);
-                m4[k] = __ldg(v.leaf_meta + o);
+                rb[k] = __ldg(recs + v.leaf_base(u, l) + (i - (l ? N[0] : 0)));
             }
         }
     };
     load_batch(0);
 
-    // ---- 1b. query prep ---------------------------------------------------------------
+    // query prep
     {
-        float qs[4];
-        const T* qu = q + (long long)u * v.G * kD;
-        load4(qu + 4 * lane, qs);
-        for (int h = 1; h < v.G; ++h) {
-            float x[4];
-            load4(qu + (long long)h * kD + 4 * lane, x);
+        float qs[4] = {qh[0][0], qh[0][1], qh[0][2], qh[0][3]};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) qs[k] = __fadd_rn(qs[k], x[k]);
-        }
+        for (int h = 1; h < G; ++h)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) qs[k] = __fadd_rn(qs[k], qh[h][k]);
         const float nq = warp_dot_fixed(qs, qs);
         float qt[4] = {0.f, 0.f, 0.f, 0.f};
         if (nq > 0.0f) {
@@ -162,26 +260,31 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 #pragma unroll
             for (int k = 0; k < 4; ++k) qt[k] = __fdiv_rn(qs[k], sn);
         }
-        for (int dir = warp; dir < L * kM; dir += kSelWarps) {
-            const float* ud = v.dirs + (long long)dir * kDirStride;
-            float w[4];
-            load4(ud + 4 * lane, w);
-            const float p = __fmaf_rn(ud[kD], 0.0f, warp_dot_fixed(w, qt));
-            if (lane == 0) s_qcode[dir / kM][dir % kM] = quantise_code(p);
+        if (warp < L * kM) {
+            const float p = __fmaf_rn(wlast, 0.0f, warp_dot_fixed(wdir, qt));
+            if (lane == 0) s_qcode[warp / kM][warp % kM] = quantise_code(p);
         }
         if (warp == 0) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) s_qsel[4 * lane + k] = qs[k];
         }
     }
+    if (tid < 97) {
+        __half2 w[4];
+        cell_widths(tid, w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s_width[tid * 4 + k] = w[k];
+    }
     for (int i = tid; i < L * kSubH * 256; i += kSelThreads) hist[i] = 0;
-    for (int i = tid; i < nwords; i += kSelThreads) {
-        bm0[i] = 0u;
-        bm_taken[i] = 0u;
+    for (int i = tid; i < nwords; i += kSelThreads) bm0[i] = 0u;
+    for (int i = tid; i < hcap; i += kSelThreads) {
+        hpage[i] = -1;
+        hkey[i] = ~0ull;
     }
     if (tid < kMaxL) {
         s_nch[tid] = 0;
         s_tot[tid] = 0;
+        s_ntie[tid] = 0;
     }
     if (tid == 0) {
         s_ncand = 0;
@@ -191,11 +294,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 
     // ---- 2. priorities + sub-histograms of token counts, all composites ------------------
     {
-        int qc[kMaxL][8];
+        __half2 qc[kMaxL][4];
 #pragma unroll
-        for (int l = 0; l < kMaxL; ++l)
+        for (int l = 0; l < kMaxL; ++l) {
+            unsigned lo4 = 0, hi4 = 0;
+            if (l < L) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) qc[l][j] = l < L ? s_qcode[l][j] : 0;
+                for (int j = 0; j < 4; ++j) {
+                    lo4 |= (unsigned)s_qcode[l][j] << (8 * j);
+                    hi4 |= (unsigned)s_qcode[l][4 + j] << (8 * j);
+                }
+            }
+            qc[l][0] = bytes_to_h2(lo4, 0x4140u);
+            qc[l][1] = bytes_to_h2(lo4, 0x4342u);
+            qc[l][2] = bytes_to_h2(hi4, 0x4140u);
+            qc[l][3] = bytes_to_h2(hi4, 0x4342u);
+        }
         const int sub = warp >> 1;
         for (int base = 0; base < Ntot; base += kScanUnr * kSelThreads) {
             if (base > 0) load_batch(base);
@@ -205,10 +319,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 if (i < Ntot) {
                     const int l = i < N[0] ? 0 : 1;
                     const int li = i - (l ? N[0] : 0);
-                    const int pr = cell_dist(c4[k], l ? qc[1] : qc[0]);
-                    const int cn = (int)(m4[k] & 0xFFu);
-                    prio[l * C + li] = (unsigned char)pr;
-                    cnts[l * C + li] = (unsigned char)cn;
+                    const int pr = leaf_priority(rb[k], l ? qc[1] : qc[0], s_width);
+                    const int cn = rec_cnt(rb[k]);
+                    st_shared_u8(prio + l * C + li, pr);
                     atomicAdd(&hist[(l * kSubH + sub) * 256 + pr], cn);
                 }
             }
@@ -253,60 +366,104 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     }
     __syncthreads();
 
-    // ---- 3b. leaves taken at pi*, in position order (contiguous range per thread) ------
+    // ---- 3b. leaves below pi* are taken; leaves at pi* are collected --------------------
     {
-        int lo_i[kMaxL], hi_i[kMaxL], mine[kMaxL], incl[kMaxL];
-#pragma unroll
-        for (int l = 0; l < kMaxL; ++l) {
-            const int per = (N[l] + kSelThreads - 1) / kSelThreads;
-            lo_i[l] = min(N[l], tid * per);
-            hi_i[l] = min(N[l], lo_i[l] + per);
-            mine[l] = 0;
-            if (l < L && s_pstar[l] < 256) {
-                const int ps = s_pstar[l];
-                for (int i = lo_i[l]; i < hi_i[l]; ++i)
-                    if (prio[l * C + i] == ps) mine[l] += cnts[l * C + i];
-            }
-            incl[l] = mine[l];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl[l], o);
-                if (lane >= o) incl[l] += y;
-            }
-            if (lane == 31) s_wsum[l][warp] = incl[l];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int l = 0; l < kMaxL; ++l) {
-            if (l >= L) break;
-            int run = incl[l] - mine[l];
-            for (int w = 0; w < warp; ++w) run += s_wsum[l][w];
-            const int ps = s_pstar[l], need = s_need[l];
-            int* ch = chosen + l * n_cand;
-            for (int i = lo_i[l]; i < hi_i[l]; ++i) {
-                const int pr = prio[l * C + i];
-                bool take = pr < ps;
-                if (pr == ps) {
-                    take = run < need;
-                    run += cnts[l * C + i];
-                }
-                if (take) {
-                    const int slot = atomicAdd(&s_nch[l], 1);
-                    if (slot < n_cand) ch[slot] = i;
-                }
+        const int ps0 = s_pstar[0], ps1 = L > 1 ? s_pstar[1] : 0;
+        for (int i = tid; i < Ntot; i += kSelThreads) {
+            const int l = i < N[0] ? 0 : 1;
+            const int li = i - (l ? N[0] : 0);
+            const int pr = prio[l * C + li];
+            const int ps = l ? ps1 : ps0;
+            if (pr < ps) {
+                const int slot = atomicAdd(&s_nch[l], 1);
+                if (slot < n_cand) chosen[l * n_cand + slot] = li;
+            } else if (pr == ps) {
+                const int slot = atomicAdd(&s_ntie[l], 1);
+                if (slot < kTieCap) tie[l * kTieCap + slot] = li;
             }
         }
     }
     __syncthreads();
+    // ---- 3c. leaves at pi*, in position order, while tokens taken before them < need ------
+    for (int l = 0; l < L; ++l) {
+        const int ntie = s_ntie[l];
+        if (ntie == 0) continue;
+        if (ntie <= kTieCap) {
+            // rank by counting (positions are distinct), then a prefix walk by warp 0
+            int* tl = tie + l * kTieCap;
+            const uint4* lrec = recs + v.leaf_base(u, l);
+            int mine = 0, r = 0;
+            const bool act = tid < ntie;
+            if (act) {
+                mine = tl[tid];
+                for (int j = 0; j < ntie; ++j) r += tl[j] < mine;
+            }
+            __syncthreads();
+            if (act) tl[r] = mine;
+            __syncthreads();
+            if (warp == 0) {
+                const int need = s_need[l];
+                int run = 0;
+                for (int k0 = 0; k0 < ntie && run < need; k0 += 32) {
+                    const int k = k0 + lane;
+                    const int li = k < ntie ? tl[k] : 0;
+                    const int c = k < ntie ? rec_cnt(__ldg(lrec + li)) : 0;
+                    int inc = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                        if (lane >= o) inc += y;
+                    }
+                    const bool take = k < ntie && run + inc - c < need;
+                    const unsigned tm = __ballot_sync(0xffffffffu, take);
+                    int base = 0;
+                    if (lane == 0 && tm) base = atomicAdd(&s_nch[l], __popc(tm));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    if (take) {
+                        const int slot = base + __popc(tm & ((1u << lane) - 1u));
+                        if (slot < n_cand) chosen[l * n_cand + slot] = li;
+                    }
+                    run += __shfl_sync(0xffffffffu, inc, 31);
+                }
+            }
+        } else {
+            // many leaves at pi*: each thread walks a contiguous range of positions
+            const int per = (N[l] + kSelThreads - 1) / kSelThreads;
+            const int lo_i = min(N[l], tid * per), hi_i = min(N[l], lo_i + per);
+            const int ps = s_pstar[l], need = s_need[l];
+            const uint4* lrec = recs + v.leaf_base(u, l);
+            int mine = 0;
+            for (int i = lo_i; i < hi_i; ++i)
+                if (prio[l * C + i] == ps) mine += rec_cnt(__ldg(lrec + i));
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) s_wsum[l][warp] = incl;
+            __syncthreads();
+            int run = incl - mine;
+            for (int w = 0; w < warp; ++w) run += s_wsum[l][w];
+            for (int i = lo_i; i < hi_i; ++i) {
+                if (prio[l * C + i] != ps) continue;
+                if (run < need) {
+                    const int slot = atomicAdd(&s_nch[l], 1);
+                    if (slot < n_cand) chosen[l * n_cand + slot] = i;
+                }
+                run += rec_cnt(__ldg(lrec + i));
+            }
+        }
+        __syncthreads();
+    }
 
-    // ---- 3c. metadata of the taken leaves (one parallel round) -------------------------
+    // ---- 3d. records of the taken leaves (one parallel round), offsets, page bitmap ------
     for (int l = 0; l < L; ++l) {
         const int nch = min(s_nch[l], n_cand);
         for (int k = tid; k < nch; k += kSelThreads)
-            cmeta[l * n_cand + k] = __ldg(v.leaf_meta + v.leaf_base(u, l) + chosen[l * n_cand + k]);
+            cmeta[l * n_cand + k] = __ldg(recs + v.leaf_base(u, l) + chosen[l * n_cand + k]).z;
     }
     __syncthreads();
-    // exclusive offsets of the taken leaves' slots (warp l), composite-0 page bitmap
     if (warp < L) {
         const int l = warp;
         const int nch = min(s_nch[l], n_cand);
@@ -385,7 +542,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     __syncthreads();
     const int ncand = min(s_ncand, sort_cap);
 
-    // ---- 5. exact rescoring, 4 rows per warp instruction ---------------------------------
+    // ---- 5. exact rescoring, 4 rows per warp instruction; per-page minimum key --------------
     {
         const int g8 = lane >> 3, p = lane & 7;
         // lane p evaluates lane partials p, p+8, p+16, p+24 of the fixed order:
@@ -396,6 +553,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 #pragma unroll
             for (int i = 0; i < 4; ++i) qv[4 * j + i] = s_qsel[4 * p + 32 * j + i];
         const T* pk = reinterpret_cast<const T*>(v.page_k) + (long long)u * C * P * kD;
+        const int hmask = hcap - 1;
         for (int r0 = warp * 4 * kRowUnr; r0 < ncand; r0 += kSelWarps * 4 * kRowUnr) {
             Chunk<T> ch[kRowUnr][4];
             int tk[kRowUnr], lc[kRowUnr];
@@ -429,113 +587,172 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 4));
                 b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 2));
                 b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 1));
-                const int r = r0 + 4 * k + g8;
                 if (p == 0 && tk[k] >= 0) {
-                    skey[r] = ((unsigned long long)score_key_desc(b) << 32) | (unsigned)tk[k];
-                    sval[r] = lc[k] / P;
-                }
-            }
-        }
-    }
-    int npow = 1;
-    while (npow < ncand) npow <<= 1;
-    for (int c = ncand + tid; c < npow; c += kSelThreads) {
-        skey[c] = ~0ull;
-        sval[c] = -1;
-    }
-    __syncthreads();
-
-    // ---- 6a. bitonic sort by (score desc, token asc) -----------------------------------
-    for (int k = 2; k <= npow; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < npow; i += kSelThreads) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const unsigned long long a = skey[i], b = skey[ixj];
-                    if ((a > b) == ((i & k) == 0)) {
-                        skey[i] = b;
-                        skey[ixj] = a;
-                        const int t = sval[i];
-                        sval[i] = sval[ixj];
-                        sval[ixj] = t;
+                    const unsigned long long key =
+                        ((unsigned long long)score_key_desc(b) << 32) | (unsigned)tk[k];
+                    const int pg = lc[k] / P;
+                    unsigned h = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
+                    for (int probe = 0; probe < hcap; ++probe) {
+                        const int old = atomicCAS(&hpage[h], -1, pg);
+                        if (old == -1 || old == pg) {
+                            atomicMin(&hkey[h], key);
+                            break;
+                        }
+                        h = (h + 1) & (unsigned)hmask;
                     }
                 }
             }
-            __syncthreads();
         }
     }
-
-    // ---- 6b. walk: first occurrences of pages in rank order -----------------------------
-    if (warp == 0) {
-        int taken = 0;
-        int32_t* out = page_ids + (long long)u * n_sel;
-        for (int c0 = 0; c0 < ncand && taken < n_sel; c0 += 32) {
-            const int c = c0 + lane;
-            const int pg = c < ncand ? sval[c] : -1;
-            bool fresh = pg >= 0 && pg < C && !((bm_taken[pg >> 5] >> (pg & 31)) & 1u);
-            const unsigned peers = __match_any_sync(0xffffffffu, pg);
-            fresh = fresh && (lane == __ffs(peers) - 1);
-            const unsigned fm = __ballot_sync(0xffffffffu, fresh);
-            if (fresh) {
-                const int r = taken + __popc(fm & ((1u << lane) - 1u));
-                if (r < n_sel) {
-                    out[r] = pg;
-                    atomicOr(&bm_taken[pg >> 5], 1u << (pg & 31));  // lanes may share a word
-                }
-            }
-            taken = min(n_sel, taken + __popc(fm));
-            __syncwarp();
+    __syncthreads();
+    // compact the occupied hash slots: one entry per distinct page
+    if (tid == 0) s_npg = 0;
+    __syncthreads();
+    for (int h0 = warp * 32; h0 < hcap; h0 += kSelThreads) {
+        const int h = h0 + lane;
+        const int pg = h < hcap ? hpage[h] : -1;
+        const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
+        int base = 0;
+        if (lane == 0 && km) base = atomicAdd(&s_npg, __popc(km));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (pg >= 0) {
+            const int pos = base + __popc(km & ((1u << lane) - 1u));
+            skey[pos] = hkey[h];
+            sval[pos] = pg;
         }
-        for (int r = taken + lane; r < n_sel; r += 32) out[r] = -1;
-        if (lane == 0) n_pages_out[u] = taken;
-        if (stats) {
-            __syncwarp();
-            int tok_sel = 0;
-            for (int r = lane; r < taken; r += 32) tok_sel += v.list_cnt[v.leaf_base(u, 0) + out[r]];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
-            if (lane == 0) {
-                stats[4 * u + 0] = Ntot;
-                stats[4 * u + 1] = ncand;
-                stats[4 * u + 2] = tok_sel;
-                stats[4 * u + 3] = s_nraw;
+    }
+    __syncthreads();
+    const int npg = s_npg;  // <= ncand <= sort_cap
+    const int taken = min(n_sel, npg);
+    int32_t* out = page_ids + (long long)u * n_sel;
+
+    // ---- 6. the n_sel smallest page keys in order ------------------------------------------
+    if (n_sel <= kTopK) {
+        unsigned long long tk = ~0ull;
+        int tv = -1;
+        for (int j0 = warp * 32; j0 < npg; j0 += kSelThreads) {  // warp-uniform
+            const int j = j0 + lane;
+            unsigned long long k = j < npg ? skey[j] : ~0ull;
+            int vv = j < npg ? sval[j] : -1;
+            warp_sort32(k, vv, lane);
+            warp_merge32(tk, tv, k, vv, lane);
+        }
+        topk[warp * kTopK + lane] = tk;
+        topv[warp * kTopK + lane] = tv;
+        __syncthreads();
+        if (warp == 0) {
+            unsigned long long a = topk[lane];
+            int av = topv[lane];
+            for (int w = 1; w < kSelWarps; ++w)
+                warp_merge32(a, av, topk[w * kTopK + lane], topv[w * kTopK + lane], lane);
+            if (lane < n_sel) out[lane] = lane < taken ? av : -1;
+        }
+    } else {
+        int npow = 1;
+        while (npow < npg) npow <<= 1;
+        for (int c = npg + tid; c < npow; c += kSelThreads) {
+            skey[c] = ~0ull;
+            sval[c] = -1;
+        }
+        __syncthreads();
+        for (int k = 2; k <= npow; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = tid; i < npow; i += kSelThreads) {
+                    const int ixj = i ^ j;
+                    if (ixj > i) {
+                        const unsigned long long a = skey[i], b = skey[ixj];
+                        if ((a > b) == ((i & k) == 0)) {
+                            skey[i] = b;
+                            skey[ixj] = a;
+                            const int t = sval[i];
+                            sval[i] = sval[ixj];
+                            sval[ixj] = t;
+                        }
+                    }
+                }
+                __syncthreads();
             }
+        }
+        for (int r = tid; r < n_sel; r += kSelThreads) out[r] = r < taken ? sval[r] : -1;
+    }
+    __syncthreads();
+    if (tid == 0) n_pages_out[u] = taken;
+    if (stats && warp == 0) {
+        int tok_sel = 0;
+        for (int r = lane; r < taken; r += 32) tok_sel += v.list_cnt[v.leaf_base(u, 0) + out[r]];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
+        if (lane == 0) {
+            stats[4 * u + 0] = Ntot;
+            stats[4 * u + 1] = ncand;
+            stats[4 * u + 2] = tok_sel;
+            stats[4 * u + 3] = s_nraw;
         }
     }
     if (tid == 0 && s_ncand > sort_cap) set_status(v.status, ICE_ERR_CAPACITY);
 }
 
-static int sort_capacity(int L, int P, int n_cand) {
+static void select_caps(int L, int P, int n_cand, int* sort_cap, int* hcap) {
     const int cand_cap = L * (n_cand + P - 1);
-    int sort_cap = 1;
-    while (sort_cap < cand_cap) sort_cap <<= 1;
-    return sort_cap;
-}
-
-cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
-                          int32_t* page_ids, int32_t* n_pages, int32_t* stats, cudaStream_t s) {
-    const int sort_cap = sort_capacity(v.L, v.P, n_cand);
-    const int bytes = sel_layout(v.C, v.L, n_cand, sort_cap).end;
-    cudaError_t e;
-    if (v.dtype == ICE_BF16) {
-        e = cudaFuncSetAttribute(select_kernel<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        select_kernel<__nv_bfloat16><<<v.U, kSelThreads, bytes, s>>>(
-            v, (const __nv_bfloat16*)q, n_sel, n_cand, sort_cap, page_ids, n_pages, stats);
-    } else {
-        e = cudaFuncSetAttribute(select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 bytes);
-        if (e != cudaSuccess) return e;
-        select_kernel<float><<<v.U, kSelThreads, bytes, s>>>(v, (const float*)q, n_sel, n_cand,
-                                                            sort_cap, page_ids, n_pages, stats);
-    }
-    return cudaGetLastError();
+    int s = 1;
+    while (s < cand_cap) s <<= 1;
+    *sort_cap = s;
+    *hcap = s;  // at least one slot per candidate: probing always ends
 }
 
 // Dynamic shared memory the select kernel needs (host check before launch).
 int select_smem_bytes(long long C, int L, int P, int n_cand) {
-    return sel_layout(C, L, n_cand, sort_capacity(L, P, n_cand)).end;
+    int sc, hc;
+    select_caps(L, P, n_cand, &sc, &hc);
+    return sel_layout(C, L, n_cand, sc, hc).end;
+}
+
+template <typename T, int G>
+static void launch_select_t(const IndexView& v, const void* q, int n_sel, int n_cand, int sort_cap,
+                            int hcap, int bytes, int32_t* page_ids, int32_t* n_pages,
+                            int32_t* stats, cudaStream_t s) {
+    select_kernel<T, G><<<v.U, kSelThreads, bytes, s>>>(v, (const T*)q, n_sel, n_cand, sort_cap,
+                                                        hcap, page_ids, n_pages, stats);
+}
+
+template <typename T>
+static cudaError_t launch_select_dt(const IndexView& v, const void* q, int n_sel, int n_cand,
+                                    int sort_cap, int hcap, int bytes, int32_t* page_ids,
+                                    int32_t* n_pages, int32_t* stats, cudaStream_t s) {
+    switch (v.G) {
+        case 1: launch_select_t<T, 1>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
+        case 2: launch_select_t<T, 2>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
+        case 4: launch_select_t<T, 4>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
+        case 8: launch_select_t<T, 8>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
+                          int32_t* page_ids, int32_t* n_pages, int32_t* stats, cudaStream_t s) {
+    int sort_cap, hcap;
+    select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
+    const int bytes = sel_layout(v.C, v.L, n_cand, sort_cap, hcap).end;
+    if (v.dtype == ICE_BF16)
+        return launch_select_dt<__nv_bfloat16>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids,
+                                               n_pages, stats, s);
+    return launch_select_dt<float>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages,
+                                   stats, s);
+}
+
+// Raise the dynamic shared memory limit of the select kernels once per device.
+cudaError_t select_prepare() {
+    const int lim = 200 * 1024;
+    cudaError_t e = cudaSuccess;
+#define ICE_SET_SMEM(T, G)                                                                     \
+    if (e == cudaSuccess)                                                                      \
+        e = cudaFuncSetAttribute(select_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    ICE_SET_SMEM(__nv_bfloat16, 1) ICE_SET_SMEM(__nv_bfloat16, 2) ICE_SET_SMEM(__nv_bfloat16, 4)
+    ICE_SET_SMEM(__nv_bfloat16, 8) ICE_SET_SMEM(float, 1) ICE_SET_SMEM(float, 2)
+    ICE_SET_SMEM(float, 4) ICE_SET_SMEM(float, 8)
+#undef ICE_SET_SMEM
+    return e;
 }
 
 }  // namespace ice

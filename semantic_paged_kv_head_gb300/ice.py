@@ -232,10 +232,16 @@ class IceIndex:
         for _ in range(L):
             lk = buf[o:o + C * 16].view(np.uint32).reshape(C, 4)
             o += C * 16
-            cell = buf[o:o + C * 16].reshape(C, 16)
+            rec = buf[o:o + C * 16].reshape(C, 16)
             o += C * 16
-            meta = buf[o:o + C * 4].view(np.uint32)
-            o += C * 4
+            meta = rec[:, 8:12].copy().view(np.uint32).reshape(C)
+            lo = rec[:, :8].astype(np.int32)
+            t = lk[:, 3].astype(np.int32)
+            # known bits of code j at prefix length t (Morton order, code j at bit j of each byte)
+            jj = np.arange(8)[None, :]
+            bj = np.where(t[:, None] >= 64, 8, np.clip((t[:, None] + 7 - jj) >> 3, 0, 8))
+            hi = lo | ((1 << (8 - bj)) - 1)
+            rec_t = rec[:, 12:16].copy().view(np.uint32).reshape(C).astype(np.int32)
             cnt = buf[o:o + C * 4].view(np.int32)
             o += C * 4
             stok = buf[o:o + C * P * 4].view(np.int32).reshape(C, P)
@@ -243,8 +249,8 @@ class IceIndex:
             skey = buf[o:o + C * P * 8].view(np.uint64).reshape(C, P)
             o += C * P * 8
             pm = lk[:, 0].astype(np.uint64) | (lk[:, 1].astype(np.uint64) << np.uint64(32))
-            out["comp"].append({"pm": pm, "pt": lk[:, 2].copy(), "t": lk[:, 3].astype(np.int32),
-                                "lo": cell[:, :8].astype(np.int32), "hi": cell[:, 8:].astype(np.int32),
+            out["comp"].append({"pm": pm, "pt": lk[:, 2].copy(), "t": t, "rec_t": rec_t,
+                                "lo": lo, "hi": hi,
                                 "id": (meta >> 8).astype(np.int32), "cnt": (meta & 0xFF).astype(np.int32),
                                 "list_cnt": cnt.copy(), "slot_tok": stok.copy(), "slot_key": skey.copy()})
         out["tok_loc"] = buf[o:o + 4 * self.info().max_tokens].view(np.int32).copy()

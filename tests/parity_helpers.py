@@ -43,6 +43,7 @@ def compare_index(gdump, orc, unit_label=""):
         assert N == len(od["t"]), (unit_label, l, N, len(od["t"]))
         assert gdump["next_id"][l] == orc.next_id(l), (unit_label, l)
         assert np.array_equal(comp["t"][:N], od["t"]), (unit_label, l)
+        assert np.array_equal(comp["rec_t"][:N], od["t"]), (unit_label, l)
         assert np.array_equal(comp["pm"][:N], od["pm"]), (unit_label, l)
         assert np.array_equal(comp["pt"][:N], od["pt"]), (unit_label, l)
         assert np.array_equal(comp["id"][:N], od["id"]), (unit_label, l)
