@@ -133,6 +133,18 @@ int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page
                int32_t* n_pages, int32_t* stats, void* stream);
 
 /*
+ * ice_select_attn - ice_select followed by ice_sparse_attn over the selected
+ * pages, in one kernel launch per call (each unit's pages are attended as soon
+ * as they are known, without a round trip of the page list through memory).
+ * Arguments and results are those of the two calls: page_ids, n_pages and
+ * stats as in ice_select, out as in ice_sparse_attn with page_stride =
+ * token_budget / page_size. The pages chosen and the attention computed are
+ * the same as with the two separate calls.
+ */
+int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
+                    int32_t* n_pages, int32_t* stats, void* out, void* stream);
+
+/*
  * ice_sparse_attn - attention of each query head over every token of the
  * selected pages (Figure 2 step 3).
  *

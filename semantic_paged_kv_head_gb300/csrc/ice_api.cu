@@ -229,20 +229,33 @@ int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
     return ICE_OK;
 }
 
-int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
-               int32_t* n_pages, int32_t* stats, void* stream) {
+static int select_common(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
+                         int32_t* n_pages, int32_t* stats, void* out, void* stream) {
     if (!ix || !q || !page_ids || !n_pages || !aligned16(q)) return ICE_ERR_INVALID_ARG;
+    if (out && !aligned16(out)) return ICE_ERR_INVALID_ARG;
     const int P = ix->p.page_size;
     if (token_budget < P || token_budget % P) return ICE_ERR_INVALID_ARG;
     const int n_sel = token_budget / P;
     if (n_sel > 512) return ICE_ERR_UNSUPPORTED;
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
     if (n_cand > (1 << 16)) return ICE_ERR_UNSUPPORTED;
-    if (select_smem_bytes(ix->C, ix->p.n_composite, P, n_cand) > 200 * 1024)
+    if (select_smem_bytes(ix->C, ix->p.n_composite, P, n_cand, n_sel, ix->G, out != nullptr) >
+        200 * 1024)
         return ICE_ERR_UNSUPPORTED;
-    cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, stats,
+    cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, stats, out,
                                   (cudaStream_t)stream);
     return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
+}
+
+int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
+               int32_t* n_pages, int32_t* stats, void* stream) {
+    return select_common(ix, q, token_budget, page_ids, n_pages, stats, nullptr, stream);
+}
+
+int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
+                    int32_t* n_pages, int32_t* stats, void* out, void* stream) {
+    if (!out) return ICE_ERR_INVALID_ARG;
+    return select_common(ix, q, token_budget, page_ids, n_pages, stats, out, stream);
 }
 
 int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const int32_t* n_pages,

@@ -261,14 +261,16 @@ cudaError_t build_phase2(const IndexView& v, const void* keys, const void* value
                          BuildScratch& s, int cur, cudaStream_t st);
 cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st);
 void scratch_free(BuildScratch& s, cudaStream_t st);
-int select_smem_bytes(long long C, int L, int P, int n_cand);
+int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, bool fused);
 cudaError_t select_prepare();
 
 // ---- launchers (implemented in the .cu files) --------------------------------------
 cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, long long tok,
                           cudaStream_t s);
+// out == nullptr: select only; otherwise select and attend over the selection.
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
-                          int32_t* page_ids, int32_t* n_pages, int32_t* stats, cudaStream_t s);
+                          int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                          cudaStream_t s);
 cudaError_t launch_attn(const IndexView& v, const void* q, const int32_t* page_ids,
                         const int32_t* n_pages, int page_stride, void* out, cudaStream_t s);
 

@@ -44,13 +44,14 @@ constexpr int kTieCap = 256;  // leaves at pi* ordered by rank counting; more ->
 constexpr int kTopK = 32;     // warp top-k width
 
 struct SelSmem {
-    int prio, hist, chosen, cmeta, coff, tie, bm0, keys, vals, hpage, hkey, top, end;
+    int prio, hist, chosen, cmeta, coff, tie, tcnt, bm0, keys, vals, hpage, hkey, top, sel, toff,
+        part, end;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
 
 __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, int sort_cap,
-                                              int hcap) {
+                                              int hcap, int n_sel, int part_floats) {
     SelSmem s;
     int o = 0;
     s.prio = o; o = align16(o + L * (int)C);
@@ -59,12 +60,16 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
     s.cmeta = o; o = align16(o + L * n_cand * 4);
     s.coff = o; o = align16(o + L * (n_cand + 1) * 4);
     s.tie = o; o = align16(o + L * kTieCap * 4);
+    s.tcnt = o; o = align16(o + L * kTieCap * 4);
     s.bm0 = o; o = align16(o + (int)((C + 31) / 32) * 4);
     s.keys = o; o = align16(o + sort_cap * 8);
     s.vals = o; o = align16(o + sort_cap * 4);
     s.hpage = o; o = align16(o + hcap * 4);
     s.hkey = o; o = align16(o + hcap * 8);
     s.top = o; o = align16(o + kSelWarps * kTopK * 12);
+    s.sel = o; o = align16(o + n_sel * 4);
+    s.toff = o; o = align16(o + (n_sel + 1) * 4);
+    s.part = o; o = align16(o + part_floats * 4);
     s.end = o;
     return s;
 }
@@ -184,29 +189,160 @@ template <> struct Chunk<float> {
     }
 };
 
+// Attention of the G query heads of unit u over every token of the selected
+// pages (the fused tail of the select kernel). A warp takes tokens w, w + 16, ...
+// of the flattened page list, one token per warp instruction (lane l owns
+// dimensions 4l .. 4l + 3), with an fp32 online softmax per warp; the 16 warp
+// partials are merged in a fixed order in shared memory.
 template <typename T, int G>
+__device__ __forceinline__ void attend_selected(const IndexView& v, int u, const T* __restrict__ q,
+                                                int npg, const int* s_sel, int* s_toff,
+                                                int* s_ntok, float* part /* [warps][G][kD+2] */,
+                                                T* __restrict__ out) {
+    constexpr int kTokRound = 2;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = v.P;
+    // token offsets of the selected pages (warp 0), counts read in parallel
+    if (warp == 0) {
+        int carry = 0;
+        for (int r0 = 0; r0 < npg; r0 += 32) {
+            const int r = r0 + lane;
+            int c = 0;
+            if (r < npg) {
+                const int pg = s_sel[r];
+                if (pg >= 0 && pg < v.C) c = v.list_cnt[v.leaf_base(u, 0) + pg];
+                c = c < 0 ? 0 : (c > P ? P : c);
+            }
+            int inc = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (r < npg) s_toff[r] = carry + inc - c;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) {
+            s_toff[npg] = carry;
+            *s_ntok = carry;
+        }
+    }
+    float qa[G][4];
+    const float sc = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        load4(q + ((long long)u * G + h) * kD + 4 * lane, qa[h]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qa[h][k] *= sc;
+    }
+    __syncthreads();
+    const int ntok = *s_ntok;
+    float m[G], lsum[G], acc[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[h][k] = 0.0f;
+    }
+    const T* pk = reinterpret_cast<const T*>(v.page_k);
+    const T* pv = reinterpret_cast<const T*>(v.page_v);
+    for (int j0 = warp; j0 < ntok; j0 += kSelWarps * kTokRound) {  // warp-uniform
+        float kx[kTokRound][4], vx[kTokRound][4];
+#pragma unroll
+        for (int t = 0; t < kTokRound; ++t) {
+            const int j = j0 + t * kSelWarps;
+            if (j < ntok) {
+                int lo = 0, hi = npg;  // last page r with s_toff[r] <= j
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_toff[mid] <= j) lo = mid; else hi = mid;
+                }
+                const long long row = v.page_row(u, s_sel[lo], j - s_toff[lo]);
+                load4_nc(pk + row * kD + 4 * lane, kx[t]);
+                load4_nc(pv + row * kD + 4 * lane, vx[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kTokRound; ++t) {
+            if (j0 + t * kSelWarps >= ntok) break;  // warp-uniform
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float a = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) a = fmaf(qa[h][k], kx[t][k], a);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                const float mn = fmaxf(m[h], a);
+                const float corr = exp2f(m[h] - mn);
+                const float p = exp2f(a - mn);
+                lsum[h] = lsum[h] * corr + p;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[h][k] = fmaf(p, vx[t][k], acc[h][k] * corr);
+                m[h] = mn;
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float* pw = part + (warp * G + h) * (kD + 2);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pw[4 * lane + k] = acc[h][k];
+        if (lane == 0) {
+            pw[kD] = m[h];
+            pw[kD + 1] = lsum[h];
+        }
+    }
+    __syncthreads();
+    T* ou = out + (long long)u * G * kD;
+    for (int e = tid; e < G * kD; e += kSelThreads) {
+        const int h = e / kD, dcol = e % kD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kSelWarps; ++w) M = fmaxf(M, part[(w * G + h) * (kD + 2) + kD]);
+        float Lt = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kSelWarps; ++w) {
+                const float* pw = part + (w * G + h) * (kD + 2);
+                if (pw[kD] == -INFINITY) continue;
+                const float cf = exp2f(pw[kD] - M);
+                Lt = fmaf(pw[kD + 1], cf, Lt);
+                O = fmaf(pw[dcol], cf, O);
+            }
+        }
+        ou[e] = from_f<T>(Lt > 0.0f ? O / Lt : 0.0f);
+    }
+}
+
+template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
-    int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out, int32_t* __restrict__ stats) {
+    int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out, int32_t* __restrict__ stats,
+    T* __restrict__ attn_out) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
     __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL], s_ntie[kMaxL];
-    __shared__ int s_ncand, s_nraw, s_npg;
+    __shared__ int s_ncand, s_nraw, s_npg, s_ntok;
     __shared__ int s_wsum[kMaxL][kSelWarps];
 
     const int u = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = v.L, P = v.P;
     const long long C = v.C;
-    const SelSmem lay = sel_layout(C, L, n_cand, sort_cap, hcap);
+    const SelSmem lay = sel_layout(C, L, n_cand, sort_cap, hcap, n_sel,
+                                   FUSED ? kSelWarps * G * (kD + 2) : 0);
     unsigned char* prio = smem + lay.prio;                            // [L][C]
     int* hist = reinterpret_cast<int*>(smem + lay.hist);              // [L][kSubH][256]
     int* chosen = reinterpret_cast<int*>(smem + lay.chosen);          // [L][n_cand] leaf index
     unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);  // [L][n_cand] id|count
     int* coff = reinterpret_cast<int*>(smem + lay.coff);              // [L][n_cand + 1]
     int* tie = reinterpret_cast<int*>(smem + lay.tie);                // [L][kTieCap]
+    int* tcnt = reinterpret_cast<int*>(smem + lay.tcnt);              // [L][kTieCap]
+    int* s_sel = reinterpret_cast<int*>(smem + lay.sel);              // [n_sel] selected pages
+    int* s_toff = reinterpret_cast<int*>(smem + lay.toff);            // [n_sel + 1] token offsets
     unsigned* bm0 = reinterpret_cast<unsigned*>(smem + lay.bm0);
     unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.keys);
     int* sval = reinterpret_cast<int*>(smem + lay.vals);
@@ -231,20 +367,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         load4(ud + 4 * lane, wdir);
         wlast = ud[kD];
     }
-    for (int l = 0; l < L; ++l) N[l] = N[l] < 0 ? 0 : (N[l] > C ? (int)C : N[l]);
-    const int Ntot = N[0] + N[1];
+    // first batch of composite 0, requested before its leaf count arrives (records
+    // past the count are read but never used; the capacity bounds the reads)
     uint4 rb[kScanUnr];
-    auto load_batch = [&](int base) {
+    {
+        const uint4* r0 = recs + v.leaf_base(u, 0);
 #pragma unroll
         for (int k = 0; k < kScanUnr; ++k) {
-            const int i = base + k * kSelThreads + tid;
-            if (i < Ntot) {
-                const int l = i < N[0] ? 0 : 1;
-                rb[k] = __ldg(recs + v.leaf_base(u, l) + (i - (l ? N[0] : 0)));
-            }
+            const int i = k * kSelThreads + tid;
+            if (i < C) rb[k] = __ldg(r0 + i);
         }
-    };
-    load_batch(0);
+    }
+    for (int l = 0; l < L; ++l) N[l] = N[l] < 0 ? 0 : (N[l] > C ? (int)C : N[l]);
+    const int Ntot = N[0] + N[1];
 
     // query prep
     {
@@ -311,18 +446,26 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             qc[l][3] = bytes_to_h2(hi4, 0x4342u);
         }
         const int sub = warp >> 1;
-        for (int base = 0; base < Ntot; base += kScanUnr * kSelThreads) {
-            if (base > 0) load_batch(base);
 #pragma unroll
-            for (int k = 0; k < kScanUnr; ++k) {
-                const int i = base + k * kSelThreads + tid;
-                if (i < Ntot) {
-                    const int l = i < N[0] ? 0 : 1;
-                    const int li = i - (l ? N[0] : 0);
-                    const int pr = leaf_priority(rb[k], l ? qc[1] : qc[0], s_width);
-                    const int cn = rec_cnt(rb[k]);
-                    st_shared_u8(prio + l * C + li, pr);
-                    atomicAdd(&hist[(l * kSubH + sub) * 256 + pr], cn);
+        for (int l = 0; l < kMaxL; ++l) {
+            if (l >= L) break;
+            const uint4* rl = recs + v.leaf_base(u, l);
+            for (int base = 0; base < N[l]; base += kScanUnr * kSelThreads) {
+                if (l > 0 || base > 0) {
+#pragma unroll
+                    for (int k = 0; k < kScanUnr; ++k) {
+                        const int i = base + k * kSelThreads + tid;
+                        if (i < N[l]) rb[k] = __ldg(rl + i);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kScanUnr; ++k) {
+                    const int i = base + k * kSelThreads + tid;
+                    if (i < N[l]) {
+                        const int pr = leaf_priority(rb[k], qc[l], s_width);
+                        st_shared_u8(prio + l * C + i, pr);
+                        atomicAdd(&hist[(l * kSubH + sub) * 256 + pr], rec_cnt(rb[k]));
+                    }
                 }
             }
         }
@@ -392,14 +535,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             // rank by counting (positions are distinct), then a prefix walk by warp 0
             int* tl = tie + l * kTieCap;
             const uint4* lrec = recs + v.leaf_base(u, l);
-            int mine = 0, r = 0;
+            int* tc = tcnt + l * kTieCap;
+            int mine = 0, r = 0, mc = 0;
             const bool act = tid < ntie;
             if (act) {
                 mine = tl[tid];
+                mc = rec_cnt(__ldg(lrec + mine));  // in flight during the counting
                 for (int j = 0; j < ntie; ++j) r += tl[j] < mine;
             }
             __syncthreads();
-            if (act) tl[r] = mine;
+            if (act) {
+                tl[r] = mine;
+                tc[r] = mc;
+            }
             __syncthreads();
             if (warp == 0) {
                 const int need = s_need[l];
@@ -407,7 +555,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 for (int k0 = 0; k0 < ntie && run < need; k0 += 32) {
                     const int k = k0 + lane;
                     const int li = k < ntie ? tl[k] : 0;
-                    const int c = k < ntie ? rec_cnt(__ldg(lrec + li)) : 0;
+                    const int c = k < ntie ? tc[k] : 0;
                     int inc = c;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
@@ -640,12 +788,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         topk[warp * kTopK + lane] = tk;
         topv[warp * kTopK + lane] = tv;
         __syncthreads();
-        if (warp == 0) {
-            unsigned long long a = topk[lane];
-            int av = topv[lane];
-            for (int w = 1; w < kSelWarps; ++w)
-                warp_merge32(a, av, topk[w * kTopK + lane], topv[w * kTopK + lane], lane);
-            if (lane < n_sel) out[lane] = lane < taken ? av : -1;
+        // pairwise merge tree over the warps' lists: warp w takes in w + s
+        for (int st = 1; st < kSelWarps; st <<= 1) {
+            if ((warp & (2 * st - 1)) == 0) {
+                unsigned long long a = topk[warp * kTopK + lane];
+                int av = topv[warp * kTopK + lane];
+                warp_merge32(a, av, topk[(warp + st) * kTopK + lane],
+                             topv[(warp + st) * kTopK + lane], lane);
+                topk[warp * kTopK + lane] = a;
+                topv[warp * kTopK + lane] = av;
+            }
+            __syncthreads();
+        }
+        if (warp == 0 && lane < n_sel) {
+            const int pg = lane < taken ? topv[lane] : -1;
+            out[lane] = pg;
+            s_sel[lane] = pg;
         }
     } else {
         int npow = 1;
@@ -673,13 +831,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 __syncthreads();
             }
         }
-        for (int r = tid; r < n_sel; r += kSelThreads) out[r] = r < taken ? sval[r] : -1;
+        for (int r = tid; r < n_sel; r += kSelThreads) {
+            const int pg = r < taken ? sval[r] : -1;
+            out[r] = pg;
+            s_sel[r] = pg;
+        }
     }
     __syncthreads();
     if (tid == 0) n_pages_out[u] = taken;
     if (stats && warp == 0) {
         int tok_sel = 0;
-        for (int r = lane; r < taken; r += 32) tok_sel += v.list_cnt[v.leaf_base(u, 0) + out[r]];
+        for (int r = lane; r < taken; r += 32) tok_sel += v.list_cnt[v.leaf_base(u, 0) + s_sel[r]];
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
         if (lane == 0) {
@@ -690,64 +852,74 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         }
     }
     if (tid == 0 && s_ncand > sort_cap) set_status(v.status, ICE_ERR_CAPACITY);
+    if constexpr (FUSED) attend_selected<T, G>(v, u, q, taken, s_sel, s_toff, &s_ntok,
+                                              reinterpret_cast<float*>(smem + lay.part), attn_out);
 }
 
 static void select_caps(int L, int P, int n_cand, int* sort_cap, int* hcap) {
     const int cand_cap = L * (n_cand + P - 1);
-    int s = 1;
-    while (s < cand_cap) s <<= 1;
-    *sort_cap = s;
-    *hcap = s;  // at least one slot per candidate: probing always ends
+    int c = 1;
+    while (c < cand_cap) c <<= 1;
+    *sort_cap = c;
+    *hcap = c;  // at least one slot per candidate: probing always ends
 }
 
 // Dynamic shared memory the select kernel needs (host check before launch).
-int select_smem_bytes(long long C, int L, int P, int n_cand) {
+int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, bool fused) {
     int sc, hc;
     select_caps(L, P, n_cand, &sc, &hc);
-    return sel_layout(C, L, n_cand, sc, hc).end;
+    return sel_layout(C, L, n_cand, sc, hc, n_sel, fused ? kSelWarps * G * (kD + 2) : 0).end;
 }
 
 template <typename T, int G>
-static void launch_select_t(const IndexView& v, const void* q, int n_sel, int n_cand, int sort_cap,
-                            int hcap, int bytes, int32_t* page_ids, int32_t* n_pages,
-                            int32_t* stats, cudaStream_t s) {
-    select_kernel<T, G><<<v.U, kSelThreads, bytes, s>>>(v, (const T*)q, n_sel, n_cand, sort_cap,
-                                                        hcap, page_ids, n_pages, stats);
+static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel, int n_cand,
+                                   int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                                   cudaStream_t s) {
+    int sort_cap, hcap;
+    select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
+    const bool fused = out != nullptr;
+    const int bytes = select_smem_bytes(v.C, v.L, v.P, n_cand, n_sel, G, fused);
+    if (fused)
+        select_kernel<T, G, true><<<v.U, kSelThreads, bytes, s>>>(
+            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, page_ids, n_pages, stats, (T*)out);
+    else
+        select_kernel<T, G, false><<<v.U, kSelThreads, bytes, s>>>(
+            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, page_ids, n_pages, stats, nullptr);
+    return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t launch_select_dt(const IndexView& v, const void* q, int n_sel, int n_cand,
-                                    int sort_cap, int hcap, int bytes, int32_t* page_ids,
-                                    int32_t* n_pages, int32_t* stats, cudaStream_t s) {
+                                    int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                                    cudaStream_t s) {
     switch (v.G) {
-        case 1: launch_select_t<T, 1>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
-        case 2: launch_select_t<T, 2>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
-        case 4: launch_select_t<T, 4>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
-        case 8: launch_select_t<T, 8>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, s); break;
+        case 1: return launch_select_g<T, 1>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+        case 2: return launch_select_g<T, 2>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+        case 4: return launch_select_g<T, 4>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+        case 8: return launch_select_g<T, 8>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
-                          int32_t* page_ids, int32_t* n_pages, int32_t* stats, cudaStream_t s) {
-    int sort_cap, hcap;
-    select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
-    const int bytes = sel_layout(v.C, v.L, n_cand, sort_cap, hcap).end;
+                          int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                          cudaStream_t s) {
     if (v.dtype == ICE_BF16)
-        return launch_select_dt<__nv_bfloat16>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids,
-                                               n_pages, stats, s);
-    return launch_select_dt<float>(v, q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages,
-                                   stats, s);
+        return launch_select_dt<__nv_bfloat16>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+    return launch_select_dt<float>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
 }
 
 // Raise the dynamic shared memory limit of the select kernels once per device.
 cudaError_t select_prepare() {
     const int lim = 200 * 1024;
     cudaError_t e = cudaSuccess;
-#define ICE_SET_SMEM(T, G)                                                                     \
-    if (e == cudaSuccess)                                                                      \
-        e = cudaFuncSetAttribute(select_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+#define ICE_SET_SMEM(T, G)                                                                        \
+    if (e == cudaSuccess)                                                                         \
+        e = cudaFuncSetAttribute(select_kernel<T, G, false>,                                      \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
+    if (e == cudaSuccess)                                                                         \
+        e = cudaFuncSetAttribute(select_kernel<T, G, true>,                                       \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
     ICE_SET_SMEM(__nv_bfloat16, 1) ICE_SET_SMEM(__nv_bfloat16, 2) ICE_SET_SMEM(__nv_bfloat16, 4)
     ICE_SET_SMEM(__nv_bfloat16, 8) ICE_SET_SMEM(float, 1) ICE_SET_SMEM(float, 2)
     ICE_SET_SMEM(float, 4) ICE_SET_SMEM(float, 8)

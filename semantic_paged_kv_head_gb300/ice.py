@@ -33,7 +33,7 @@ ICE_F32 = 0
 ICE_BF16 = 1
 
 # every symbol include/ice.h declares
-EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_sparse_attn", "ice_get_error",
+EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_select_attn", "ice_sparse_attn", "ice_get_error",
            "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page"]
 
 
@@ -73,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_insert.restype = ctypes.c_int
     lib.ice_select.argtypes = [vp, vp, i32, vp, vp, vp, vp]
     lib.ice_select.restype = ctypes.c_int
+    lib.ice_select_attn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.ice_select_attn.restype = ctypes.c_int
     lib.ice_sparse_attn.argtypes = [vp, vp, vp, vp, i32, vp, vp]
     lib.ice_sparse_attn.restype = ctypes.c_int
     lib.ice_get_error.argtypes = [vp, vp]
@@ -174,6 +176,27 @@ class IceIndex:
                                _dev_ptr(n_pages, torch.int32, "n_pages"), sp, _stream(stream)),
                "ice_select")
         return page_ids, n_pages
+
+    def select_attn(self, q: torch.Tensor, token_budget: int, out: torch.Tensor | None = None,
+                    page_ids: torch.Tensor | None = None, n_pages: torch.Tensor | None = None,
+                    stats: torch.Tensor | None = None, stream=None):
+        """ice_select_attn; returns (out, page_ids, n_pages)."""
+        U = self.n_units
+        n_sel = token_budget // self.params.page_size
+        dev = q.device
+        if page_ids is None:
+            page_ids = torch.empty((U, n_sel), dtype=torch.int32, device=dev)
+        if n_pages is None:
+            n_pages = torch.empty((U,), dtype=torch.int32, device=dev)
+        if out is None:
+            out = torch.empty_like(q)
+        sp = _dev_ptr(stats, torch.int32, "stats") if stats is not None else None
+        _check(_lib.ice_select_attn(self._h, _dev_ptr(q, self.dtype, "q"), int(token_budget),
+                                    _dev_ptr(page_ids, torch.int32, "page_ids"),
+                                    _dev_ptr(n_pages, torch.int32, "n_pages"), sp,
+                                    _dev_ptr(out, self.dtype, "out"), _stream(stream)),
+               "ice_select_attn")
+        return out, page_ids, n_pages
 
     def sparse_attn(self, q: torch.Tensor, page_ids: torch.Tensor, n_pages: torch.Tensor,
                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

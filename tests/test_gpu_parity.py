@@ -38,8 +38,16 @@ def _run(ice, w, keys, values, q, max_tokens=None):
     stats = torch.zeros((gix.n_units, 4), dtype=torch.int32, device="cuda")
     ids, npg = gix.select(qd, w.budget, stats=stats)
     out = gix.sparse_attn(qd, ids, npg)
+    # the fused call selects the same pages; its attention is checked against the
+    # oracle by the callers through `out_f` on the same tolerance
+    stats_f = torch.zeros_like(stats)
+    out_f, ids_f, npg_f = gix.select_attn(qd, w.budget, stats=stats_f)
     torch.cuda.synchronize()
     assert gix.get_error() == 0
+    assert torch.equal(ids_f, ids) and torch.equal(npg_f, npg) and torch.equal(stats_f, stats)
+    d = (out_f.float() - out.float()).abs().max().item() if out.numel() else 0.0
+    assert d <= (4e-2 if w.dtype == torch.bfloat16 else 2e-5), d
+    gix._last_fused_out = out_f
     return gix, ids, npg, out, stats
 
 
@@ -60,6 +68,8 @@ def _full_check(ice, w, units=None, max_pages=8):
         err, _ = check_select_attn(w, orc, qu, ids[u], npg[u], out.view(-1, G, w.d)[u], stats[u],
                                    f"unit {u}")
         errs.append(err)
+        check_select_attn(w, orc, qu, ids[u], npg[u], gix._last_fused_out.view(-1, G, w.d)[u],
+                          None, f"unit {u} fused")
     return errs
 
 
