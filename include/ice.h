@@ -213,6 +213,35 @@ int ice_debug_page(ice_index* ix, int32_t unit, int32_t page_id, void* host_k, v
                    void* stream);
 
 
+/*
+ * ice_key_codes_noalloc - the key transform of ice_build (squared norms, the
+ * frozen scale exponent per unit, the 8-bit codes of every key on the L x 8
+ * random directions, their Morton interleave) without allocating any memory.
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory while they run (a process whose memory is all
+ * handed to its own pool allocator, or a latency-critical loop where a
+ * cudaMalloc, which can synchronise the device, is not acceptable).
+ *
+ * params: as for ice_build (d = 128, n_proj = 8, n_composite, dtype, seed, and
+ *   batch x n_layers x n_kv_heads units; the other fields are ignored).
+ * keys: device, [units][n_tokens][d], dtype; 16-byte aligned.
+ * morton_out: device uint64 [n_composite][units][n_tokens]; receives the
+ *   Morton key of each token (the same value ice_build indexes).
+ * e_out: device int32 [units]; receives the scale exponent e (c = 2^e).
+ *
+ * Scratch lives in fixed device arrays inside the library: at most
+ * units * n_tokens <= 1,048,576 tokens and units <= 4096 per call; larger
+ * requests return ICE_ERR_CAPACITY before anything runs. The arrays (about
+ * 4.1 MB) stay on every GPU that loads the library until the process exits.
+ * All calls share them: calls that overlap on the GPU (two streams) race; calls
+ * on one stream are ordered. The first call on each device looks up the arrays'
+ * device addresses (cudaGetSymbolAddress); make that first call before any
+ * stream capture. The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine) and returns without waiting.
+ */
+int ice_key_codes_noalloc(const ice_params* params, const void* keys, int64_t n_tokens,
+                          uint64_t* morton_out, int32_t* e_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,7 +34,8 @@ ICE_BF16 = 1
 
 # every symbol include/ice.h declares
 EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_select_attn", "ice_sparse_attn", "ice_get_error",
-           "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page"]
+           "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page",
+           "ice_key_codes_noalloc"]
 
 
 class ice_params(ctypes.Structure):
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_debug_dump.restype = i64
     lib.ice_debug_page.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.ice_debug_page.restype = ctypes.c_int
+    lib.ice_key_codes_noalloc.argtypes = [P(ice_params), vp, i64, vp, vp, vp]
+    lib.ice_key_codes_noalloc.restype = ctypes.c_int
     return lib
 
 
@@ -287,6 +290,29 @@ class IceIndex:
         _check(_lib.ice_debug_page(self._h, unit, page_id, hk.data_ptr(), hv.data_ptr(),
                                    _stream(stream)), "ice_debug_page")
         return hk, hv
+
+
+def key_codes_noalloc(keys: torch.Tensor, *, n_composite: int = 2, n_proj: int = 8, seed: int = 0,
+                      morton_out: torch.Tensor | None = None, e_out: torch.Tensor | None = None,
+                      stream=None):
+    """ice_key_codes_noalloc on keys [batch, layers, kv_heads, n, d].
+
+    Returns (morton [n_composite, units, n] as int64 bit patterns, e [units]).
+    Pass preallocated outputs to keep the call free of allocations."""
+    B, Ly, H, n, d = keys.shape
+    U = B * Ly * H
+    p = ice_params(d=d, n_kv_heads=H, n_q_heads=H, n_layers=Ly, batch=B, page_size=1,
+                   n_proj=n_proj, n_composite=n_composite, n_cand=0, dtype=_code(keys.dtype),
+                   max_tokens=n, seed=seed)
+    if morton_out is None:
+        morton_out = torch.empty((n_composite, U, n), dtype=torch.int64, device=keys.device)
+    if e_out is None:
+        e_out = torch.empty((U,), dtype=torch.int32, device=keys.device)
+    _check(_lib.ice_key_codes_noalloc(ctypes.byref(p), _dev_ptr(keys, None, "keys"), n,
+                                      _dev_ptr(morton_out, torch.int64, "morton_out"),
+                                      _dev_ptr(e_out, torch.int32, "e_out"), _stream(stream)),
+           "ice_key_codes_noalloc")
+    return morton_out, e_out
 
 
 def raw_library() -> ctypes.CDLL:
