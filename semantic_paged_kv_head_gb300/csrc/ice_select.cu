@@ -1,6 +1,7 @@
 // Decode-time page selection ("IceCache", Figure 2 steps 2-3; the blog's
 // mechanism section: P-DCI, the prioritised DCI search, picks the pages most
-// relevant to the current query).
+// relevant to the current query), and optionally the attention over the
+// selected pages in the same block (Figure 2 step 3).
 //
 // One 512-thread block per unit. The work of a unit is a chain of dependent
 // phases, so each phase is organised to keep many requests in flight and to
@@ -9,15 +10,16 @@
 //     directions are requested together; the first batch of leaf records is
 //     requested before the query prep (q_sel = sum of the heads in head order,
 //     normalised, projected and quantised per composite) is computed;
-//  2. all composites are scanned in one pass: the priority of a leaf is the
-//     L-infinity distance in code units between the query codes and the leaf's
-//     cell, evaluated two directions per instruction on fp16x2 (codes are
-//     exact small integers there); token counts by priority go to
-//     sub-histograms shared by two warps;
+//  2. all composites are scanned: the priority of a leaf is the L-infinity
+//     distance in code units between the query codes and the leaf's cell,
+//     evaluated two directions per instruction on fp16x2 (codes are exact
+//     small integers there); priority and token count of every leaf go to
+//     shared memory, token counts by priority to sub-histograms;
 //  3. per composite, pi* is the smallest priority whose cumulative count
-//     reaches n_cand; leaves below pi* are taken, and leaves at pi* in
-//     left-to-right order while the tokens taken before them at pi* are fewer
-//     than needed (the order a best-first tree search visits leaves in);
+//     reaches n_cand; leaves below pi* are taken (their records requested in
+//     the same pass), and leaves at pi* in left-to-right order while the tokens
+//     taken before them at pi* are fewer than needed (the order a best-first
+//     tree search visits leaves in);
 //  4. every slot of every taken leaf becomes a candidate (token, row) in one
 //     parallel round; a composite-1 token whose page composite 0 already took
 //     is a duplicate and dropped;
@@ -27,8 +29,14 @@
 //     into its page's slot of a shared-memory hash table: a page's first
 //     occurrence in the ranked candidate list is its smallest key;
 //  6. the n_sel pages with the smallest keys, in key order, are the selection
-//     (warp-level bitonic top-32 and a fixed-order merge of the warps' lists;
-//     a block-wide bitonic sort when n_sel > 32).
+//     (warp-level bitonic top-32 and a merge tree over the warps' lists; a
+//     block-wide bitonic sort when n_sel > 32);
+//  7. (fused) the K and V rows of the selected pages are staged in shared
+//     memory with bulk asynchronous copies (cp.async.bulk, one per page and
+//     tensor, completing on one mbarrier) into the space the selection no
+//     longer needs, and the G query heads attend over them: lane = (head, 32/G
+//     dimensions' group), one token per warp instruction, fp32 online softmax
+//     per warp, warps merged in a fixed order.
 #include "ice_internal.cuh"
 
 #include <cuda_fp16.h>
@@ -42,36 +50,76 @@ constexpr int kScanUnr = 8;   // leaf records in flight per thread
 constexpr int kRowUnr = 2;    // candidate rows per lane group per round
 constexpr int kTieCap = 256;  // leaves at pi* ordered by rank counting; more -> range scan
 constexpr int kTopK = 32;     // warp top-k width
+constexpr int kFusedSmem = 108 * 1024;  // fused blocks grow to this (two blocks per SM)
+constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // bounded barrier wait
 
+// Shared-memory layout. sel/toff live through the whole kernel; keys .. top
+// hold the candidates and the page hash from phase 4 on. Everything from `free`
+// on is dead once the candidates are expanded: rescoring stages candidate rows
+// there, and the fused attention stages pages there (from `keys` on, after the
+// ranking) and finally the warps' partial results.
 struct SelSmem {
-    int prio, hist, chosen, cmeta, coff, tie, tcnt, bm0, keys, vals, hpage, hkey, top, sel, toff,
-        part, end;
+    int sel, toff;
+    int keys, vals, hpage, hkey, top;
+    int free;
+    int prio, cnt, chosen, cmeta, coff, tie, tcnt, bm0, hist;
+    int end;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
 
 __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, int sort_cap,
-                                              int hcap, int n_sel, int part_floats) {
+                                              int hcap, int n_sel, int min_total) {
     SelSmem s;
     int o = 0;
-    s.prio = o; o = align16(o + L * (int)C);
-    s.hist = o; o = align16(o + L * kSubH * 256 * 4);
+    s.sel = o; o = align16(o + n_sel * 4);
+    s.toff = o; o = align16(o + (n_sel + 1) * 4);
+    s.keys = o; o = align16(o + sort_cap * 8);
+    s.vals = o; o = align16(o + sort_cap * 4);
+    s.hpage = o; o = align16(o + hcap * 4);
+    s.hkey = o; o = align16(o + hcap * 8);
+    s.top = o; o = align16(o + kSelWarps * kTopK * 12);
+    s.free = o;
+    const int Cp = align16((int)C);
+    s.prio = o; o = align16(o + L * Cp);
+    s.cnt = o; o = align16(o + L * Cp);
     s.chosen = o; o = align16(o + L * n_cand * 4);
     s.cmeta = o; o = align16(o + L * n_cand * 4);
     s.coff = o; o = align16(o + L * (n_cand + 1) * 4);
     s.tie = o; o = align16(o + L * kTieCap * 4);
     s.tcnt = o; o = align16(o + L * kTieCap * 4);
     s.bm0 = o; o = align16(o + (int)((C + 31) / 32) * 4);
-    s.keys = o; o = align16(o + sort_cap * 8);
-    s.vals = o; o = align16(o + sort_cap * 4);
-    s.hpage = o; o = align16(o + hcap * 4);
-    s.hkey = o; o = align16(o + hcap * 8);
-    s.top = o; o = align16(o + kSelWarps * kTopK * 12);
-    s.sel = o; o = align16(o + n_sel * 4);
-    s.toff = o; o = align16(o + (n_sel + 1) * 4);
-    s.part = o; o = align16(o + part_floats * 4);
-    s.end = o;
+    s.hist = o; o = align16(o + L * kSubH * 256 * 4);
+    s.end = o > min_total ? o : min_total;
     return s;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+
+// Returns true once phase `parity` of the mbarrier has completed, false if it
+// has not within kWaitNs of wall time (the caller then reports a timeout).
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity) {
+    const unsigned long long t0 = global_ns();
+    for (int i = 0;; ++i) {
+        unsigned done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 15) == 15 && global_ns() - t0 > kWaitNs) return false;
+        __nanosleep(i < 64 ? 20 : 200);
+    }
 }
 
 // Two bytes of x (selector s) as two fp16 values 1024 + byte (exact). The bit
@@ -190,18 +238,23 @@ template <> struct Chunk<float> {
 };
 
 // Attention of the G query heads of unit u over every token of the selected
-// pages (the fused tail of the select kernel). A warp takes tokens w, w + 16, ...
-// of the flattened page list, one token per warp instruction (lane l owns
-// dimensions 4l .. 4l + 3), with an fp32 online softmax per warp; the 16 warp
-// partials are merged in a fixed order in shared memory.
+// pages (the fused tail). Pages are staged in rounds that fit the staging
+// region: lanes of warp 0 issue one bulk copy per page for K and one for V onto
+// one mbarrier; then every warp takes tokens w, w + 16, ... of the round. Lane
+// (h, g) holds query head h on dimensions [g*DPL, (g+1)*DPL), DPL = 4G; a token
+// costs one warp instruction per step and log2(32/G) shuffles per head.
 template <typename T, int G>
-__device__ __forceinline__ void attend_selected(const IndexView& v, int u, const T* __restrict__ q,
-                                                int npg, const int* s_sel, int* s_toff,
-                                                int* s_ntok, float* part /* [warps][G][kD+2] */,
-                                                T* __restrict__ out) {
-    constexpr int kTokRound = 2;
+__device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T* __restrict__ q,
+                                              int npg, const int* s_sel, int* s_toff,
+                                              int* s_ntok, unsigned char* stage,
+                                              int stage_bytes, unsigned bar, int* s_fail,
+                                              T* __restrict__ out) {
+    constexpr int LPH = 32 / G;     // lanes per head
+    constexpr int DPL = kD / LPH;   // dimensions per lane
+    constexpr int ROWB = kD * (int)sizeof(T);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = v.P;
+    const int h = lane / LPH, g = lane % LPH;
     // token offsets of the selected pages (warp 0), counts read in parallel
     if (warp == 0) {
         int carry = 0;
@@ -227,84 +280,120 @@ __device__ __forceinline__ void attend_selected(const IndexView& v, int u, const
             *s_ntok = carry;
         }
     }
-    float qa[G][4];
-    const float sc = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
+    float qa[DPL];
+    {
+        const float sc = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
+        const T* qh = q + ((long long)u * G + h) * kD + g * DPL;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        load4(q + ((long long)u * G + h) * kD + 4 * lane, qa[h]);
+        for (int k = 0; k < DPL; k += 4) {
+            float x[4];
+            load4(qh + k, x);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) qa[h][k] *= sc;
+            for (int z = 0; z < 4; ++z) qa[k + z] = x[z] * sc;
+        }
     }
     __syncthreads();
     const int ntok = *s_ntok;
-    float m[G], lsum[G], acc[G][4];
+    const int rows_cap = stage_bytes / (2 * ROWB);
+    const T* sk = reinterpret_cast<const T*>(stage);
+    const T* sv = reinterpret_cast<const T*>(stage + (size_t)rows_cap * ROWB);
+    float m = -INFINITY, lsum = 0.0f, acc[DPL];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m[h] = -INFINITY;
-        lsum[h] = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc[h][k] = 0.0f;
-    }
-    const T* pk = reinterpret_cast<const T*>(v.page_k);
-    const T* pv = reinterpret_cast<const T*>(v.page_v);
-    for (int j0 = warp; j0 < ntok; j0 += kSelWarps * kTokRound) {  // warp-uniform
-        float kx[kTokRound][4], vx[kTokRound][4];
-#pragma unroll
-        for (int t = 0; t < kTokRound; ++t) {
-            const int j = j0 + t * kSelWarps;
-            if (j < ntok) {
-                int lo = 0, hi = npg;  // last page r with s_toff[r] <= j
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (s_toff[mid] <= j) lo = mid; else hi = mid;
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.0f;
+    int p0 = 0, round = 0;
+    while (p0 < npg) {  // every thread computes the same rounds
+        int p1 = p0 + 1;
+        while (p1 < npg && s_toff[p1 + 1] - s_toff[p0] <= rows_cap) ++p1;
+        const int t0 = s_toff[p0], nrow = s_toff[p1] - t0;
+        if (warp == 0) {
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                             "r"((unsigned)(2 * nrow * ROWB))
+                             : "memory");
+            }
+            __syncwarp();
+            for (int r = p0 + lane; r < p1; r += 32) {
+                const int c = s_toff[r + 1] - s_toff[r];
+                if (c > 0) {
+                    const long long row0 = v.page_row(u, s_sel[r], 0);
+                    const unsigned off = (unsigned)(s_toff[r] - t0) * ROWB;
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            smem_u32(sk) + off),
+                        "l"(reinterpret_cast<const char*>(v.page_k) + row0 * ROWB), "r"((unsigned)c * ROWB),
+                        "r"(bar)
+                        : "memory");
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            smem_u32(sv) + off),
+                        "l"(reinterpret_cast<const char*>(v.page_v) + row0 * ROWB), "r"((unsigned)c * ROWB),
+                        "r"(bar)
+                        : "memory");
                 }
-                const long long row = v.page_row(u, s_sel[lo], j - s_toff[lo]);
-                load4_nc(pk + row * kD + 4 * lane, kx[t]);
-                load4_nc(pv + row * kD + 4 * lane, vx[t]);
             }
         }
+        const bool ok = mbar_wait_bounded(bar, (unsigned)(round & 1));
+        if (!ok && tid == 0) {
+            set_status(v.status, ICE_ERR_TIMEOUT);
+            *s_fail = 1;
+        }
+        if (ok) {
+            for (int j = warp; j < nrow; j += kSelWarps) {  // warp-uniform
+                float kx[DPL];
 #pragma unroll
-        for (int t = 0; t < kTokRound; ++t) {
-            if (j0 + t * kSelWarps >= ntok) break;  // warp-uniform
+                for (int k = 0; k < DPL; k += 4) {
+                    float x[4];
+                    load4(sk + (size_t)j * kD + g * DPL + k, x);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float a = 0.0f;
+                    for (int z = 0; z < 4; ++z) kx[k + z] = x[z];
+                }
+                float s = 0.0f;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) a = fmaf(qa[h][k], kx[t][k], a);
+                for (int k = 0; k < DPL; ++k) s = fmaf(qa[k], kx[k], s);
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                const float mn = fmaxf(m[h], a);
-                const float corr = exp2f(m[h] - mn);
-                const float p = exp2f(a - mn);
-                lsum[h] = lsum[h] * corr + p;
+                for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                const float mn = fmaxf(m, s);
+                const float corr = exp2f(m - mn);
+                const float p = exp2f(s - mn);
+                lsum = lsum * corr + p;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) acc[h][k] = fmaf(p, vx[t][k], acc[h][k] * corr);
-                m[h] = mn;
+                for (int k = 0; k < DPL; k += 4) {
+                    float x[4];
+                    load4(sv + (size_t)j * kD + g * DPL + k, x);
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) acc[k + z] = fmaf(p, x[z], acc[k + z] * corr);
+                }
+                m = mn;
             }
         }
+        __syncthreads();  // the round's rows are consumed before the next copies land
+        p0 = p1;
+        ++round;
     }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
+    // partials into the (now free) staging region: [warp][head][kD + 2]
+    float* part = reinterpret_cast<float*>(stage);
+    {
         float* pw = part + (warp * G + h) * (kD + 2);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) pw[4 * lane + k] = acc[h][k];
-        if (lane == 0) {
-            pw[kD] = m[h];
-            pw[kD + 1] = lsum[h];
+        for (int k = 0; k < DPL; ++k) pw[g * DPL + k] = acc[k];
+        if (g == 0) {
+            pw[kD] = m;
+            pw[kD + 1] = lsum;
         }
     }
     __syncthreads();
     T* ou = out + (long long)u * G * kD;
     for (int e = tid; e < G * kD; e += kSelThreads) {
-        const int h = e / kD, dcol = e % kD;
+        const int hh = e / kD, dcol = e % kD;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kSelWarps; ++w) M = fmaxf(M, part[(w * G + h) * (kD + 2) + kD]);
+        for (int w = 0; w < kSelWarps; ++w) M = fmaxf(M, part[(w * G + hh) * (kD + 2) + kD]);
         float Lt = 0.0f, O = 0.0f;
-        if (M != -INFINITY) {
+        if (M != -INFINITY && !*s_fail) {
 #pragma unroll
             for (int w = 0; w < kSelWarps; ++w) {
-                const float* pw = part + (w * G + h) * (kD + 2);
+                const float* pw = part + (w * G + hh) * (kD + 2);
                 if (pw[kD] == -INFINITY) continue;
                 const float cf = exp2f(pw[kD] - M);
                 Lt = fmaf(pw[kD + 1], cf, Lt);
@@ -318,31 +407,33 @@ __device__ __forceinline__ void attend_selected(const IndexView& v, int u, const
 template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
-    int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out, int32_t* __restrict__ stats,
-    T* __restrict__ attn_out) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
+    int32_t* __restrict__ stats, T* __restrict__ attn_out) {
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
     __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL], s_ntie[kMaxL];
-    __shared__ int s_ncand, s_nraw, s_npg, s_ntok;
+    __shared__ int s_ncand, s_nraw, s_npg, s_ntok, s_fail, s_cmp;
     __shared__ int s_wsum[kMaxL][kSelWarps];
+    __shared__ __align__(8) unsigned long long s_bar;
 
     const int u = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = v.L, P = v.P;
     const long long C = v.C;
-    const SelSmem lay = sel_layout(C, L, n_cand, sort_cap, hcap, n_sel,
-                                   FUSED ? kSelWarps * G * (kD + 2) : 0);
-    unsigned char* prio = smem + lay.prio;                            // [L][C]
+    const int Cp = align16((int)C);
+    const SelSmem lay = sel_layout(C, L, n_cand, sort_cap, hcap, n_sel, 0);
+    int* s_sel = reinterpret_cast<int*>(smem + lay.sel);              // [n_sel] selected pages
+    int* s_toff = reinterpret_cast<int*>(smem + lay.toff);            // [n_sel + 1] token offsets
+    unsigned char* prio = smem + lay.prio;                            // [L][Cp]
+    unsigned char* cnts = smem + lay.cnt;                             // [L][Cp]
     int* hist = reinterpret_cast<int*>(smem + lay.hist);              // [L][kSubH][256]
     int* chosen = reinterpret_cast<int*>(smem + lay.chosen);          // [L][n_cand] leaf index
     unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);  // [L][n_cand] id|count
     int* coff = reinterpret_cast<int*>(smem + lay.coff);              // [L][n_cand + 1]
     int* tie = reinterpret_cast<int*>(smem + lay.tie);                // [L][kTieCap]
     int* tcnt = reinterpret_cast<int*>(smem + lay.tcnt);              // [L][kTieCap]
-    int* s_sel = reinterpret_cast<int*>(smem + lay.sel);              // [n_sel] selected pages
-    int* s_toff = reinterpret_cast<int*>(smem + lay.toff);            // [n_sel + 1] token offsets
     unsigned* bm0 = reinterpret_cast<unsigned*>(smem + lay.bm0);
     unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.keys);
     int* sval = reinterpret_cast<int*>(smem + lay.vals);
@@ -424,10 +515,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     if (tid == 0) {
         s_ncand = 0;
         s_nraw = 0;
+        s_npg = 0;
+        s_fail = 0;
+        if (FUSED) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
     }
     __syncthreads();
 
-    // ---- 2. priorities + sub-histograms of token counts, all composites ------------------
+    // ---- 2. priorities, counts and sub-histograms of token counts --------------------
     {
         __half2 qc[kMaxL][4];
 #pragma unroll
@@ -463,8 +560,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                     const int i = base + k * kSelThreads + tid;
                     if (i < N[l]) {
                         const int pr = leaf_priority(rb[k], qc[l], s_width);
-                        st_shared_u8(prio + l * C + i, pr);
-                        atomicAdd(&hist[(l * kSubH + sub) * 256 + pr], rec_cnt(rb[k]));
+                        const int cn = rec_cnt(rb[k]);
+                        st_shared_u8(prio + l * Cp + i, pr);
+                        st_shared_u8(cnts + l * Cp + i, cn);
+                        atomicAdd(&hist[(l * kSubH + sub) * 256 + pr], cn);
                     }
                 }
             }
@@ -509,109 +608,129 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     }
     __syncthreads();
 
-    // ---- 3b. leaves below pi* are taken; leaves at pi* are collected --------------------
-    {
-        const int ps0 = s_pstar[0], ps1 = L > 1 ? s_pstar[1] : 0;
-        for (int i = tid; i < Ntot; i += kSelThreads) {
-            const int l = i < N[0] ? 0 : 1;
-            const int li = i - (l ? N[0] : 0);
-            const int pr = prio[l * C + li];
-            const int ps = l ? ps1 : ps0;
-            if (pr < ps) {
-                const int slot = atomicAdd(&s_nch[l], 1);
-                if (slot < n_cand) chosen[l * n_cand + slot] = li;
-            } else if (pr == ps) {
-                const int slot = atomicAdd(&s_ntie[l], 1);
-                if (slot < kTieCap) tie[l * kTieCap + slot] = li;
+    // ---- 3b. leaves below pi* are taken (records requested now); leaves at pi* listed ---
+#pragma unroll
+    for (int l = 0; l < kMaxL; ++l) {
+        if (l >= L) break;
+        const int ps = s_pstar[l];
+        const unsigned* p32 = reinterpret_cast<const unsigned*>(prio + l * Cp);
+        const uint4* lrec = recs + v.leaf_base(u, l);
+        const int nw = (N[l] + 3) >> 2;
+        for (int w4 = tid; w4 < nw; w4 += kSelThreads) {
+            const unsigned word = p32[w4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int i = 4 * w4 + b;
+                if (i >= N[l]) break;
+                const int pr = (int)((word >> (8 * b)) & 0xFFu);
+                if (pr < ps) {
+                    const int slot = atomicAdd(&s_nch[l], 1);
+                    if (slot < n_cand) {
+                        chosen[l * n_cand + slot] = i;
+                        cmeta[l * n_cand + slot] = __ldg(lrec + i).z;
+                    }
+                } else if (pr == ps) {
+                    const int slot = atomicAdd(&s_ntie[l], 1);
+                    if (slot < kTieCap) tie[l * kTieCap + slot] = i;
+                }
             }
         }
     }
     __syncthreads();
     // ---- 3c. leaves at pi*, in position order, while tokens taken before them < need ------
-    for (int l = 0; l < L; ++l) {
-        const int ntie = s_ntie[l];
-        if (ntie == 0) continue;
-        if (ntie <= kTieCap) {
-            // rank by counting (positions are distinct), then a prefix walk by warp 0
-            int* tl = tie + l * kTieCap;
-            const uint4* lrec = recs + v.leaf_base(u, l);
-            int* tc = tcnt + l * kTieCap;
-            int mine = 0, r = 0, mc = 0;
-            const bool act = tid < ntie;
-            if (act) {
-                mine = tl[tid];
-                mc = rec_cnt(__ldg(lrec + mine));  // in flight during the counting
-                for (int j = 0; j < ntie; ++j) r += tl[j] < mine;
-            }
-            __syncthreads();
-            if (act) {
-                tl[r] = mine;
-                tc[r] = mc;
-            }
-            __syncthreads();
-            if (warp == 0) {
-                const int need = s_need[l];
+    // Both composites at once: threads [256 l, 256 l + ntie_l) rank composite l's
+    // ties by counting, warp l walks them in order. A composite with more than
+    // kTieCap ties is handled afterwards by a range walk over its positions.
+    {
+        const int l = tid >> 8, t = tid & 255;  // kSelThreads = 2 * kTieCap
+        const int ntie = l < L ? s_ntie[l] : 0;
+        int* tl = tie + l * kTieCap;
+        int* tc = tcnt + l * kTieCap;
+        const bool act = l < L && ntie <= kTieCap && t < ntie;
+        int mine = 0, r = 0, mc = 0;
+        if (act) {
+            mine = tl[t];
+            mc = cnts[l * Cp + mine];
+            for (int j = 0; j < ntie; ++j) r += tl[j] < mine;
+        }
+        __syncthreads();
+        if (act) {
+            tl[r] = mine;
+            tc[r] = mc;
+        }
+        __syncthreads();
+        if (warp < L) {
+            const int lw = warp;
+            const int nt = s_ntie[lw];
+            if (nt > 0 && nt <= kTieCap) {
+                const int* tlw = tie + lw * kTieCap;
+                const int* tcw = tcnt + lw * kTieCap;
+                const uint4* lrec = recs + v.leaf_base(u, lw);
+                const int need = s_need[lw];
                 int run = 0;
-                for (int k0 = 0; k0 < ntie && run < need; k0 += 32) {
+                for (int k0 = 0; k0 < nt && run < need; k0 += 32) {
                     const int k = k0 + lane;
-                    const int li = k < ntie ? tl[k] : 0;
-                    const int c = k < ntie ? tc[k] : 0;
+                    const int li = k < nt ? tlw[k] : 0;
+                    const int c = k < nt ? tcw[k] : 0;
                     int inc = c;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
                         const int y = __shfl_up_sync(0xffffffffu, inc, o);
                         if (lane >= o) inc += y;
                     }
-                    const bool take = k < ntie && run + inc - c < need;
+                    const bool take = k < nt && run + inc - c < need;
                     const unsigned tm = __ballot_sync(0xffffffffu, take);
                     int base = 0;
-                    if (lane == 0 && tm) base = atomicAdd(&s_nch[l], __popc(tm));
+                    if (lane == 0 && tm) base = atomicAdd(&s_nch[lw], __popc(tm));
                     base = __shfl_sync(0xffffffffu, base, 0);
                     if (take) {
                         const int slot = base + __popc(tm & ((1u << lane) - 1u));
-                        if (slot < n_cand) chosen[l * n_cand + slot] = li;
+                        if (slot < n_cand) {
+                            chosen[lw * n_cand + slot] = li;
+                            cmeta[lw * n_cand + slot] = __ldg(lrec + li).z;
+                        }
                     }
                     run += __shfl_sync(0xffffffffu, inc, 31);
                 }
             }
-        } else {
-            // many leaves at pi*: each thread walks a contiguous range of positions
-            const int per = (N[l] + kSelThreads - 1) / kSelThreads;
-            const int lo_i = min(N[l], tid * per), hi_i = min(N[l], lo_i + per);
-            const int ps = s_pstar[l], need = s_need[l];
-            const uint4* lrec = recs + v.leaf_base(u, l);
-            int mine = 0;
-            for (int i = lo_i; i < hi_i; ++i)
-                if (prio[l * C + i] == ps) mine += rec_cnt(__ldg(lrec + i));
-            int incl = mine;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane == 31) s_wsum[l][warp] = incl;
-            __syncthreads();
-            int run = incl - mine;
-            for (int w = 0; w < warp; ++w) run += s_wsum[l][w];
-            for (int i = lo_i; i < hi_i; ++i) {
-                if (prio[l * C + i] != ps) continue;
-                if (run < need) {
-                    const int slot = atomicAdd(&s_nch[l], 1);
-                    if (slot < n_cand) chosen[l * n_cand + slot] = i;
-                }
-                run += rec_cnt(__ldg(lrec + i));
-            }
         }
-        __syncthreads();
     }
-
-    // ---- 3d. records of the taken leaves (one parallel round), offsets, page bitmap ------
     for (int l = 0; l < L; ++l) {
-        const int nch = min(s_nch[l], n_cand);
-        for (int k = tid; k < nch; k += kSelThreads)
-            cmeta[l * n_cand + k] = __ldg(recs + v.leaf_base(u, l) + chosen[l * n_cand + k]).z;
+        const int ntie = s_ntie[l];
+        if (ntie <= kTieCap) continue;  // block-uniform
+        // many leaves at pi*: each thread walks a contiguous range of positions
+        const uint4* lrec = recs + v.leaf_base(u, l);
+        const int per = (N[l] + kSelThreads - 1) / kSelThreads;
+        const int lo_i = min(N[l], tid * per), hi_i = min(N[l], lo_i + per);
+        const int ps = s_pstar[l], need = s_need[l];
+        int mine = 0;
+        for (int i = lo_i; i < hi_i; ++i)
+            if (prio[l * Cp + i] == ps) mine += cnts[l * Cp + i];
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wsum[l][warp] = incl;
+        __syncthreads();
+        int run = incl - mine;
+        for (int w = 0; w < warp; ++w) run += s_wsum[l][w];
+        for (int i = lo_i; i < hi_i; ++i) {
+            if (prio[l * Cp + i] != ps) continue;
+            if (run < need) {
+                const int slot = atomicAdd(&s_nch[l], 1);
+                if (slot < n_cand) {
+                    chosen[l * n_cand + slot] = i;
+                    cmeta[l * n_cand + slot] = __ldg(lrec + i).z;
+                }
+            }
+            run += cnts[l * Cp + i];
+        }
     }
     __syncthreads();
+
+    // ---- 3d. slot offsets of the taken leaves (warp l), composite-0 page bitmap ------------
     if (warp < L) {
         const int l = warp;
         const int nch = min(s_nch[l], n_cand);
@@ -691,7 +810,15 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     const int ncand = min(s_ncand, sort_cap);
 
     // ---- 5. exact rescoring, 4 rows per warp instruction; per-page minimum key --------------
+    // Candidate rows are staged in the free region with cp.async (16 B per
+    // request, all rows of a round in flight); chunk c of row r is stored at
+    // chunk position c ^ ((r mod 4) * chunks-per-row / 4) so that the four rows
+    // a warp reads at once fall in different banks.
     {
+        constexpr int CPR = kD * (int)sizeof(T) / 16;  // 16-byte chunks per row
+        constexpr int ROWB = kD * (int)sizeof(T);
+        unsigned char* stg = smem + lay.free;
+        const int rows_cap = (smem_total - lay.free) / ROWB;
         const int g8 = lane >> 3, p = lane & 7;
         // lane p evaluates lane partials p, p+8, p+16, p+24 of the fixed order:
         // elements 4p + 32j .. 4p + 32j + 3 for j = 0..3
@@ -700,31 +827,31 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i) qv[4 * j + i] = s_qsel[4 * p + 32 * j + i];
-        const T* pk = reinterpret_cast<const T*>(v.page_k) + (long long)u * C * P * kD;
+        const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = hcap - 1;
-        for (int r0 = warp * 4 * kRowUnr; r0 < ncand; r0 += kSelWarps * 4 * kRowUnr) {
-            Chunk<T> ch[kRowUnr][4];
-            int tk[kRowUnr], lc[kRowUnr];
-#pragma unroll
-            for (int k = 0; k < kRowUnr; ++k) {
-                const int r = r0 + 4 * k + g8;
-                tk[k] = -1;
-                lc[k] = 0;
-                if (r < ncand) {
-                    tk[k] = (int)skey[r];
-                    lc[k] = sval[r];
-                    const T* row = pk + (long long)lc[k] * kD + 4 * p;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) ch[k][j].load(row + 32 * j);
-                }
+        for (int rb0 = 0; rb0 < ncand; rb0 += rows_cap) {  // block-uniform rounds
+            const int nr = min(rows_cap, ncand - rb0);
+            for (int k = tid; k < nr * CPR; k += kSelThreads) {
+                const int r = k / CPR, c = k % CPR;
+                const char* src = pk + (long long)sval[rb0 + r] * ROWB + 16 * c;
+                const unsigned dst = smem_u32(stg + r * ROWB + 16 * (c ^ ((r & 3) * (CPR / 4))));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src)
+                             : "memory");
             }
-#pragma unroll
-            for (int k = 0; k < kRowUnr; ++k) {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncthreads();
+            for (int r0 = warp * 4; r0 < nr; r0 += kSelWarps * 4) {  // warp-uniform
+                const int r = r0 + g8;
+                const bool ok = r < nr;
                 float part[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     float x[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (tk[k] >= 0) ch[k][j].get(x);
+                    if (ok) {
+                        const int e = 4 * p + 32 * j;  // element of the row
+                        const int c = (e * (int)sizeof(T)) / 16, in = (e * (int)sizeof(T)) % 16;
+                        load4(reinterpret_cast<const T*>(stg + r * ROWB + 16 * (c ^ ((r & 3) * (CPR / 4))) + in), x);
+                    }
                     float a = 0.0f;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) a = __fmaf_rn(qv[4 * j + i], x[i], a);
@@ -735,14 +862,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 4));
                 b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 2));
                 b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 1));
-                if (p == 0 && tk[k] >= 0) {
+                if (p == 0 && ok) {
+                    const int tk = (int)skey[rb0 + r];
+                    const int lc = sval[rb0 + r];
                     const unsigned long long key =
-                        ((unsigned long long)score_key_desc(b) << 32) | (unsigned)tk[k];
-                    const int pg = lc[k] / P;
+                        ((unsigned long long)score_key_desc(b) << 32) | (unsigned)tk;
+                    const int pg = lc / P;
                     unsigned h = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
                     for (int probe = 0; probe < hcap; ++probe) {
                         const int old = atomicCAS(&hpage[h], -1, pg);
                         if (old == -1 || old == pg) {
+                            if (old == -1) atomicAdd(&s_npg, 1);
                             atomicMin(&hkey[h], key);
                             break;
                         }
@@ -750,18 +880,24 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                     }
                 }
             }
+            __syncthreads();  // the round's rows are read before the next round lands
         }
     }
     __syncthreads();
-    // compact the occupied hash slots: one entry per distinct page
-    if (tid == 0) s_npg = 0;
+    const int npg = s_npg;  // distinct pages among the candidates
+    const int taken = min(n_sel, npg);
+    int32_t* out = page_ids + (long long)u * n_sel;
+
+    // ---- 6. the n_sel smallest page keys in order ------------------------------------------
+    // compact the occupied hash slots into (key, page) pairs
+    if (tid == 0) s_cmp = 0;
     __syncthreads();
-    for (int h0 = warp * 32; h0 < hcap; h0 += kSelThreads) {
+    for (int h0 = warp * 32; h0 < hcap; h0 += kSelThreads) {  // warp-uniform
         const int h = h0 + lane;
         const int pg = h < hcap ? hpage[h] : -1;
         const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
         int base = 0;
-        if (lane == 0 && km) base = atomicAdd(&s_npg, __popc(km));
+        if (lane == 0 && km) base = atomicAdd(&s_cmp, __popc(km));
         base = __shfl_sync(0xffffffffu, base, 0);
         if (pg >= 0) {
             const int pos = base + __popc(km & ((1u << lane) - 1u));
@@ -770,27 +906,26 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         }
     }
     __syncthreads();
-    const int npg = s_npg;  // <= ncand <= sort_cap
-    const int taken = min(n_sel, npg);
-    int32_t* out = page_ids + (long long)u * n_sel;
-
-    // ---- 6. the n_sel smallest page keys in order ------------------------------------------
     if (n_sel <= kTopK) {
+        const int nb = (npg + 31) / 32;  // batches of 32 entries
         unsigned long long tk = ~0ull;
         int tv = -1;
-        for (int j0 = warp * 32; j0 < npg; j0 += kSelThreads) {  // warp-uniform
-            const int j = j0 + lane;
+        for (int bt = warp; bt < nb; bt += kSelWarps) {  // warp-uniform
+            const int j = bt * 32 + lane;
             unsigned long long k = j < npg ? skey[j] : ~0ull;
             int vv = j < npg ? sval[j] : -1;
             warp_sort32(k, vv, lane);
             warp_merge32(tk, tv, k, vv, lane);
         }
-        topk[warp * kTopK + lane] = tk;
-        topv[warp * kTopK + lane] = tv;
+        const int nw = min(kSelWarps, max(nb, 1));  // warps holding a list
+        if (warp < nw) {
+            topk[warp * kTopK + lane] = tk;
+            topv[warp * kTopK + lane] = tv;
+        }
         __syncthreads();
-        // pairwise merge tree over the warps' lists: warp w takes in w + s
-        for (int st = 1; st < kSelWarps; st <<= 1) {
-            if ((warp & (2 * st - 1)) == 0) {
+        // pairwise merge tree over the warps' lists: warp w takes in w + st
+        for (int st = 1; st < nw; st <<= 1) {
+            if ((warp & (2 * st - 1)) == 0 && warp + st < nw) {
                 unsigned long long a = topk[warp * kTopK + lane];
                 int av = topv[warp * kTopK + lane];
                 warp_merge32(a, av, topk[(warp + st) * kTopK + lane],
@@ -806,6 +941,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             s_sel[lane] = pg;
         }
     } else {
+        // a block-wide bitonic sort of the compacted pairs
         int npow = 1;
         while (npow < npg) npow <<= 1;
         for (int c = npg + tid; c < npow; c += kSelThreads) {
@@ -851,9 +987,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             stats[4 * u + 3] = s_nraw;
         }
     }
-    if (tid == 0 && s_ncand > sort_cap) set_status(v.status, ICE_ERR_CAPACITY);
-    if constexpr (FUSED) attend_selected<T, G>(v, u, q, taken, s_sel, s_toff, &s_ntok,
-                                              reinterpret_cast<float*>(smem + lay.part), attn_out);
+    if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
+    if constexpr (FUSED)
+        attend_staged<T, G>(v, u, q, taken, s_sel, s_toff, &s_ntok, smem + lay.keys,
+                            smem_total - lay.keys, smem_u32(&s_bar), &s_fail, attn_out);
 }
 
 static void select_caps(int L, int P, int n_cand, int* sort_cap, int* hcap) {
@@ -864,11 +1001,14 @@ static void select_caps(int L, int P, int n_cand, int* sort_cap, int* hcap) {
     *hcap = c;  // at least one slot per candidate: probing always ends
 }
 
-// Dynamic shared memory the select kernel needs (host check before launch).
+// Dynamic shared memory of a launch (fused blocks are padded up to kFusedSmem so
+// that the page staging region is as large as two blocks per SM allow).
 int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, bool fused) {
+    (void)G;
     int sc, hc;
     select_caps(L, P, n_cand, &sc, &hc);
-    return sel_layout(C, L, n_cand, sc, hc, n_sel, fused ? kSelWarps * G * (kD + 2) : 0).end;
+    (void)fused;
+    return sel_layout(C, L, n_cand, sc, hc, n_sel, kFusedSmem).end;
 }
 
 template <typename T, int G>
@@ -881,10 +1021,10 @@ static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel,
     const int bytes = select_smem_bytes(v.C, v.L, v.P, n_cand, n_sel, G, fused);
     if (fused)
         select_kernel<T, G, true><<<v.U, kSelThreads, bytes, s>>>(
-            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, page_ids, n_pages, stats, (T*)out);
+            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, (T*)out);
     else
         select_kernel<T, G, false><<<v.U, kSelThreads, bytes, s>>>(
-            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, page_ids, n_pages, stats, nullptr);
+            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, nullptr);
     return cudaGetLastError();
 }
 
