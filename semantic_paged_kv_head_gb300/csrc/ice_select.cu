@@ -45,7 +45,8 @@ namespace ice {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSubH = 8;      // sub-histograms per composite (two warps each)
+constexpr int kSubH = 8;      // sub-histograms per composite (lane groups)
+constexpr int kHistRow = 257;  // words per sub-histogram row (256 priorities + 1 pad)
 constexpr int kScanUnr = 8;   // leaf records in flight per thread
 constexpr int kRowUnr = 2;    // candidate rows per lane group per round
 constexpr int kTieCap = 256;  // leaves at pi* ordered by rank counting; more -> range scan
@@ -89,7 +90,7 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
     s.tie = o; o = align16(o + L * kTieCap * 4);
     s.tcnt = o; o = align16(o + L * kTieCap * 4);
     s.bm0 = o; o = align16(o + (int)((C + 31) / 32) * 4);
-    s.hist = o; o = align16(o + L * kSubH * 256 * 4);
+    s.hist = o; o = align16(o + L * kSubH * kHistRow * 4);
     s.end = o > min_total ? o : min_total;
     return s;
 }
@@ -216,6 +217,24 @@ __device__ __forceinline__ void warp_merge32(unsigned long long& ka, int& va, un
             va = ov;
         }
     }
+}
+
+// The 16-byte chunk at shared address p as fp32 values (8 bf16 or 4 f32).
+template <typename T> __device__ __forceinline__ void load_chunk(const unsigned char* p, float (&x)[16 / sizeof(T)]);
+template <>
+__device__ __forceinline__ void load_chunk<__nv_bfloat16>(const unsigned char* p, float (&x)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const unsigned u4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x[2 * k] = __uint_as_float(u4[k] << 16);
+        x[2 * k + 1] = __uint_as_float(u4[k] & 0xFFFF0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void load_chunk<float>(const unsigned char* p, float (&x)[4]) {
+    const float4 w = *reinterpret_cast<const float4*>(p);
+    x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
 }
 
 template <typename T> struct Chunk;
@@ -410,7 +429,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
     int32_t* __restrict__ stats, T* __restrict__ attn_out) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float s_qsel[kD];
+    __shared__ __align__(16) float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
     __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL], s_ntie[kMaxL];
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int* s_toff = reinterpret_cast<int*>(smem + lay.toff);            // [n_sel + 1] token offsets
     unsigned char* prio = smem + lay.prio;                            // [L][Cp]
     unsigned char* cnts = smem + lay.cnt;                             // [L][Cp]
-    int* hist = reinterpret_cast<int*>(smem + lay.hist);              // [L][kSubH][256]
+    int* hist = reinterpret_cast<int*>(smem + lay.hist);              // [L][kSubH][kHistRow]
     int* chosen = reinterpret_cast<int*>(smem + lay.chosen);          // [L][n_cand] leaf index
     unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);  // [L][n_cand] id|count
     int* coff = reinterpret_cast<int*>(smem + lay.coff);              // [L][n_cand + 1]
@@ -501,7 +520,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 #pragma unroll
         for (int k = 0; k < 4; ++k) s_width[tid * 4 + k] = w[k];
     }
-    for (int i = tid; i < L * kSubH * 256; i += kSelThreads) hist[i] = 0;
+    for (int i = tid; i < L * kSubH * kHistRow; i += kSelThreads) hist[i] = 0;
     for (int i = tid; i < nwords; i += kSelThreads) bm0[i] = 0u;
     for (int i = tid; i < hcap; i += kSelThreads) {
         hpage[i] = -1;
@@ -542,7 +561,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             qc[l][2] = bytes_to_h2(hi4, 0x4140u);
             qc[l][3] = bytes_to_h2(hi4, 0x4342u);
         }
-        const int sub = warp >> 1;
+        const int sub = lane & (kSubH - 1);
 #pragma unroll
         for (int l = 0; l < kMaxL; ++l) {
             if (l >= L) break;
@@ -555,6 +574,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                         if (i < N[l]) rb[k] = __ldg(rl + i);
                     }
                 }
+                // neighbouring leaves share few priorities (a handful per 32 leaves):
+                // lanes l, l+8, l+16, l+24 share a sub-histogram, so at most four
+                // lanes of an instruction add to one counter, and the 257-word row
+                // stride puts equal priorities of different sub-histograms in
+                // different banks
 #pragma unroll
                 for (int k = 0; k < kScanUnr; ++k) {
                     const int i = base + k * kSelThreads + tid;
@@ -563,7 +587,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                         const int cn = rec_cnt(rb[k]);
                         st_shared_u8(prio + l * Cp + i, pr);
                         st_shared_u8(cnts + l * Cp + i, cn);
-                        atomicAdd(&hist[(l * kSubH + sub) * 256 + pr], cn);
+                        atomicAdd(&hist[(l * kSubH + sub) * kHistRow + pr], cn);
                     }
                 }
             }
@@ -579,7 +603,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         for (int k = 0; k < 8; ++k) {
             int x = 0;
 #pragma unroll
-            for (int s = 0; s < kSubH; ++s) x += hist[(l * kSubH + s) * 256 + lane * 8 + k];
+            for (int s = 0; s < kSubH; ++s) x += hist[(l * kSubH + s) * kHistRow + lane * 8 + k];
             loc[k] = x;
             sum += x;
         }
@@ -809,75 +833,89 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     __syncthreads();
     const int ncand = min(s_ncand, sort_cap);
 
-    // ---- 5. exact rescoring, 4 rows per warp instruction; per-page minimum key --------------
-    // Candidate rows are staged in the free region with cp.async (16 B per
-    // request, all rows of a round in flight); chunk c of row r is stored at
-    // chunk position c ^ ((r mod 4) * chunks-per-row / 4) so that the four rows
-    // a warp reads at once fall in different banks.
+    // ---- 5. exact rescoring, one candidate row per thread; per-page minimum key ------------
+    // Candidate rows are staged in the free region with cp.async: each thread
+    // requests the 16-byte chunks of one row, and all rows of a round are in
+    // flight at once. Chunk c of row r is stored at chunk position
+    // c ^ (r mod chunks-per-row), so the eight rows that one shared-memory
+    // wavefront serves fall in distinct banks. Each thread then evaluates the
+    // fixed-order dot of its row by itself: virtual lane l accumulates elements
+    // 4l..4l+3, and the pairwise tree first adds lanes l and l+16, so chunks c
+    // and c + chunks-per-row/2 (elements 64 apart) are taken together.
     {
-        constexpr int CPR = kD * (int)sizeof(T) / 16;  // 16-byte chunks per row
+        constexpr int EPC = 16 / (int)sizeof(T);  // elements per chunk
+        constexpr int CPR = kD / EPC;             // chunks per row
+        constexpr int VPC = EPC / 4;              // virtual lanes per chunk
         constexpr int ROWB = kD * (int)sizeof(T);
         unsigned char* stg = smem + lay.free;
-        const int rows_cap = (smem_total - lay.free) / ROWB;
-        const int g8 = lane >> 3, p = lane & 7;
-        // lane p evaluates lane partials p, p+8, p+16, p+24 of the fixed order:
-        // elements 4p + 32j .. 4p + 32j + 3 for j = 0..3
-        float qv[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) qv[4 * j + i] = s_qsel[4 * p + 32 * j + i];
+        const int rows_cap = min((smem_total - lay.free) / ROWB, kSelThreads);
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = hcap - 1;
         for (int rb0 = 0; rb0 < ncand; rb0 += rows_cap) {  // block-uniform rounds
             const int nr = min(rows_cap, ncand - rb0);
-            for (int k = tid; k < nr * CPR; k += kSelThreads) {
-                const int r = k / CPR, c = k % CPR;
-                const char* src = pk + (long long)sval[rb0 + r] * ROWB + 16 * c;
-                const unsigned dst = smem_u32(stg + r * ROWB + 16 * (c ^ ((r & 3) * (CPR / 4))));
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src)
-                             : "memory");
+            const int r = tid;
+            const bool ok = r < nr;
+            const int sw = r & (CPR - 1);
+            if (ok) {
+                const char* src = pk + (long long)sval[rb0 + r] * ROWB;
+                const unsigned dst = smem_u32(stg + r * ROWB);
+#pragma unroll
+                for (int c = 0; c < CPR; ++c)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * (c ^ sw)),
+                                 "l"(src + 16 * c)
+                                 : "memory");
             }
             asm volatile("cp.async.wait_all;" ::: "memory");
             __syncthreads();
-            for (int r0 = warp * 4; r0 < nr; r0 += kSelWarps * 4) {  // warp-uniform
-                const int r = r0 + g8;
-                const bool ok = r < nr;
-                float part[4];
+            int pg = -1;
+            unsigned long long key = ~0ull;
+            if (ok) {
+                const unsigned char* row = stg + r * ROWB;
+                float s16[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float x[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (ok) {
-                        const int e = 4 * p + 32 * j;  // element of the row
-                        const int c = (e * (int)sizeof(T)) / 16, in = (e * (int)sizeof(T)) % 16;
-                        load4(reinterpret_cast<const T*>(stg + r * ROWB + 16 * (c ^ ((r & 3) * (CPR / 4))) + in), x);
-                    }
-                    float a = 0.0f;
+                for (int c = 0; c < CPR / 2; ++c) {
+                    float lo[EPC], hi[EPC];
+                    load_chunk<T>(row + 16 * (c ^ sw), lo);
+                    load_chunk<T>(row + 16 * ((c + CPR / 2) ^ sw), hi);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) a = __fmaf_rn(qv[4 * j + i], x[i], a);
-                    part[j] = a;
-                }
-                // levels 16 and 8 of the pairwise sum inside the lane, 4, 2, 1 across lanes
-                float b = __fadd_rn(__fadd_rn(part[0], part[2]), __fadd_rn(part[1], part[3]));
-                b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 4));
-                b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 2));
-                b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 1));
-                if (p == 0 && ok) {
-                    const int tk = (int)skey[rb0 + r];
-                    const int lc = sval[rb0 + r];
-                    const unsigned long long key =
-                        ((unsigned long long)score_key_desc(b) << 32) | (unsigned)tk;
-                    const int pg = lc / P;
-                    unsigned h = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
-                    for (int probe = 0; probe < hcap; ++probe) {
-                        const int old = atomicCAS(&hpage[h], -1, pg);
-                        if (old == -1 || old == pg) {
-                            if (old == -1) atomicAdd(&s_npg, 1);
-                            atomicMin(&hkey[h], key);
-                            break;
+                    for (int z = 0; z < VPC; ++z) {
+                        const int e0 = 4 * (c * VPC + z);
+                        float a = 0.0f, b = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            a = __fmaf_rn(s_qsel[e0 + i], lo[4 * z + i], a);
+                            b = __fmaf_rn(s_qsel[e0 + 64 + i], hi[4 * z + i], b);
                         }
-                        h = (h + 1) & (unsigned)hmask;
+                        s16[c * VPC + z] = __fadd_rn(a, b);
                     }
+                }
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+                    for (int l = 0; l < o; ++l) s16[l] = __fadd_rn(s16[l], s16[l + o]);
+                pg = sval[rb0 + r] / P;
+                key = ((unsigned long long)score_key_desc(s16[0]) << 32) | (unsigned)skey[rb0 + r];
+            }
+            // rows of one page are adjacent in the candidate list: a segmented
+            // minimum over runs of equal pages leaves each run's minimum in its
+            // last lane, which alone updates the table
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int opg = __shfl_up_sync(0xffffffffu, pg, o);
+                const unsigned long long okey = __shfl_up_sync(0xffffffffu, key, o);
+                if (lane >= o && opg == pg && okey < key) key = okey;
+            }
+            const int next_pg = __shfl_down_sync(0xffffffffu, pg, 1);
+            if (ok && (lane == 31 || next_pg != pg)) {
+                unsigned h = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
+                for (int probe = 0; probe < hcap; ++probe) {
+                    const int old = atomicCAS(&hpage[h], -1, pg);
+                    if (old == -1 || old == pg) {
+                        if (old == -1) atomicAdd(&s_npg, 1);
+                        atomicMin(&hkey[h], key);
+                        break;
+                    }
+                    h = (h + 1) & (unsigned)hmask;
                 }
             }
             __syncthreads();  // the round's rows are read before the next round lands
