@@ -162,7 +162,9 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         // list capacity: the largest leaf count plus one new leaf per future insert
         long long mx = 0;
         for (int x : nleaf) mx = std::max<long long>(mx, x);
-        ix->C = std::max<long long>(1, mx + (v.max_tokens - n));
+        // rounded up to 64 leaves: the selection scan copies leaf records in
+        // aligned chunks of 64 that must stay inside the list
+        ix->C = (std::max<long long>(1, mx + (v.max_tokens - n)) + 63) / 64 * 64;
         if (ix->C >= (1LL << 24) || ix->C * P > (1LL << 31) - 1) {
             scratch_free(s, st);
             free_all(ix);
@@ -175,6 +177,8 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         bool okc = true;
         okc = okc && dev_alloc(ix, &v.leaf_key, (size_t)U * L * C) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.leaf_rec, (size_t)U * L * C) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.leaf_lo, (size_t)U * L * C) == cudaSuccess;
+        okc = okc && dev_alloc(ix, &v.leaf_tc, (size_t)U * L * C) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.n_leaf, (size_t)U * L) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.next_id, (size_t)U * L) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.list_cnt, (size_t)U * L * C) == cudaSuccess;

@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(256) leaf_write_kernel(
         k.pt = pt;
         k.t = (unsigned)depth;
         v.leaf_key[lb] = k;
-        v.leaf_rec[lb] = make_leaf_rec(pm, (unsigned)depth, leaf, end - start);
+        put_leaf(v, lb, make_leaf_rec(pm, (unsigned)depth, leaf, end - start));
         v.list_cnt[v.leaf_base(u, l) + leaf] = end - start;
     }
     if (i == 0) {

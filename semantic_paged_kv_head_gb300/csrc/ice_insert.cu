@@ -23,23 +23,30 @@ struct InsKey {
     unsigned int t;
 };
 
-// Shift leaf keys and records [from, N) one place to the right (backwards, in
-// chunks of one element per thread).
-__device__ void shift_right(LeafKey* key, uint4* rec, int from, int N) {
+// Shift leaf keys, records and the records' scan copies [from, N) one place to
+// the right (backwards, in chunks of one element per thread).
+__device__ void shift_right(LeafKey* key, uint4* rec, unsigned long long* lo, unsigned short* tc,
+                            int from, int N) {
     for (int end = N; end > from; end -= kInsThreads) {
         const int start = max(from, end - kInsThreads);
         const int i = start + (int)threadIdx.x;
         LeafKey k;
         uint4 r;
+        unsigned long long a = 0;
+        unsigned short c = 0;
         const bool act = i < end;
         if (act) {
             k = key[i];
             r = rec[i];
+            a = lo[i];
+            c = tc[i];
         }
         __syncthreads();
         if (act) {
             key[i + 1] = k;
             rec[i + 1] = r;
+            lo[i + 1] = a;
+            tc[i + 1] = c;
         }
         __syncthreads();
     }
@@ -98,7 +105,10 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
         const unsigned long long xm = s_mk[l];
         const unsigned int xt = (unsigned)tok;
         LeafKey* lk = v.leaf_key + v.leaf_base(u, l);
-        uint4* lr = v.leaf_rec + v.leaf_base(u, l);
+        const long long lb0 = v.leaf_base(u, l);
+        uint4* lr = v.leaf_rec + lb0;
+        unsigned long long* llo = v.leaf_lo + lb0;
+        unsigned short* ltc = v.leaf_tc + lb0;
         int* cntl = v.list_cnt + v.leaf_base(u, l);
         int* stok = v.slot_tok + v.slot_base(u, l);
         unsigned long long* skey = v.slot_key + v.slot_base(u, l);
@@ -171,7 +181,9 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 stok[sb] = tok;
                 skey[sb] = xm;
                 cntl[id] = cnt + 1;
-                lr[pos].z = ((unsigned)id << 8) | (unsigned)(cnt + 1);
+                uint4 r2 = rc;
+                r2.z = ((unsigned)id << 8) | (unsigned)(cnt + 1);
+                put_leaf(v, lb0 + pos, r2);
                 if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = id * P + cnt;
             }
             if (l == 0) {
@@ -245,7 +257,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 }
             }
             __syncthreads();
-            shift_right(lk, lr, pos + 1, N);
+            shift_right(lk, lr, llo, ltc, pos + 1, N);
             if (tid == 0) {
                 cntl[id] = nl;
                 cntl[rid] = nr;
@@ -255,9 +267,9 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 prefix96(e_m[g], e_t[g], t, kr.pm, kr.pt);
                 kl.t = kr.t = (unsigned)t;
                 lk[pos] = kl;
-                lr[pos] = make_leaf_rec(kl.pm, (unsigned)t, id, nl);
+                put_leaf(v, lb0 + pos, make_leaf_rec(kl.pm, (unsigned)t, id, nl));
                 lk[pos + 1] = kr;
-                lr[pos + 1] = make_leaf_rec(kr.pm, (unsigned)t, rid, nr);
+                put_leaf(v, lb0 + pos + 1, make_leaf_rec(kr.pm, (unsigned)t, rid, nr));
                 v.n_leaf[v.ul(u, l)] = N + 1;
                 v.next_id[v.ul(u, l)] = nid + 1;
             }
@@ -304,7 +316,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                     pv[i] = vin[i];
                 }
             }
-            shift_right(lk, lr, pos + 1, N);
+            shift_right(lk, lr, llo, ltc, pos + 1, N);
             if (tid == 0) {
                 stok[(long long)nidl * P] = tok;
                 skey[(long long)nidl * P] = xm;
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
                 prefix96(xm, xt, t, k.pm, k.pt);
                 k.t = (unsigned)t;
                 lk[pos + 1] = k;
-                lr[pos + 1] = make_leaf_rec(k.pm, (unsigned)t, nidl, 1);
+                put_leaf(v, lb0 + pos + 1, make_leaf_rec(k.pm, (unsigned)t, nidl, 1));
                 v.n_leaf[v.ul(u, l)] = N + 1;
                 v.next_id[v.ul(u, l)] = nid + 1;
             }

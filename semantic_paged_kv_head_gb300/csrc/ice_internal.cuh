@@ -51,6 +51,10 @@ struct IndexView {
     int* e_unit;
     LeafKey* leaf_key;
     uint4* leaf_rec;
+    // what the selection scan reads of each leaf record, 10 bytes instead of 16:
+    // the lower cell corner (8 codes) and (prefix length | count << 7)
+    unsigned long long* leaf_lo;
+    unsigned short* leaf_tc;
     int* n_leaf;
     int* next_id;
     int* list_cnt;
@@ -198,6 +202,16 @@ __device__ __forceinline__ uint4 make_leaf_rec(unsigned long long pm, unsigned t
     return make_uint4(cell.x, cell.y, ((unsigned)id << 8) | (unsigned)cnt, t);
 }
 __device__ __forceinline__ int rec_id(const uint4& r) { return (int)(r.z >> 8); }
+
+// Writes leaf record r at position lb (leaf_base + index) and its scan copy.
+__device__ __forceinline__ void put_leaf(const IndexView& v, long long lb, const uint4& r) {
+    v.leaf_rec[lb] = r;
+    v.leaf_lo[lb] = ((unsigned long long)r.y << 32) | r.x;
+    v.leaf_tc[lb] = (unsigned short)(min(r.w, 127u) | ((r.z & 0xFFu) << 7));
+}
+// Scan-copy fields: prefix length and token count.
+__device__ __forceinline__ int tc_t(unsigned tc) { return (int)(tc & 127u); }
+__device__ __forceinline__ int tc_cnt(unsigned tc) { return (int)(tc >> 7); }
 __device__ __forceinline__ int rec_cnt(const uint4& r) { return (int)(r.z & 0xFFu); }
 
 // Length of the common prefix of two 96-bit keys.

@@ -47,21 +47,23 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSubH = 8;      // sub-histograms per composite (lane groups)
 constexpr int kHistRow = 257;  // words per sub-histogram row (256 priorities + 1 pad)
-constexpr int kScanUnr = 8;   // leaf records in flight per thread
-constexpr int kRowUnr = 2;    // candidate rows per lane group per round
+constexpr int kRing = 3;      // scan chunks of 64 leaves in flight per warp
+constexpr int kSlotB = 640;   // one chunk: 64 corners (8 B) + 64 (t | count << 7) (2 B)
+constexpr int kRingB = kSelWarps * kRing * kSlotB;
 constexpr int kTieCap = 256;  // leaves at pi* ordered by rank counting; more -> range scan
 constexpr int kTopK = 32;     // warp top-k width
 constexpr int kFusedSmem = 108 * 1024;  // fused blocks grow to this (two blocks per SM)
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // bounded barrier wait
 
 // Shared-memory layout. sel/toff live through the whole kernel; keys .. top
-// hold the candidates and the page hash from phase 4 on. Everything from `free`
+// hold the leaf-record copy ring during the scan, then the page hash (from
+// phase 3b on) and the candidates (from phase 4 on). Everything from `free`
 // on is dead once the candidates are expanded: rescoring stages candidate rows
 // there, and the fused attention stages pages there (from `keys` on, after the
 // ranking) and finally the warps' partial results.
 struct SelSmem {
     int sel, toff;
-    int keys, vals, hpage, hkey, top;
+    int keys, vals, hpage, hkey, top, ring;
     int free;
     int prio, cnt, chosen, cmeta, coff, tie, tcnt, bm0, hist;
     int end;
@@ -80,6 +82,8 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
     s.hpage = o; o = align16(o + hcap * 4);
     s.hkey = o; o = align16(o + hcap * 8);
     s.top = o; o = align16(o + kSelWarps * kTopK * 12);
+    s.ring = s.keys;  // the scan's copy ring, dead before the candidates are written
+    if (o < s.ring + kRingB) o = s.ring + kRingB;
     s.free = o;
     const int Cp = align16((int)C);
     s.prio = o; o = align16(o + L * Cp);
@@ -150,12 +154,13 @@ __device__ __forceinline__ void cell_widths(int t, __half2 (&w)[4]) {
 }
 
 // L-infinity distance (code units) between the query codes q (biased fp16x2,
-// directions 2k, 2k+1 in word k) and the cell of a leaf record.
-__device__ __forceinline__ int leaf_priority(const uint4& rec, const __half2 (&q)[4],
+// directions 2k, 2k+1 in word k) and the cell of a leaf: lower corner codes 0-3
+// in x and 4-7 in y (one byte each), prefix length t.
+__device__ __forceinline__ int leaf_priority(unsigned x, unsigned y, int t, const __half2 (&q)[4],
                                              const __half2* widths /* [97][4] */) {
-    const __half2 lo[4] = {bytes_to_h2(rec.x, 0x4140u), bytes_to_h2(rec.x, 0x4342u),
-                           bytes_to_h2(rec.y, 0x4140u), bytes_to_h2(rec.y, 0x4342u)};
-    const int t = (int)min(rec.w, 96u);
+    const __half2 lo[4] = {bytes_to_h2(x, 0x4140u), bytes_to_h2(x, 0x4342u),
+                           bytes_to_h2(y, 0x4140u), bytes_to_h2(y, 0x4342u)};
+    t = min(t, 96);
     __half2 m[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -175,6 +180,12 @@ __device__ __forceinline__ int leaf_priority(const uint4& rec, const __half2 (&q
 __device__ __forceinline__ void st_shared_u8(unsigned char* p, int v) {
     const unsigned a = (unsigned)__cvta_generic_to_shared(p);
     asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"((unsigned)v & 0xFFu) : "memory");
+}
+
+// Two-byte store to shared memory (shared-window address a), explicit for the
+// same reason as st_shared_u8.
+__device__ __forceinline__ void st_shared_u16(unsigned a, int v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)(v & 0xFFFF)) : "memory");
 }
 
 // Ascending bitonic sort of one (key, value) per lane across the warp.
@@ -312,7 +323,6 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
         }
     }
     __syncthreads();
-    const int ntok = *s_ntok;
     const int rows_cap = stage_bytes / (2 * ROWB);
     const T* sk = reinterpret_cast<const T*>(stage);
     const T* sv = reinterpret_cast<const T*>(stage + (size_t)rows_cap * ROWB);
@@ -477,16 +487,32 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         load4(ud + 4 * lane, wdir);
         wlast = ud[kD];
     }
-    // first batch of composite 0, requested before its leaf count arrives (records
-    // past the count are read but never used; the capacity bounds the reads)
-    uint4 rb[kScanUnr];
-    {
-        const uint4* r0 = recs + v.leaf_base(u, 0);
+    // The scan streams the leaves' 10-byte scan copies through a per-warp ring of
+    // cp.async copies: warp w reads composite sl = w / wpc, chunks of 64 leaves
+    // wg, wg + wpc, ...; lane t copies (and later reads) leaves 2t and 2t+1 of a
+    // chunk, so each lane consumes only its own copies and no barrier is needed.
+    // The first kRing chunks are requested now, before the leaf count arrives
+    // (chunks past the count are copied but never read; the capacity, a multiple
+    // of 64, bounds the reads).
+    const int wpc = kSelWarps / L;
+    const int sl = warp / wpc, wg = warp % wpc;
+    const unsigned long long* slo = v.leaf_lo + v.leaf_base(u, sl);
+    const unsigned short* stc = v.leaf_tc + v.leaf_base(u, sl);
+    const unsigned ring = smem_u32(smem + lay.ring + warp * (kRing * kSlotB));
+    auto ring_issue = [&](int k, int slot) {
+        const unsigned d = ring + slot * kSlotB;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + lane * 16),
+                     "l"(slo + 64 * k + 2 * lane)
+                     : "memory");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d + 512 + lane * 4),
+                     "l"(stc + 64 * k + 2 * lane)
+                     : "memory");
+    };
 #pragma unroll
-        for (int k = 0; k < kScanUnr; ++k) {
-            const int i = k * kSelThreads + tid;
-            if (i < C) rb[k] = __ldg(r0 + i);
-        }
+    for (int sidx = 0; sidx < kRing; ++sidx) {
+        const int k = wg + sidx * wpc;
+        if (64LL * k < C) ring_issue(k, sidx);
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
     for (int l = 0; l < L; ++l) N[l] = N[l] < 0 ? 0 : (N[l] > C ? (int)C : N[l]);
     const int Ntot = N[0] + N[1];
@@ -522,10 +548,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     }
     for (int i = tid; i < L * kSubH * kHistRow; i += kSelThreads) hist[i] = 0;
     for (int i = tid; i < nwords; i += kSelThreads) bm0[i] = 0u;
-    for (int i = tid; i < hcap; i += kSelThreads) {
-        hpage[i] = -1;
-        hkey[i] = ~0ull;
-    }
     if (tid < kMaxL) {
         s_nch[tid] = 0;
         s_tot[tid] = 0;
@@ -545,53 +567,56 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 
     // ---- 2. priorities, counts and sub-histograms of token counts --------------------
     {
-        __half2 qc[kMaxL][4];
-#pragma unroll
-        for (int l = 0; l < kMaxL; ++l) {
+        __half2 qc[4];
+        {
             unsigned lo4 = 0, hi4 = 0;
-            if (l < L) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    lo4 |= (unsigned)s_qcode[l][j] << (8 * j);
-                    hi4 |= (unsigned)s_qcode[l][4 + j] << (8 * j);
-                }
+            for (int j = 0; j < 4; ++j) {
+                lo4 |= (unsigned)s_qcode[sl][j] << (8 * j);
+                hi4 |= (unsigned)s_qcode[sl][4 + j] << (8 * j);
             }
-            qc[l][0] = bytes_to_h2(lo4, 0x4140u);
-            qc[l][1] = bytes_to_h2(lo4, 0x4342u);
-            qc[l][2] = bytes_to_h2(hi4, 0x4140u);
-            qc[l][3] = bytes_to_h2(hi4, 0x4342u);
+            qc[0] = bytes_to_h2(lo4, 0x4140u);
+            qc[1] = bytes_to_h2(lo4, 0x4342u);
+            qc[2] = bytes_to_h2(hi4, 0x4140u);
+            qc[3] = bytes_to_h2(hi4, 0x4342u);
         }
-        const int sub = lane & (kSubH - 1);
-#pragma unroll
-        for (int l = 0; l < kMaxL; ++l) {
-            if (l >= L) break;
-            const uint4* rl = recs + v.leaf_base(u, l);
-            for (int base = 0; base < N[l]; base += kScanUnr * kSelThreads) {
-                if (l > 0 || base > 0) {
-#pragma unroll
-                    for (int k = 0; k < kScanUnr; ++k) {
-                        const int i = base + k * kSelThreads + tid;
-                        if (i < N[l]) rb[k] = __ldg(rl + i);
-                    }
-                }
-                // neighbouring leaves share few priorities (a handful per 32 leaves):
-                // lanes l, l+8, l+16, l+24 share a sub-histogram, so at most four
-                // lanes of an instruction add to one counter, and the 257-word row
-                // stride puts equal priorities of different sub-histograms in
-                // different banks
-#pragma unroll
-                for (int k = 0; k < kScanUnr; ++k) {
-                    const int i = base + k * kSelThreads + tid;
-                    if (i < N[l]) {
-                        const int pr = leaf_priority(rb[k], qc[l], s_width);
-                        const int cn = rec_cnt(rb[k]);
-                        st_shared_u8(prio + l * Cp + i, pr);
-                        st_shared_u8(cnts + l * Cp + i, cn);
-                        atomicAdd(&hist[(l * kSubH + sub) * kHistRow + pr], cn);
-                    }
-                }
+        // neighbouring leaves share few priorities (a handful per 32 leaves):
+        // lanes t, t+8, t+16, t+24 share a sub-histogram, so at most four lanes of
+        // an instruction add to one counter, and the 257-word row stride puts
+        // equal priorities of different sub-histograms in different banks
+        const int Nl = N[sl];
+        int* hl = hist + (sl * kSubH + (lane & (kSubH - 1))) * kHistRow;
+        const unsigned pr_base = smem_u32(prio + sl * Cp);
+        const unsigned cn_base = smem_u32(cnts + sl * Cp);
+        int slot = 0;
+        for (int k = wg; 64 * k < Nl; k += wpc) {  // warp-uniform
+            asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+            const unsigned d = ring + slot * kSlotB;
+            uint4 lo2;
+            unsigned tc2;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(lo2.x), "=r"(lo2.y), "=r"(lo2.z), "=r"(lo2.w)
+                         : "r"(d + lane * 16)
+                         : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tc2) : "r"(d + 512 + lane * 4) : "memory");
+            const int i0 = 64 * k + 2 * lane;
+            const unsigned tca = tc2 & 0xFFFFu, tcb = tc2 >> 16;
+            const int p0 = leaf_priority(lo2.x, lo2.y, tc_t(tca), qc, s_width);
+            const int p1 = leaf_priority(lo2.z, lo2.w, tc_t(tcb), qc, s_width);
+            const int c0 = tc_cnt(tca), c1 = tc_cnt(tcb);
+            if (i0 < Nl) {
+                st_shared_u16(pr_base + i0, p0 | (p1 << 8));
+                st_shared_u16(cn_base + i0, c0 | (c1 << 8));
+                atomicAdd(&hl[p0], c0);
+                if (i0 + 1 < Nl) atomicAdd(&hl[p1], c1);
             }
+            // the slot's values are in registers: refill it with the chunk kRing ahead
+            const int kn = k + kRing * wpc;
+            if (64 * kn < Nl) ring_issue(kn, slot);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            slot = slot + 1 == kRing ? 0 : slot + 1;
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     __syncthreads();
 
@@ -633,6 +658,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     __syncthreads();
 
     // ---- 3b. leaves below pi* are taken (records requested now); leaves at pi* listed ---
+    // (the page table takes over the scan ring's memory)
+    for (int i = tid; i < hcap; i += kSelThreads) {
+        hpage[i] = -1;
+        hkey[i] = ~0ull;
+    }
 #pragma unroll
     for (int l = 0; l < kMaxL; ++l) {
         if (l >= L) break;
