@@ -31,7 +31,13 @@ METRIC = "decode-step select+attn latency (µs/layer) & achieved HBM GB/s vs pea
 UNIT = "us/layer"
 WORKLOAD = "llama8b_36k"
 FLUSH_BYTES = 256 << 20
-LEAF_BYTES = 13  # information per leaf record: 8 B cell corner, 4 B id | count, 1 B depth
+INSERT_WORKLOAD = "mistral7b_gen8k"
+
+
+def leaf_bytes(w):
+    """Index bytes per leaf in the canonical count: the cell's low and high code
+    of every projection (2m bytes) plus a 4-byte count/offset."""
+    return 2 * w.n_proj + 4
 
 
 def _peaks():
@@ -208,6 +214,162 @@ def _traffic_for(kernel, src_file):
     return ent.get("dram_bytes_per_launch_full")
 
 
+def per_layer_serial(ice, w, keys, values, q, flush, timed, args):
+    """One launch per layer, in sequence, as a decode loop issues them: an index per
+    layer (its KV heads), and the step = n_layers fused calls after an L2 flush."""
+    import torch
+    idx, qs, outs = [], [], []
+    for l in range(w.n_layers):
+        kl = keys[:, l:l + 1].contiguous()
+        vl = values[:, l:l + 1].contiguous()
+        idx.append(ice.IceIndex.build(kl, vl, page_size=w.page_size, n_q_heads=w.n_q_heads,
+                                      n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed))
+        qs.append(q[:, l:l + 1].contiguous())
+        outs.append(torch.empty_like(qs[-1]))
+        del kl, vl
+
+    def step():
+        flush.zero_()
+        for ixl, ql, ol in zip(idx, qs, outs):
+            ixl.select_attn(ql, w.budget, ol)
+
+    n = max(20, args.steps // 30)
+    timed(step, 3)
+    t_f = timed(lambda: flush.zero_(), n)
+    t_s = timed(step, n)
+    for ixl in idx:
+        ixl.check()
+        ixl.destroy()
+    us = (t_s - t_f) / n * 1e3 / (w.n_layers * w.batch)
+    return {"value": round(us, 3), "unit": UNIT, "launches_per_step": w.n_layers,
+            "note": (f"each layer's {w.batch * w.n_kv_heads} units in their own launch, the "
+                     f"{w.n_layers} launches in sequence after an L2 flush")}
+
+
+def insert_run(ice, synth, dev, flush, timed, args):
+    """Generation with insertion (the Mistral-7B shape): prefill 8192 tokens, then
+    one inserted token per KV head per step for 8192 steps from a drifting
+    mixture; insert latency, select+attn latency before and after, leaf growth."""
+    import torch
+    w = synth.WORKLOADS[INSERT_WORKLOAD]
+    keys, values, centers = synth.make_kv(w, device=dev)
+    deltas = synth.make_drift(w, centers)
+    ks, vs = [], []
+    for t in range(w.n_insert):
+        k, v = synth.make_insert_token(w, centers, deltas, t)
+        ks.append(k)
+        vs.append(v)
+    K = torch.stack(ks)
+    V = torch.stack(vs)
+    del ks, vs
+    ix = ice.IceIndex.build(keys, values, page_size=w.page_size, n_q_heads=w.n_q_heads,
+                            n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed,
+                            max_tokens=w.n_tokens + w.n_insert)
+    q0 = synth.make_queries(w, centers, step=0, drift_deltas=deltas)
+    q1 = synth.make_queries(w, centers, step=w.n_insert, drift_deltas=deltas)
+    out = torch.empty_like(q0)
+    n_sa = max(50, args.steps // 20)
+
+    def sa_us(qq):
+        t_f = timed(lambda: flush.zero_(), n_sa)
+        t_s = timed(lambda: (flush.zero_(), ix.select_attn(qq, w.budget, out)), n_sa)
+        return (t_s - t_f) / n_sa * 1e3 / (w.n_layers * w.batch)
+
+    U = ix.n_units
+    leaves0 = [ix.dump(u)["n_leaf"] for u in range(U)]
+    before = sa_us(q0)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(w.n_insert):
+        ix.insert(K[t], V[t])
+    e1.record()
+    torch.cuda.synchronize()
+    ix.check()
+    us_ins = e0.elapsed_time(e1) * 1e3 / w.n_insert
+    after = sa_us(q1)
+    ix.check()
+    leaves1 = [ix.dump(u)["n_leaf"] for u in range(U)]
+    n_fin = w.n_tokens + w.n_insert
+    pages0 = sum(x[0] for x in leaves0)
+    pages1 = sum(x[0] for x in leaves1)
+    ix.destroy()
+    return {"workload": w.name, "units": U, "steps": w.n_insert,
+            "insert_us_per_step": round(us_ins, 3),
+            "note": ("one ice_insert call per step inserts one token into every unit; back-to-back "
+                     "calls, device time per call"),
+            "select_attn_us_per_layer_before": round(before, 3),
+            "select_attn_us_per_layer_after": round(after, 3),
+            "pages_per_unit_before": round(pages0 / U, 1), "pages_per_unit_after": round(pages1 / U, 1),
+            "occupancy_before": round(w.n_tokens * U / (pages0 * w.page_size), 4),
+            "occupancy_after": round(n_fin * U / (pages1 * w.page_size), 4),
+            "leaves_per_unit_after": [round(sum(x[l] for x in leaves1) / U, 1)
+                                      for l in range(w.n_composite)]}
+
+
+def _oracle_worker(a):
+    """One process of the parallel oracle timing: build untimed, then time
+    select+attn of its unit for the given wall budget."""
+    d, m, L, P, seed, budget, k, v, qq, secs = a
+    from oracle.oracle import OracleIndex
+    ix = OracleIndex(d, m, L, P, seed)
+    ix.build(k, v)
+    ids, npg, _ = ix.select(qq, budget)
+    ix.attn(qq, ids, npg)
+    reps = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < secs:
+        ids, npg, _ = ix.select(qq, budget)
+        ix.attn(qq, ids, npg)
+        reps += 1
+    return (time.perf_counter() - t0) / max(reps, 1)
+
+
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_parallel(w, keys, values, q, U, args):
+    """The oracle over independent units in nproc processes (spawned)."""
+    import multiprocessing as mp
+    nproc = os.cpu_count() or 1
+    units = [(i * U) // nproc for i in range(nproc)]
+    secs = max(2.0, args.cpu_seconds / 2)
+    jobs = []
+    for u in units:
+        k = keys.view(U, w.n_tokens, w.d)[u].float().cpu().numpy()
+        v = values.view(U, w.n_tokens, w.d)[u].float().cpu().numpy()
+        qq = q.view(U, w.group, w.d)[u].float().cpu().numpy()
+        jobs.append((w.d, w.n_proj, w.n_composite, w.page_size, w.seed, w.budget, k, v, qq, secs))
+    t0 = time.perf_counter()
+    with mp.get_context("spawn").Pool(nproc) as pool:
+        per = pool.map(_oracle_worker, jobs)
+    wall = time.perf_counter() - t0
+    units_per_layer = U // (w.n_layers * w.batch)
+    # nproc units in flight at once: throughput nproc / mean(seconds per unit)
+    us_layer = statistics.mean(per) * 1e6 * units_per_layer / nproc
+    return {"value": round(us_layer, 2), "unit": UNIT, "cores": nproc, "kind": "oracle",
+            "cpu": _cpu_model(), "wall_s": round(wall, 1),
+            "sample": (f"{nproc} units of this workload, one per process, each timed for "
+                       f"~{secs:.0f} s; build untimed")}
+
+
 def run_ice(args):
     import torch
     import torch.distributed as dist
@@ -243,21 +405,20 @@ def run_ice(args):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    # algorithmic bytes (counters verified against the oracle trace by the tests):
-    # per leaf record 13 B (8 code bytes of the cell's lower corner, 4 B id/count,
-    # 1 B prefix length), per rescored candidate its key row + 4 B id, per token of
-    # a selected page its K and V rows, q in, out back, page ids out/in
+    # canonical algorithmic bytes of a step (counters verified against the oracle
+    # trace by the tests): per leaf 2m + 4 B (cell low/high codes, count/offset),
+    # per rescored candidate its key row + 4 B id, per token of a selected page its
+    # K and V rows, per unit the G query rows in and the G output rows out
     ix.select(q, w.budget, page_ids, n_pages, stats)
     ix.sparse_attn(q, page_ids, n_pages, out)
     torch.cuda.synchronize()
     ix.check()
     st = stats.double().sum(0).tolist()
     es = 2 if w.dtype == torch.bfloat16 else 4
-    qo = U * w.group * w.d * es
-    ids_b = U * (n_sel + 1) * 4
-    sel_bytes = st[0] * LEAF_BYTES + st[1] * (w.d * es + 4) + qo + ids_b
-    attn_bytes = st[2] * 2 * w.d * es + 2 * qo + ids_b
-    step_bytes = sel_bytes + attn_bytes
+    q_b = U * w.group * w.d * es
+    sel_bytes = st[0] * leaf_bytes(w) + st[1] * (w.d * es + 4) + q_b
+    attn_bytes = st[2] * 2 * w.d * es + 2 * q_b
+    step_bytes = sel_bytes + attn_bytes - q_b  # the fused step reads q once
 
     def flush_only():
         flush.zero_()
@@ -352,7 +513,9 @@ def run_ice(args):
     else:
         dom, dom_bytes, dom_ms, src = "attn_kernel", attn_bytes, ms_att, "ice_attn.cu"
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
-    us_layer = ms_step * 1e3 / (w.n_layers * w.batch)
+    # every rank runs its own replica of the workload: the job processes
+    # world x n_layers layers per step
+    us_layer = ms_step * 1e3 / (w.n_layers * w.batch * world)
     line = {
         "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world,
         "steps": n_steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
@@ -375,7 +538,7 @@ def run_ice(args):
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": _traffic_for(dom, src), "algorithmic_bytes": int(dom_bytes)},
-        "e2e": {"value": round(ms_e2e * 1e3 / (w.n_layers * w.batch), 4), "unit": UNIT,
+        "e2e": {"value": round(ms_e2e * 1e3 / (w.n_layers * w.batch * world), 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(q.numel() * q.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size())},
         "gpu_launches": 4 * n_steps,
@@ -386,6 +549,13 @@ def run_ice(args):
         "wall_s_timed_region": round(wall, 3),
         "clocks": clk.summary(),
     }
+    # warm L2 (no flush): the same fused step repeated on resident data
+    t_w = timed(lambda: ix.select_attn(q, w.budget, out, page_ids, n_pages), max(100, args.steps // 3))
+    line["warm"] = {"value": round(t_w / max(100, args.steps // 3) * 1e3 / (w.n_layers * w.batch), 4),
+                    "unit": UNIT, "note": "no L2 flush between steps"}
+    if not args.no_extras:
+        line["per_layer_serial"] = per_layer_serial(ice, w, keys, values, q, flush, timed, args)
+        line["insert"] = insert_run(ice, synth, dev, flush, timed, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_units = [0, 85, 170, 255][: max(1, min(4, U))]
         ku = [keys.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]
@@ -408,6 +578,8 @@ def run_ice(args):
                        f"us/layer = us/unit x {units_per_layer} KV heads")}
         line["parity_sampled"] = {"units": sample_units, "page_ids_equal": bool(same),
                                   "byte_counters_equal": bool(stats_same)}
+        if not args.no_extras:
+            line["cpu_baseline_parallel"] = oracle_parallel(w, keys, values, q, U, args)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -425,6 +597,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-layer-serial, insert and parallel-oracle measurements")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -93,6 +93,8 @@ def _load():
 
 def as_f32(x) -> np.ndarray:
     """float32 view of a torch tensor / numpy array; bf16 is widened exactly."""
+    if isinstance(x, np.ndarray) or type(x).__module__.split(".")[0] != "torch":
+        return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
     try:
         import torch
         if isinstance(x, torch.Tensor):
