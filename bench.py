@@ -246,6 +246,78 @@ def per_layer_serial(ice, w, keys, values, q, flush, timed, args):
                      f"{w.n_layers} launches in sequence after an L2 flush")}
 
 
+def host_kv_run(ice, w, keys, values, q, flush, timed, args, st):
+    """The offloaded KV tier: the same workload with the page pool in pinned host
+    memory (the index stays in HBM); select+attn latency, the bytes read from
+    the pool per step over the CPU-GPU link, and the link's copy bandwidth."""
+    import torch
+    ix = ice.IceIndex.build(keys, values, page_size=w.page_size, n_q_heads=w.n_q_heads,
+                            n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed, kv_host=True)
+    out = torch.empty_like(q)
+    n = max(20, args.steps // 30)
+    timed(lambda: ix.select_attn(q, w.budget, out), 3)
+    t_f = timed(lambda: flush.zero_(), n)
+    t_s = timed(lambda: (flush.zero_(), ix.select_attn(q, w.budget, out)), n)
+    ix.check()
+    host_bytes = ix.info().host_bytes
+    ix.destroy()
+    ms = (t_s - t_f) / n
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    pool_bytes = st[1] * w.d * es + st[2] * 2 * w.d * es  # rescored key rows + selected pages
+    # the link: a pinned host -> device copy of 1 GiB
+    hbuf = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(1 << 30, dtype=torch.uint8, device=q.device)
+    t_c = timed(lambda: dbuf.copy_(hbuf, non_blocking=True), 5)
+    del hbuf, dbuf
+    return {"value": round(ms * 1e3 / (w.n_layers * w.batch), 3), "unit": UNIT,
+            "pool_bytes_per_step": int(pool_bytes),
+            "pool_read_gbs": round(pool_bytes / (ms * 1e-3) / 1e9, 1),
+            "link_h2d_copy_gbs": round(5 * (1 << 30) / (t_c * 1e-3) / 1e9, 1),
+            "host_pool_bytes": int(host_bytes),
+            "note": ("page pool (K and V rows) in pinned host memory mapped into the GPU; "
+                     "ice_select + ice_sparse_attn read it over the CPU-GPU link; L2 flushed "
+                     "between steps")}
+
+
+REUSE_R, REUSE_RHO, REUSE_STEPS = 8, 0.995, 64
+
+
+def reuse_run(ice, synth, ix, w, centers, flush, timed, args):
+    """Selection reuse across steps (ice_select_attn_reuse, r = REUSE_R) over a
+    stream of correlated decode queries (AR(1) noise, rho = REUSE_RHO)."""
+    import torch
+    U, n_sel = ix.n_units, w.budget // w.page_size
+    qs = synth.make_query_stream(w, centers, REUSE_STEPS, REUSE_RHO)
+    ids = torch.full((U, n_sel), -1, dtype=torch.int32, device=centers.device)
+    npg = torch.zeros((U,), dtype=torch.int32, device=centers.device)
+    out = torch.empty_like(qs[0])
+    flags = torch.zeros((REUSE_STEPS, U), dtype=torch.int32, device=centers.device)
+
+    def stream():
+        ix.reuse_reset()
+        for t in range(REUSE_STEPS):
+            flush.zero_()
+            ix.select_attn_reuse(qs[t], w.budget, REUSE_R, ids, npg, out, reselected=flags[t])
+
+    def flushes():
+        for _ in range(REUSE_STEPS):
+            flush.zero_()
+
+    timed(stream, 1)
+    reps = max(2, args.steps // 300)
+    t_s = timed(stream, reps)
+    t_f = timed(flushes, reps)
+    ix.check()
+    frac = float(flags.float().mean())
+    ms = (t_s - t_f) / (reps * REUSE_STEPS)
+    return {"value": round(ms * 1e3 / (w.n_layers * w.batch), 4), "unit": UNIT, "r": REUSE_R,
+            "reselect_fraction": round(frac, 4), "steps": REUSE_STEPS,
+            "note": (f"{REUSE_STEPS} consecutive steps of AR(1)-correlated queries (rho {REUSE_RHO}); "
+                     "a unit keeps its pages while its query codes are unchanged, at most r steps; "
+                     "L2 flushed between steps; two launches per step (reuse decision, fused "
+                     "select+attn)")}
+
+
 def insert_run(ice, synth, dev, flush, timed, args):
     """Generation with insertion (the Mistral-7B shape): prefill 8192 tokens, then
     one inserted token per KV head per step for 8192 steps from a drifting
@@ -556,6 +628,8 @@ def run_ice(args):
     if not args.no_extras:
         line["per_layer_serial"] = per_layer_serial(ice, w, keys, values, q, flush, timed, args)
         line["insert"] = insert_run(ice, synth, dev, flush, timed, args)
+        line["host_kv"] = host_kv_run(ice, w, keys, values, q, flush, timed, args, st)
+        line["reuse"] = reuse_run(ice, synth, ix, w, centers, flush, timed, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_units = [0, 85, 170, 255][: max(1, min(4, U))]
         ku = [keys.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]

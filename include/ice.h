@@ -68,7 +68,19 @@ typedef struct ice_params {
     int32_t dtype;       /* ICE_BF16 or ICE_F32                                      */
     int64_t max_tokens;  /* token capacity per unit (>= n_tokens of ice_build)       */
     uint64_t seed;       /* seed of the random projection directions (splitmix64)    */
+    int32_t kv_location; /* ICE_KV_DEVICE: the page pool in device memory (HBM);     */
+                         /* ICE_KV_HOST: in pinned host memory mapped into the       */
+                         /* GPU's address space, read by the kernels over the        */
+                         /* CPU-GPU link (the pages' offloaded KV tier)              */
+    int32_t reserved;    /* must be 0                                               */
 } ice_params;
+
+/* Page pool placement (ice_params.kv_location). With ICE_KV_HOST the index
+ * (leaf tables, slot lists, token locations) stays in device memory and only
+ * the K/V rows live on the host; ice_select_attn then runs as ice_select
+ * followed by ice_sparse_attn (both read the pool with plain or cp.async
+ * loads). */
+enum { ICE_KV_DEVICE = 0, ICE_KV_HOST = 1 };
 
 /*
  * ice_build - index the prefill keys and values (Figure 2 step 1, Figure 3).
@@ -145,6 +157,34 @@ int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t*
                     int32_t* n_pages, int32_t* stats, void* out, void* stream);
 
 /*
+ * ice_select_attn_reuse - ice_select_attn that keeps a unit's pages across
+ * calls ("IceCache" paper, the IceCache(r) variant, whose mechanism the pages
+ * leave open). Reading: a unit reuses the pages of its last selection for up
+ * to r further calls while its query codes (the 8-bit codes of the group
+ * query on every projection direction, which the selection computes first)
+ * are exactly those of the call that selected the pages. Any changed code, r
+ * reuses in a row, a unit without a selection yet or a changed token_budget
+ * selects again. Inserted tokens are seen: the attention reads each page's
+ * current tokens.
+ *
+ * page_ids, n_pages: device, as in ice_select; they carry the selection from
+ * call to call, so the same buffers must be passed every time (in: the pages
+ * in use; out: the pages used by this call).
+ * r: >= 0 (0 selects on every call, the same as ice_select_attn).
+ * reselected: optional device int32 [units]; 1 where this call selected.
+ * out: as in ice_select_attn.
+ * The per-unit codes and reuse counts live in the index (allocated on the
+ * first call, ICE_ERR_CAPACITY if that fails). stats are not written.
+ */
+int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, int32_t r,
+                          int32_t* page_ids, int32_t* n_pages, int32_t* reselected, void* out,
+                          void* stream);
+
+/* ice_reuse_reset - forget every unit's kept selection (the next
+ * ice_select_attn_reuse selects everywhere). Asynchronous on `stream`. */
+int ice_reuse_reset(ice_index* ix, void* stream);
+
+/*
  * ice_sparse_attn - attention of each query head over every token of the
  * selected pages (Figure 2 step 3).
  *
@@ -183,6 +223,9 @@ typedef struct ice_info {
     int32_t n_composite;   /* L                                                 */
     int32_t page_size;     /* P                                                 */
     int32_t dtype;         /* ICE_BF16 / ICE_F32                                */
+    int64_t host_bytes;    /* pinned host bytes held by the handle (host pool)  */
+    int32_t kv_location;   /* ICE_KV_DEVICE / ICE_KV_HOST                       */
+    int32_t reserved;
 } ice_info;
 
 int ice_get_info(const ice_index* ix, ice_info* info);

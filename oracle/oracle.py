@@ -282,3 +282,41 @@ class OracleIndex:
         out = np.zeros(max(k, 1), np.int32)
         self._lib.orc_exact_topk(self._h, q.reshape(-1), q.shape[0], k, out)
         return out[:k]
+
+
+class ReuseOracle:
+    """Selection reuse across decode steps ("IceCache" paper, the IceCache(r)
+    variant; the pages name it but give no mechanism).
+
+    Reading: a unit keeps the pages of its last selection for up to r further
+    steps while its query codes (``OracleIndex.query``: the 8-bit codes of the
+    group query on every projection direction) are exactly those of the step
+    that selected them. A changed code, r reuses in a row, no selection yet or
+    a changed budget selects again. The attention always reads the kept pages'
+    current tokens (inserted tokens included).
+    """
+
+    def __init__(self, index: OracleIndex, r: int):
+        if r < 0:
+            raise ValueError("r must be >= 0")
+        self.ix = index
+        self.r = r
+        self.codes = None
+        self.age = -1
+        self.budget = None
+        self.ids = None
+        self.npg = 0
+
+    def step(self, q, budget: int, n_cand: int | None = None):
+        """One decode step: returns (page_ids, n_pages, reselected, attention)."""
+        codes, _ = self.ix.query(q)
+        keep = (self.codes is not None and self.budget == budget and 0 <= self.age < self.r
+                and np.array_equal(codes, self.codes))
+        if keep:
+            self.age += 1
+        else:
+            self.ids, self.npg, _ = self.ix.select(q, budget, n_cand)
+            self.codes = codes
+            self.budget = budget
+            self.age = 0
+        return self.ids, self.npg, not keep, self.ix.attn(q, self.ids, self.npg)

@@ -17,8 +17,15 @@ struct ice_index {
     long long C = 0;
     long long n_tok = 0;
     size_t bytes = 0;
+    size_t host_bytes = 0;
     int device = 0;
     std::vector<void*> owned;
+    std::vector<void*> owned_host;  // pinned host page pool (ICE_KV_HOST)
+    // selection reuse across steps (ice_select_attn_reuse), allocated on first use
+    unsigned char* reuse_codes = nullptr;  // [U][kMaxL * kM] query codes of the last selection
+    int* reuse_age = nullptr;              // [U] reuses since that selection; -1 = none
+    int32_t* reuse_flag = nullptr;         // [U] 1 where this step selects
+    int reuse_budget = -1;
     IndexView v;
 };
 
@@ -44,6 +51,7 @@ int check_params(const ice_params* p) {
     if (p->n_composite < 1 || p->n_composite > kMaxL) return ICE_ERR_INVALID_ARG;
     if (p->n_cand < 0) return ICE_ERR_INVALID_ARG;
     if (p->dtype != ICE_F32 && p->dtype != ICE_BF16) return ICE_ERR_INVALID_ARG;
+    if (p->kv_location != ICE_KV_DEVICE && p->kv_location != ICE_KV_HOST) return ICE_ERR_INVALID_ARG;
     if (p->max_tokens < 0 || p->max_tokens > (1LL << 30)) return ICE_ERR_INVALID_ARG;
     const long long units = (long long)p->batch * p->n_layers * p->n_kv_heads;
     if (units > (1LL << 24)) return ICE_ERR_INVALID_ARG;
@@ -64,9 +72,27 @@ cudaError_t dev_alloc(ice_index* ix, T** out, size_t count) {
     return cudaSuccess;
 }
 
+// Pinned host memory mapped into the device's address space; *out is the
+// device-side address of it.
+cudaError_t host_alloc(ice_index* ix, unsigned char** out, size_t bytes) {
+    void* h = nullptr;
+    bytes = std::max<size_t>(bytes, 16);
+    cudaError_t e = cudaHostAlloc(&h, bytes, cudaHostAllocMapped);
+    if (e != cudaSuccess) return e;
+    ix->owned_host.push_back(h);
+    ix->host_bytes += bytes;
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, h, 0);
+    if (e != cudaSuccess) return e;
+    *out = reinterpret_cast<unsigned char*>(d);
+    return cudaSuccess;
+}
+
 void free_all(ice_index* ix) {
     for (void* p : ix->owned) cudaFree(p);
     ix->owned.clear();
+    for (void* p : ix->owned_host) cudaFreeHost(p);
+    ix->owned_host.clear();
 }
 
 }  // namespace
@@ -187,8 +213,14 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         okc = okc && dev_alloc(ix, &v.tok_loc, (size_t)U * v.max_tokens) == cudaSuccess;
         unsigned char* pk = nullptr;
         unsigned char* pv = nullptr;
-        okc = okc && dev_alloc(ix, &pk, (size_t)U * C * P * kD * es) == cudaSuccess;
-        okc = okc && dev_alloc(ix, &pv, (size_t)U * C * P * kD * es) == cudaSuccess;
+        const size_t pool = (size_t)U * C * P * kD * es;
+        if (params->kv_location == ICE_KV_HOST) {
+            okc = okc && host_alloc(ix, &pk, pool) == cudaSuccess;
+            okc = okc && host_alloc(ix, &pv, pool) == cudaSuccess;
+        } else {
+            okc = okc && dev_alloc(ix, &pk, pool) == cudaSuccess;
+            okc = okc && dev_alloc(ix, &pv, pool) == cudaSuccess;
+        }
         if (!okc) {
             scratch_free(s, st);
             cudaGetLastError();
@@ -233,8 +265,8 @@ int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
     return ICE_OK;
 }
 
-static int select_common(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
-                         int32_t* n_pages, int32_t* stats, void* out, void* stream) {
+static int select_args(const ice_index* ix, const void* q, int32_t token_budget,
+                       const int32_t* page_ids, const int32_t* n_pages, const void* out) {
     if (!ix || !q || !page_ids || !n_pages || !aligned16(q)) return ICE_ERR_INVALID_ARG;
     if (out && !aligned16(out)) return ICE_ERR_INVALID_ARG;
     const int P = ix->p.page_size;
@@ -246,7 +278,18 @@ static int select_common(ice_index* ix, const void* q, int32_t token_budget, int
     if (select_smem_bytes(ix->C, ix->p.n_composite, P, n_cand, n_sel, ix->G, out != nullptr) >
         200 * 1024)
         return ICE_ERR_UNSUPPORTED;
-    cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, stats, out,
+    return ICE_OK;
+}
+
+static int select_common(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
+                         int32_t* n_pages, int32_t* stats, void* out, void* stream,
+                         const int32_t* reselect = nullptr) {
+    const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
+    if (a != ICE_OK) return a;
+    const int P = ix->p.page_size;
+    const int n_sel = token_budget / P;
+    const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
+    cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect,
                                   (cudaStream_t)stream);
     return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
 }
@@ -258,8 +301,65 @@ int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page
 
 int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
                     int32_t* n_pages, int32_t* stats, void* out, void* stream) {
-    if (!out) return ICE_ERR_INVALID_ARG;
+    if (!ix || !out) return ICE_ERR_INVALID_ARG;
+    if (ix->p.kv_location == ICE_KV_HOST) {
+        // the fused kernel stages pages with bulk tensor-memory copies; a host pool
+        // is read by the two plain-load kernels instead
+        if (!aligned16(out)) return ICE_ERR_INVALID_ARG;
+        int r = select_common(ix, q, token_budget, page_ids, n_pages, stats, nullptr, stream);
+        if (r != ICE_OK) return r;
+        return ice_sparse_attn(ix, q, page_ids, n_pages, token_budget / ix->p.page_size, out, stream);
+    }
     return select_common(ix, q, token_budget, page_ids, n_pages, stats, out, stream);
+}
+
+int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, int32_t r,
+                          int32_t* page_ids, int32_t* n_pages, int32_t* reselected, void* out,
+                          void* stream) {
+    if (!ix || !out || r < 0) return ICE_ERR_INVALID_ARG;
+    const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
+    if (a != ICE_OK) return a;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int U = ix->U;
+    if (!ix->reuse_age) {
+        bool ok = dev_alloc(ix, &ix->reuse_codes, (size_t)U * kMaxL * kM) == cudaSuccess;
+        ok = ok && dev_alloc(ix, &ix->reuse_age, (size_t)U) == cudaSuccess;
+        ok = ok && dev_alloc(ix, &ix->reuse_flag, (size_t)U) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            return ICE_ERR_CAPACITY;
+        }
+        ix->reuse_budget = -1;
+    }
+    if (token_budget != ix->reuse_budget) {  // kept pages were chosen for another budget
+        if (cudaMemsetAsync(ix->reuse_age, 0xFF, sizeof(int) * U, st) != cudaSuccess) return ICE_ERR_CUDA;
+        ix->reuse_budget = token_budget;
+    }
+    if (launch_reuse(ix->v, q, r, ix->reuse_codes, ix->reuse_age, ix->reuse_flag, st) != cudaSuccess)
+        return ICE_ERR_CUDA;
+    int res;
+    if (ix->p.kv_location == ICE_KV_HOST) {
+        res = select_common(ix, q, token_budget, page_ids, n_pages, nullptr, nullptr, stream,
+                            ix->reuse_flag);
+        if (res == ICE_OK)
+            res = ice_sparse_attn(ix, q, page_ids, n_pages, token_budget / ix->p.page_size, out, stream);
+    } else {
+        res = select_common(ix, q, token_budget, page_ids, n_pages, nullptr, out, stream,
+                            ix->reuse_flag);
+    }
+    if (res == ICE_OK && reselected &&
+        cudaMemcpyAsync(reselected, ix->reuse_flag, sizeof(int32_t) * U, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
+        return ICE_ERR_CUDA;
+    return res;
+}
+
+int ice_reuse_reset(ice_index* ix, void* stream) {
+    if (!ix) return ICE_ERR_INVALID_ARG;
+    if (!ix->reuse_age) return ICE_OK;
+    return cudaMemsetAsync(ix->reuse_age, 0xFF, sizeof(int) * ix->U, (cudaStream_t)stream) == cudaSuccess
+               ? ICE_OK
+               : ICE_ERR_CUDA;
 }
 
 int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const int32_t* n_pages,
@@ -300,6 +400,9 @@ int ice_get_info(const ice_index* ix, ice_info* info) {
     info->n_composite = ix->p.n_composite;
     info->page_size = ix->p.page_size;
     info->dtype = ix->p.dtype;
+    info->host_bytes = (int64_t)ix->host_bytes;
+    info->kv_location = ix->p.kv_location;
+    info->reserved = 0;
     return ICE_OK;
 }
 
@@ -358,8 +461,8 @@ int ice_debug_page(ice_index* ix, int32_t unit, int32_t page_id, void* host_k, v
     const size_t es = ix->p.dtype == ICE_BF16 ? 2 : 4;
     const size_t bytes = (size_t)ix->p.page_size * kD * es;
     const size_t off = (size_t)ix->v.page_row(unit, page_id, 0) * kD * es;
-    bool ok = cudaMemcpy(host_k, (char*)ix->v.page_k + off, bytes, cudaMemcpyDeviceToHost) == cudaSuccess;
-    ok = ok && cudaMemcpy(host_v, (char*)ix->v.page_v + off, bytes, cudaMemcpyDeviceToHost) == cudaSuccess;
+    bool ok = cudaMemcpy(host_k, (char*)ix->v.page_k + off, bytes, cudaMemcpyDefault) == cudaSuccess;
+    ok = ok && cudaMemcpy(host_v, (char*)ix->v.page_v + off, bytes, cudaMemcpyDefault) == cudaSuccess;
     return ok ? ICE_OK : ICE_ERR_CUDA;
 }
 

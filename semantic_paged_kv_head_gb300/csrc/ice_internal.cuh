@@ -282,9 +282,15 @@ cudaError_t select_prepare();
 cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, long long tok,
                           cudaStream_t s);
 // out == nullptr: select only; otherwise select and attend over the selection.
+// reselect: nullable [U]; a unit whose flag is 0 keeps its pages (page_ids,
+// n_pages unchanged) and, in the fused call, attends over them
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
                           int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                          cudaStream_t s);
+                          const int32_t* reselect, cudaStream_t s);
+// Reuse decision per unit (query codes against the codes of the unit's last
+// selection, and the reuse age); writes reselect[U] and updates codes/age.
+cudaError_t launch_reuse(const IndexView& v, const void* q, int r, unsigned char* codes, int* age,
+                         int32_t* reselect, cudaStream_t s);
 cudaError_t launch_attn(const IndexView& v, const void* q, const int32_t* page_ids,
                         const int32_t* n_pages, int page_stride, void* out, cudaStream_t s);
 

@@ -437,7 +437,7 @@ template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
     int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
-    int32_t* __restrict__ stats, T* __restrict__ attn_out) {
+    int32_t* __restrict__ stats, T* __restrict__ attn_out, const int32_t* __restrict__ reselect) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
@@ -472,6 +472,24 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int* topv = reinterpret_cast<int*>(smem + lay.top + kSelWarps * kTopK * 8);
     const int nwords = (int)((C + 31) / 32);
     const uint4* recs = v.leaf_rec;
+
+    // the unit keeps the pages it selected before (reuse across steps): no
+    // selection, and the fused call attends over the pages in page_ids
+    if (reselect != nullptr && reselect[u] == 0) {  // block-uniform
+        if (FUSED) {
+            const int taken = min(max(n_pages_out[u], 0), n_sel);
+            for (int i = tid; i < taken; i += kSelThreads) s_sel[i] = page_ids[(long long)u * n_sel + i];
+            if (tid == 0) {
+                s_fail = 0;
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
+                asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            }
+            __syncthreads();
+            attend_staged<T, G>(v, u, q, taken, s_sel, s_toff, &s_ntok, smem + lay.keys,
+                                smem_total - lay.keys, smem_u32(&s_bar), &s_fail, attn_out);
+        }
+        return;
+    }
 
     // ---- 1. leaf counts, query heads and directions requested together -------------------
     int N[kMaxL] = {0, 0};
@@ -1082,39 +1100,42 @@ int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, b
 template <typename T, int G>
 static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel, int n_cand,
                                    int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                                   cudaStream_t s) {
+                                   const int32_t* reselect, cudaStream_t s) {
     int sort_cap, hcap;
     select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
     const bool fused = out != nullptr;
     const int bytes = select_smem_bytes(v.C, v.L, v.P, n_cand, n_sel, G, fused);
     if (fused)
         select_kernel<T, G, true><<<v.U, kSelThreads, bytes, s>>>(
-            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, (T*)out);
+            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, (T*)out,
+            reselect);
     else
         select_kernel<T, G, false><<<v.U, kSelThreads, bytes, s>>>(
-            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, nullptr);
+            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, nullptr,
+            reselect);
     return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t launch_select_dt(const IndexView& v, const void* q, int n_sel, int n_cand,
                                     int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                                    cudaStream_t s) {
+                                    const int32_t* reselect, cudaStream_t s) {
     switch (v.G) {
-        case 1: return launch_select_g<T, 1>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
-        case 2: return launch_select_g<T, 2>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
-        case 4: return launch_select_g<T, 4>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
-        case 8: return launch_select_g<T, 8>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+        case 1: return launch_select_g<T, 1>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
+        case 2: return launch_select_g<T, 2>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
+        case 4: return launch_select_g<T, 4>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
+        case 8: return launch_select_g<T, 8>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
                           int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                          cudaStream_t s) {
+                          const int32_t* reselect, cudaStream_t s) {
     if (v.dtype == ICE_BF16)
-        return launch_select_dt<__nv_bfloat16>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
-    return launch_select_dt<float>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+        return launch_select_dt<__nv_bfloat16>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out,
+                                               reselect, s);
+    return launch_select_dt<float>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
 }
 
 // Raise the dynamic shared memory limit of the select kernels once per device.

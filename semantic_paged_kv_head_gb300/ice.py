@@ -35,7 +35,7 @@ ICE_BF16 = 1
 # every symbol include/ice.h declares
 EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_select_attn", "ice_sparse_attn", "ice_get_error",
            "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page",
-           "ice_key_codes_noalloc"]
+           "ice_key_codes_noalloc", "ice_select_attn_reuse", "ice_reuse_reset"]
 
 
 class ice_params(ctypes.Structure):
@@ -44,7 +44,11 @@ class ice_params(ctypes.Structure):
                 ("batch", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("n_proj", ctypes.c_int32), ("n_composite", ctypes.c_int32),
                 ("n_cand", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("max_tokens", ctypes.c_int64), ("seed", ctypes.c_uint64)]
+                ("max_tokens", ctypes.c_int64), ("seed", ctypes.c_uint64),
+                ("kv_location", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+KV_DEVICE, KV_HOST = 0, 1  # ice_params.kv_location
 
 
 class ice_info(ctypes.Structure):
@@ -52,7 +56,8 @@ class ice_info(ctypes.Structure):
                 ("max_tokens", ctypes.c_int64), ("list_capacity", ctypes.c_int64),
                 ("pool_bytes", ctypes.c_int64), ("group", ctypes.c_int32),
                 ("n_composite", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("host_bytes", ctypes.c_int64),
+                ("kv_location", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class IceError(RuntimeError):
@@ -92,6 +97,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_debug_page.restype = ctypes.c_int
     lib.ice_key_codes_noalloc.argtypes = [P(ice_params), vp, i64, vp, vp, vp]
     lib.ice_key_codes_noalloc.restype = ctypes.c_int
+    lib.ice_select_attn_reuse.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp]
+    lib.ice_select_attn_reuse.restype = ctypes.c_int
+    lib.ice_reuse_reset.argtypes = [vp, vp]
+    lib.ice_reuse_reset.restype = ctypes.c_int
     return lib
 
 
@@ -142,15 +151,17 @@ class IceIndex:
     @classmethod
     def build(cls, keys: torch.Tensor, values: torch.Tensor, *, page_size: int, n_q_heads: int,
               n_composite: int = 2, n_proj: int = 8, n_cand: int = 0, max_tokens: int | None = None,
-              seed: int = 0, stream=None) -> "IceIndex":
-        """ice_build over keys/values shaped [batch, layers, kv_heads, n, d]."""
+              seed: int = 0, kv_host: bool = False, stream=None) -> "IceIndex":
+        """ice_build over keys/values shaped [batch, layers, kv_heads, n, d].
+
+        kv_host places the page pool in pinned host memory (ICE_KV_HOST)."""
         if keys.dim() != 5 or keys.shape != values.shape:
             raise ValueError("keys/values must be [batch, layers, kv_heads, n, d] and equal in shape")
         B, Ly, H, n, d = keys.shape
         p = ice_params(d=d, n_kv_heads=H, n_q_heads=n_q_heads, n_layers=Ly, batch=B,
                        page_size=page_size, n_proj=n_proj, n_composite=n_composite, n_cand=n_cand,
                        dtype=_code(keys.dtype), max_tokens=n if max_tokens is None else max_tokens,
-                       seed=seed)
+                       seed=seed, kv_location=KV_HOST if kv_host else KV_DEVICE, reserved=0)
         h = ctypes.c_void_p()
         kp = _dev_ptr(keys, values.dtype, "keys") if n else 0
         vp = _dev_ptr(values, keys.dtype, "values") if n else 0
@@ -200,6 +211,25 @@ class IceIndex:
                                     _dev_ptr(out, self.dtype, "out"), _stream(stream)),
                "ice_select_attn")
         return out, page_ids, n_pages
+
+    def select_attn_reuse(self, q: torch.Tensor, token_budget: int, r: int, page_ids: torch.Tensor,
+                          n_pages: torch.Tensor, out: torch.Tensor | None = None,
+                          reselected: torch.Tensor | None = None, stream=None):
+        """ice_select_attn_reuse; page_ids/n_pages carry the selection between calls
+        (pass the same tensors every step). Returns (out, page_ids, n_pages)."""
+        if out is None:
+            out = torch.empty_like(q)
+        _check(_lib.ice_select_attn_reuse(self._h, _dev_ptr(q, self.dtype, "q"), int(token_budget),
+                                          int(r), _dev_ptr(page_ids, torch.int32, "page_ids"),
+                                          _dev_ptr(n_pages, torch.int32, "n_pages"),
+                                          (_dev_ptr(reselected, torch.int32, "reselected")
+                                           if reselected is not None else None),
+                                          _dev_ptr(out, self.dtype, "out"), _stream(stream)),
+               "ice_select_attn_reuse")
+        return out, page_ids, n_pages
+
+    def reuse_reset(self, stream=None):
+        _check(_lib.ice_reuse_reset(self._h, _stream(stream)), "ice_reuse_reset")
 
     def sparse_attn(self, q: torch.Tensor, page_ids: torch.Tensor, n_pages: torch.Tensor,
                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -30,6 +30,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass, field
 
+import math
+
 import torch
 
 
@@ -147,6 +149,28 @@ def make_queries(w: Workload, centers: torch.Tensor, step: int = 0, device=None,
         mu = mu + (step / w.n_insert) * drift_deltas[torch.arange(U, device=device), c_star]
     q = mu[:, None, :] + w.spread * _randn((U, G, d), g, device)
     return q.to(w.dtype).view(w.batch, w.n_layers, w.n_kv_heads * G, d)
+
+
+def make_query_stream(w: Workload, centers: torch.Tensor, n_steps: int, rho: float, device=None):
+    """Queries of ``n_steps`` consecutive decode steps: each unit's queries stay
+    around one centre and their noise follows an AR(1) process
+    ``z_t = rho z_(t-1) + sqrt(1 - rho^2) e_t`` (consecutive queries of a head
+    are correlated; ``rho`` sets how much). Returns a list of tensors shaped
+    like ``make_queries``."""
+    device = centers.device if device is None else device
+    g = _gen(w.seed * 1_000_003 + 61, device)
+    U, d, G = w.n_units, w.d, w.group
+    c_star = torch.randint(0, w.n_centers, (U,), generator=g, device=device)
+    mu = centers[torch.arange(U, device=device), c_star]
+    z = _randn((U, G, d), g, device)
+    a = math.sqrt(max(0.0, 1.0 - rho * rho))
+    out = []
+    for t in range(n_steps):
+        if t:
+            z = rho * z + a * _randn((U, G, d), g, device)
+        q = mu[:, None, :] + w.spread * z
+        out.append(q.to(w.dtype).view(w.batch, w.n_layers, w.n_kv_heads * G, d))
+    return out
 
 
 def make_drift(w: Workload, centers: torch.Tensor):

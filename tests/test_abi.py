@@ -50,7 +50,8 @@ def test_host_side_argument_errors(lib):
            ("page_size", 0, lib.ICE_ERR_INVALID_ARG), ("page_size", 65, lib.ICE_ERR_INVALID_ARG),
            ("n_composite", 3, lib.ICE_ERR_INVALID_ARG), ("n_q_heads", 30, lib.ICE_ERR_INVALID_ARG),
            ("n_q_heads", 24, lib.ICE_ERR_UNSUPPORTED), ("dtype", 7, lib.ICE_ERR_INVALID_ARG),
-           ("n_cand", -1, lib.ICE_ERR_INVALID_ARG), ("max_tokens", -1, lib.ICE_ERR_INVALID_ARG)]
+           ("n_cand", -1, lib.ICE_ERR_INVALID_ARG), ("max_tokens", -1, lib.ICE_ERR_INVALID_ARG),
+           ("kv_location", 2, lib.ICE_ERR_INVALID_ARG)]
     for field, val, code in bad:
         q = lib.ice_params.from_buffer_copy(p)
         setattr(q, field, val)
@@ -68,3 +69,32 @@ def test_host_side_argument_errors(lib):
     info = lib.ice_info()
     assert raw.ice_get_info(None, ctypes.byref(info)) == lib.ICE_ERR_INVALID_ARG
     raw.ice_destroy(None)  # a no-op
+
+
+def test_struct_layouts_match_the_header(lib, tmp_path):
+    """The ctypes mirrors of ice_params and ice_info have the header's field
+    offsets and sizes (compiled with the host C compiler)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    structs = {"ice_params": lib.ice_params, "ice_info": lib.ice_info}
+    lines = ['#include <stdio.h>', '#include "ice.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{name} {fname} %zu\\n", offsetof({name}, {fname}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        name, field, val = line.split()
+        got[(name, field)] = int(val)
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for fname, _ in cls._fields_:
+            assert got[(name, fname)] == getattr(cls, fname).offset, (name, fname)

@@ -30,10 +30,10 @@ def _synth():
     return synth
 
 
-def _run(ice, w, keys, values, q, max_tokens=None):
+def _run(ice, w, keys, values, q, max_tokens=None, kv_host=False):
     gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
                              n_q_heads=w.n_q_heads, n_composite=w.n_composite, n_proj=w.n_proj,
-                             seed=w.seed, max_tokens=max_tokens)
+                             seed=w.seed, max_tokens=max_tokens, kv_host=kv_host)
     qd = q.cuda().contiguous()
     stats = torch.zeros((gix.n_units, 4), dtype=torch.int32, device="cuda")
     ids, npg = gix.select(qd, w.budget, stats=stats)
@@ -51,11 +51,11 @@ def _run(ice, w, keys, values, q, max_tokens=None):
     return gix, ids, npg, out, stats
 
 
-def _full_check(ice, w, units=None, max_pages=8):
+def _full_check(ice, w, units=None, max_pages=8, kv_host=False):
     synth = _synth()
     keys, values, centers = synth.make_kv(w)
     q = synth.make_queries(w, centers)
-    gix, ids, npg, out, stats = _run(ice, w, keys, values, q)
+    gix, ids, npg, out, stats = _run(ice, w, keys, values, q, kv_host=kv_host)
     units = range(w.n_units) if units is None else units
     errs = []
     for u in units:
@@ -167,6 +167,51 @@ def test_insert_matches_oracle(ice):
                 compare_index(gix.dump(u), orcs[u], f"step {s} unit {u}")
                 check_select_attn(w, orcs[u], q_of_unit(w, q, u), ids[u], npg[u],
                                   out.view(-1, w.group, w.d)[u], None, f"step {s} unit {u}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_host_resident_pool(ice, dtype):
+    """Page pool in pinned host memory (the offloaded KV tier): same index, same
+    pages and the same attention as the oracle; the pool bytes are on the host."""
+    synth = _synth()
+    w = synth.scaled(synth.WORKLOADS["llama8b_36k"], n_layers=2, n_kv_heads=2, n_tokens=3001,
+                     dtype=dtype, n_centers=32, seed=11)
+    _full_check(ice, w, kv_host=True)
+    keys, values, centers = synth.make_kv(w)
+    gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                             n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed,
+                             kv_host=True)
+    inf = gix.info()
+    assert inf.kv_location == ice.KV_HOST
+    es = 2 if dtype == torch.bfloat16 else 4
+    assert inf.host_bytes >= 2 * gix.n_units * inf.list_capacity * w.page_size * w.d * es
+
+
+def test_host_resident_pool_inserts(ice):
+    """Inserts write the new rows into the host pool; selections follow the oracle."""
+    synth = _synth()
+    w = synth.scaled(synth.WORKLOADS["mistral7b_gen8k"], n_kv_heads=2, n_tokens=500,
+                     n_insert=120, n_centers=16, seed=15)
+    keys, values, centers = synth.make_kv(w)
+    deltas = synth.make_drift(w, centers)
+    gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                             n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed,
+                             max_tokens=w.n_tokens + w.n_insert, kv_host=True)
+    orcs = [oracle_for_unit(w, keys, values, u) for u in range(w.n_units)]
+    for s in range(w.n_insert):
+        k, v = synth.make_insert_token(w, centers, deltas, s)
+        gix.insert(k.cuda(), v.cuda())
+        for u in range(w.n_units):
+            orcs[u].insert(k.view(-1, w.d)[u], v.view(-1, w.d)[u])
+    q = synth.make_queries(w, centers, step=w.n_insert, drift_deltas=deltas)
+    out, ids, npg = gix.select_attn(q.cuda(), w.budget)
+    torch.cuda.synchronize()
+    assert gix.get_error() == 0
+    for u in range(w.n_units):
+        gd = gix.dump(u)
+        compare_index(gd, orcs[u], f"unit {u}")
+        check_select_attn(w, orcs[u], q_of_unit(w, q, u), ids[u], npg[u],
+                          out.view(-1, w.group, w.d)[u], None, f"unit {u}")
 
 
 def test_empty_build_then_inserts(ice):
