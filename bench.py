@@ -318,6 +318,56 @@ def reuse_run(ice, synth, ix, w, centers, flush, timed, args):
                      "select+attn)")}
 
 
+RECALL_NCAND = (1, 2, 4)  # n_cand as multiples of the token budget (shared-memory bound: <= 4x)
+
+
+def recall_run(ice, w, keys, values, q, flush, timed, args):
+    """recall@k (k = the token budget) of the tokens in the selected pages against
+    the exact top-k of the group query q_sel . k (fp64 brute force), for one
+    layer of the workload and n_cand = 1, 2, 4 x budget; with the latency of
+    that layer's fused call (one launch, L2 flushed)."""
+    import numpy as np
+    import torch
+    kl = keys[:, :1].contiguous()
+    vl = values[:, :1].contiguous()
+    ql = q[:, :1].contiguous()
+    U1 = w.batch * w.n_kv_heads
+    K = kl.view(U1, w.n_tokens, w.d).float().cpu().numpy().astype(np.float64)
+    Q = ql.view(U1, w.group, w.d).float().cpu().numpy()
+    k = w.budget
+    top = []
+    for u in range(U1):
+        qs = Q[u].sum(0, dtype=np.float32).astype(np.float64)  # q_sel in fp32, as selected
+        sc = K[u] @ qs
+        top.append(set(np.argpartition(-sc, k - 1)[:k].tolist()))
+    res = []
+    out = torch.empty_like(ql)
+    for mult in RECALL_NCAND:
+        ix = ice.IceIndex.build(kl, vl, page_size=w.page_size, n_q_heads=w.n_q_heads,
+                                n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed,
+                                n_cand=mult * w.budget)
+        _, ids, npg = ix.select_attn(ql, w.budget, out)
+        torch.cuda.synchronize()
+        ix.check()
+        rec = []
+        for u in range(U1):
+            c0 = ix.dump(u)["comp"][0]
+            sel = set()
+            for p in ids[u, :int(npg[u])].tolist():
+                sel.update(c0["slot_tok"][p, :c0["list_cnt"][p]].tolist())
+            rec.append(len(sel & top[u]) / k)
+        n = max(20, args.steps // 50)
+        t_f = timed(lambda: flush.zero_(), n)
+        t_s = timed(lambda: (flush.zero_(), ix.select_attn(ql, w.budget, out)), n)
+        ix.destroy()
+        res.append({"n_cand": mult * w.budget, "recall_at_k": round(float(np.mean(rec)), 4),
+                    "min_unit": round(float(np.min(rec)), 4),
+                    "layer_us": round((t_s - t_f) / n * 1e3, 2)})
+    return {"k": k, "units": U1, "curve": res,
+            "note": ("tokens of the selected pages against the exact top-k tokens of q_sel (fp64); "
+                     "one layer, one launch per n_cand, L2 flushed")}
+
+
 def insert_run(ice, synth, dev, flush, timed, args):
     """Generation with insertion (the Mistral-7B shape): prefill 8192 tokens, then
     one inserted token per KV head per step for 8192 steps from a drifting
@@ -630,6 +680,7 @@ def run_ice(args):
         line["insert"] = insert_run(ice, synth, dev, flush, timed, args)
         line["host_kv"] = host_kv_run(ice, w, keys, values, q, flush, timed, args, st)
         line["reuse"] = reuse_run(ice, synth, ix, w, centers, flush, timed, args)
+        line["recall"] = recall_run(ice, w, keys, values, q, flush, timed, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_units = [0, 85, 170, 255][: max(1, min(4, U))]
         ku = [keys.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]

@@ -255,6 +255,17 @@ int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap,
 int ice_debug_page(ice_index* ix, int32_t unit, int32_t page_id, void* host_k, void* host_v,
                    void* stream);
 
+/*
+ * ice_debug_set_flags - test hooks (0 = normal operation).
+ * ICE_DEBUG_STALL_ATTN: the fused call's page staging expects 16 bytes more
+ * than its copies deliver, so its bounded wait (200 ms of wall time) runs out
+ * twice; the call then skips the attention of that round, writes zeros and
+ * reports ICE_ERR_TIMEOUT through ice_get_error(). Nothing is left in flight
+ * and the context stays usable. Used to test the timeout path.
+ */
+enum { ICE_DEBUG_STALL_ATTN = 1 };
+int ice_debug_set_flags(ice_index* ix, int32_t flags);
+
 
 /*
  * ice_key_codes_noalloc - the key transform of ice_build (squared norms, the

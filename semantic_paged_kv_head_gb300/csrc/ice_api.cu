@@ -6,8 +6,17 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ice_internal.cuh"
 
+namespace {
+// NVTX range over one API call (visible in Nsight timelines; free otherwise).
+struct ApiRange {
+    explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+    ~ApiRange() { nvtxRangePop(); }
+};
+}  // namespace
 
 using namespace ice;
 
@@ -114,6 +123,7 @@ const char* ice_status_string(int s) {
 
 int ice_build(const ice_params* params, const void* keys, const void* values, int64_t n_tokens,
               void* stream, ice_index** out) {
+    ApiRange range_("ice_build");
     if (!out) return ICE_ERR_INVALID_ARG;
     *out = nullptr;
     int rc = check_params(params);
@@ -257,6 +267,7 @@ fail:
 }
 
 int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
+    ApiRange range_("ice_insert");
     if (!ix || !k || !v || !aligned16(k) || !aligned16(v)) return ICE_ERR_INVALID_ARG;
     if (ix->n_tok >= ix->v.max_tokens) return ICE_ERR_CAPACITY;
     cudaError_t e = launch_insert(ix->v, k, v, ix->n_tok, (cudaStream_t)stream);
@@ -296,11 +307,13 @@ static int select_common(ice_index* ix, const void* q, int32_t token_budget, int
 
 int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
                int32_t* n_pages, int32_t* stats, void* stream) {
+    ApiRange range_("ice_select");
     return select_common(ix, q, token_budget, page_ids, n_pages, stats, nullptr, stream);
 }
 
 int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
                     int32_t* n_pages, int32_t* stats, void* out, void* stream) {
+    ApiRange range_("ice_select_attn");
     if (!ix || !out) return ICE_ERR_INVALID_ARG;
     if (ix->p.kv_location == ICE_KV_HOST) {
         // the fused kernel stages pages with bulk tensor-memory copies; a host pool
@@ -316,6 +329,7 @@ int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t*
 int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, int32_t r,
                           int32_t* page_ids, int32_t* n_pages, int32_t* reselected, void* out,
                           void* stream) {
+    ApiRange range_("ice_select_attn_reuse");
     if (!ix || !out || r < 0) return ICE_ERR_INVALID_ARG;
     const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
     if (a != ICE_OK) return a;
@@ -364,6 +378,7 @@ int ice_reuse_reset(ice_index* ix, void* stream) {
 
 int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const int32_t* n_pages,
                     int32_t page_stride, void* out, void* stream) {
+    ApiRange range_("ice_sparse_attn");
     if (!ix || !q || !page_ids || !n_pages || !out || !aligned16(q) || !aligned16(out))
         return ICE_ERR_INVALID_ARG;
     if (page_stride < 1 || page_stride > 512) return ICE_ERR_INVALID_ARG;
@@ -387,6 +402,12 @@ void ice_destroy(ice_index* ix) {
     cudaDeviceSynchronize();
     free_all(ix);
     delete ix;
+}
+
+int ice_debug_set_flags(ice_index* ix, int32_t flags) {
+    if (!ix || (flags & ~ICE_DEBUG_STALL_ATTN)) return ICE_ERR_INVALID_ARG;
+    ix->v.debug = flags;
+    return ICE_OK;
 }
 
 int ice_get_info(const ice_index* ix, ice_info* info) {

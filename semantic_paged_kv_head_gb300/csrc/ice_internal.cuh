@@ -64,6 +64,7 @@ struct IndexView {
     void* page_k;
     void* page_v;
     int* status;
+    int debug;  // ICE_DEBUG_* flags (tests only), 0 in normal use
 
     __host__ __device__ long long ul(int u, int l) const { return (long long)u * L + l; }
     __host__ __device__ long long leaf_base(int u, int l) const { return ul(u, l) * C; }

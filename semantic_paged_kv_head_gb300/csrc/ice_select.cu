@@ -337,8 +337,11 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
         if (warp == 0) {
             if (lane == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                // ICE_DEBUG_STALL_ATTN: expect 16 bytes that no copy delivers, so the
+                // bounded wait below runs out (tests of the timeout path)
+                const unsigned extra = (v.debug & ICE_DEBUG_STALL_ATTN) ? 16u : 0u;
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                             "r"((unsigned)(2 * nrow * ROWB))
+                             "r"((unsigned)(2 * nrow * ROWB) + extra)
                              : "memory");
             }
             __syncwarp();
@@ -363,9 +366,12 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
             }
         }
         const bool ok = mbar_wait_bounded(bar, (unsigned)(round & 1));
-        if (!ok && tid == 0) {
-            set_status(v.status, ICE_ERR_TIMEOUT);
-            *s_fail = 1;
+        if (!ok) {
+            if (tid == 0) {
+                set_status(v.status, ICE_ERR_TIMEOUT);
+                *s_fail = 1;
+            }
+            mbar_wait_bounded(bar, (unsigned)(round & 1));  // copies possibly still in flight
         }
         if (ok) {
             for (int j = warp; j < nrow; j += kSelWarps) {  // warp-uniform

@@ -35,7 +35,8 @@ ICE_BF16 = 1
 # every symbol include/ice.h declares
 EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_select_attn", "ice_sparse_attn", "ice_get_error",
            "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page",
-           "ice_key_codes_noalloc", "ice_select_attn_reuse", "ice_reuse_reset"]
+           "ice_key_codes_noalloc", "ice_select_attn_reuse", "ice_reuse_reset",
+           "ice_debug_set_flags"]
 
 
 class ice_params(ctypes.Structure):
@@ -49,6 +50,7 @@ class ice_params(ctypes.Structure):
 
 
 KV_DEVICE, KV_HOST = 0, 1  # ice_params.kv_location
+DEBUG_STALL_ATTN = 1       # ice_debug_set_flags
 
 
 class ice_info(ctypes.Structure):
@@ -101,6 +103,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_select_attn_reuse.restype = ctypes.c_int
     lib.ice_reuse_reset.argtypes = [vp, vp]
     lib.ice_reuse_reset.restype = ctypes.c_int
+    lib.ice_debug_set_flags.argtypes = [vp, i32]
+    lib.ice_debug_set_flags.restype = ctypes.c_int
     return lib
 
 
@@ -227,6 +231,11 @@ class IceIndex:
                                           _dev_ptr(out, self.dtype, "out"), _stream(stream)),
                "ice_select_attn_reuse")
         return out, page_ids, n_pages
+
+    def debug_set_flags(self, flags: int):
+        """ice_debug_set_flags (tests only): DEBUG_STALL_ATTN forces the fused call's
+        bounded wait to run out."""
+        _check(_lib.ice_debug_set_flags(self._h, int(flags)), "ice_debug_set_flags")
 
     def reuse_reset(self, stream=None):
         _check(_lib.ice_reuse_reset(self._h, _stream(stream)), "ice_reuse_reset")
