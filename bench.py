@@ -363,7 +363,49 @@ def recall_run(ice, w, keys, values, q, flush, timed, args):
         res.append({"n_cand": mult * w.budget, "recall_at_k": round(float(np.mean(rec)), 4),
                     "min_unit": round(float(np.min(rec)), 4),
                     "layer_us": round((t_s - t_f) / n * 1e3, 2)})
-    return {"k": k, "units": U1, "curve": res,
+    # variants at n_cand = budget: Gaussian directions; per-query-head selection
+    # with a union over the group (up to G x budget/P pages attended)
+    ix = ice.IceIndex.build(kl, vl, page_size=w.page_size, n_q_heads=w.n_q_heads,
+                            n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed, dir_kind=1)
+    _, ids, npg = ix.select_attn(ql, w.budget, out)
+    torch.cuda.synchronize()
+    ix.check()
+    rec = []
+    for u in range(U1):
+        c0 = ix.dump(u)["comp"][0]
+        sel = set()
+        for p in ids[u, :int(npg[u])].tolist():
+            sel.update(c0["slot_tok"][p, :c0["list_cnt"][p]].tolist())
+        rec.append(len(sel & top[u]) / k)
+    ix.destroy()
+    gauss = {"recall_at_k": round(float(np.mean(rec)), 4), "n_cand": w.budget}
+    ix = ice.IceIndex.build(kl, vl, page_size=w.page_size, n_q_heads=w.n_q_heads,
+                            n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed)
+    uids, un, _, _ = ix.select_heads(ql, w.budget)
+    torch.cuda.synchronize()
+    rec, pages = [], []
+    for u in range(U1):
+        c0 = ix.dump(u)["comp"][0]
+        sel = set()
+        for p in uids[u, :int(un[u])].tolist():
+            sel.update(c0["slot_tok"][p, :c0["list_cnt"][p]].tolist())
+        rec.append(len(sel & top[u]) / k)
+        pages.append(int(un[u]))
+    n = max(20, args.steps // 50)
+    t_f = timed(lambda: flush.zero_(), n)
+
+    def heads_step():
+        flush.zero_()
+        a, b, _, _ = ix.select_heads(ql, w.budget)
+        ix.sparse_attn(ql, a, b, out)
+
+    t_s = timed(heads_step, n)
+    ix.check()
+    ix.destroy()
+    heads = {"recall_at_k": round(float(np.mean(rec)), 4), "pages_per_unit": round(float(np.mean(pages)), 1),
+             "layer_us": round((t_s - t_f) / n * 1e3, 2),
+             "note": "ice_select_heads + ice_sparse_attn over the union, one layer"}
+    return {"k": k, "units": U1, "curve": res, "gaussian_directions": gauss, "per_head_union": heads,
             "note": ("tokens of the selected pages against the exact top-k tokens of q_sel (fp64); "
                      "one layer, one launch per n_cand, L2 flushed")}
 

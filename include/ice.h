@@ -72,8 +72,13 @@ typedef struct ice_params {
                          /* ICE_KV_HOST: in pinned host memory mapped into the       */
                          /* GPU's address space, read by the kernels over the        */
                          /* CPU-GPU link (the pages' offloaded KV tier)              */
-    int32_t reserved;    /* must be 0                                               */
+    int32_t dir_kind;    /* projection directions: ICE_DIR_RADEMACHER (+-1/16 per   */
+                         /* component, one splitmix64 draw each) or ICE_DIR_GAUSSIAN */
+                         /* (z/16, z from the Box-Muller transform of two draws)     */
 } ice_params;
+
+/* Distribution of the random projection directions (ice_params.dir_kind). */
+enum { ICE_DIR_RADEMACHER = 0, ICE_DIR_GAUSSIAN = 1 };
 
 /* Page pool placement (ice_params.kv_location). With ICE_KV_HOST the index
  * (leaf tables, slot lists, token locations) stays in device memory and only
@@ -179,6 +184,21 @@ int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t*
 int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, int32_t r,
                           int32_t* page_ids, int32_t* n_pages, int32_t* reselected, void* out,
                           void* stream);
+
+/*
+ * ice_select_heads - per-query-head selection with a union over the group (a
+ * variant of Figure 2 step 2): every query head g of unit u selects pages with
+ * its own query as q_sel (the same search and ranking as ice_select, G = 1),
+ * and the unit's pages are the union of its heads' lists, head 0's pages first
+ * in their order, then each later head's pages not yet listed.
+ *
+ * head_page_ids: device int32 [units][G][n_sel]; head_n_pages: [units][G].
+ * page_ids: device int32 [units][G * n_sel] (the union, -1 padded); n_pages:
+ * [units]. Attend with ice_sparse_attn(..., page_stride = G * n_sel, ...).
+ * G * n_sel must be <= 512 (ICE_ERR_UNSUPPORTED otherwise).
+ */
+int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t* head_page_ids,
+                     int32_t* head_n_pages, int32_t* page_ids, int32_t* n_pages, void* stream);
 
 /* ice_reuse_reset - forget every unit's kept selection (the next
  * ice_select_attn_reuse selects everywhere). Asynchronous on `stream`. */

@@ -393,8 +393,31 @@ void orc_directions(uint64_t seed, int L, int m, int d, float* out) {
             }
 }
 
-void* orc_create(int d, int m, int L, int P, uint64_t seed) {
+// Gaussian directions (a variant of the search): each component is z / 16 with
+// z standard normal from the Box-Muller transform (Box & Muller, 1958) of two
+// splitmix64 draws x1, x2 taken in the order l, j, i:
+//   u1 = ((x1 >> 11) + 1) * 2^-53 in (0, 1],  u2 = (x2 >> 11) * 2^-53 in [0, 1),
+//   z = sqrt(-2 ln u1) * cos(2 pi u2), in double, rounded to float after / 16.
+// The variance of a component is that of the Rademacher +-1/16 directions.
+void orc_directions_gauss(uint64_t seed, int L, int m, int d, float* out) {
+    uint64_t st = seed;
+    const double two_pi = 2.0 * 3.14159265358979323846;
+    for (int l = 0; l < L; ++l)
+        for (int j = 0; j < m; ++j)
+            for (int i = 0; i <= d; ++i) {
+                const uint64_t x1 = splitmix64_next(st);
+                const uint64_t x2 = splitmix64_next(st);
+                const double u1 = (double)((x1 >> 11) + 1) * 0x1.0p-53;
+                const double u2 = (double)(x2 >> 11) * 0x1.0p-53;
+                const double z = std::sqrt(-2.0 * std::log(u1)) * std::cos(two_pi * u2);
+                out[((size_t)l * m + j) * (d + 1) + i] = (float)(z / 16.0);
+            }
+}
+
+// kind 0: Rademacher +-1/16 (the default reading); kind 1: Gaussian.
+void* orc_create_kind(int d, int m, int L, int P, uint64_t seed, int kind) {
     if (d <= 0 || d % 32 != 0 || m < 1 || m > 8 || L < 1 || P < 1) return nullptr;
+    if (kind != 0 && kind != 1) return nullptr;
     Index* ix = new Index();
     ix->d = d;
     ix->m = m;
@@ -402,10 +425,15 @@ void* orc_create(int d, int m, int L, int P, uint64_t seed) {
     ix->P = P;
     ix->seed = seed;
     ix->dirs.resize((size_t)L * m * (d + 1));
-    orc_directions(seed, L, m, d, ix->dirs.data());
+    if (kind == 0)
+        orc_directions(seed, L, m, d, ix->dirs.data());
+    else
+        orc_directions_gauss(seed, L, m, d, ix->dirs.data());
     ix->comp.resize(L);
     return ix;
 }
+
+void* orc_create(int d, int m, int L, int P, uint64_t seed) { return orc_create_kind(d, m, L, P, seed, 0); }
 
 void orc_destroy(void* h) { delete (Index*)h; }
 

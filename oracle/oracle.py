@@ -63,6 +63,8 @@ def _load():
         "orc_morton": (u64, [I32P, i32]),
         "orc_directions": (None, [u64, i32, i32, i32, F32P]),
         "orc_create": (vp, [i32, i32, i32, i32, u64]),
+        "orc_create_kind": (vp, [i32, i32, i32, i32, u64, i32]),
+        "orc_directions_gauss": (None, [u64, i32, i32, i32, F32P]),
         "orc_destroy": (None, [vp]),
         "orc_build": (i32, [vp, F32P, F32P, i32, i32]),
         "orc_insert": (i32, [vp, F32P, F32P]),
@@ -132,9 +134,13 @@ def morton(codes) -> int:
     return int(_load().orc_morton(c, c.size))
 
 
-def directions(seed: int, L: int, m: int, d: int) -> np.ndarray:
+def directions(seed: int, L: int, m: int, d: int, kind: int = 0) -> np.ndarray:
+    """Projection directions [L, m, d+1]: kind 0 Rademacher +-1/16, kind 1 Gaussian."""
     out = np.zeros((L, m, d + 1), dtype=np.float32)
-    _load().orc_directions(seed, L, m, d, out.reshape(-1))
+    if kind == 0:
+        _load().orc_directions(seed, L, m, d, out.reshape(-1))
+    else:
+        _load().orc_directions_gauss(seed, L, m, d, out.reshape(-1))
     return out
 
 
@@ -150,10 +156,10 @@ def dense_attn(q, K, V) -> np.ndarray:
 class OracleIndex:
     """The index of one unit, built by the oracle."""
 
-    def __init__(self, d: int, m: int, L: int, page_size: int, seed: int):
+    def __init__(self, d: int, m: int, L: int, page_size: int, seed: int, dir_kind: int = 0):
         self._lib = _load()
         self.d, self.m, self.L, self.P = d, m, L, page_size
-        self._h = self._lib.orc_create(d, m, L, page_size, seed)
+        self._h = self._lib.orc_create_kind(d, m, L, page_size, seed, dir_kind)
         if not self._h:
             raise ValueError("invalid oracle parameters")
 
@@ -320,3 +326,18 @@ class ReuseOracle:
             self.budget = budget
             self.age = 0
         return self.ids, self.npg, not keep, self.ix.attn(q, self.ids, self.npg)
+
+
+def select_heads(index: OracleIndex, q, budget: int, n_cand: int | None = None):
+    """Per-query-head selection with a union over the group (a variant of the
+    selection, "IceCache" Figure 2 step 2): head g selects with its own query
+    as q_sel; the union lists head 0's pages in order, then every later head's
+    pages not listed yet. Returns (union ids, n, per-head [(ids, n)])."""
+    q = as_f32(q)
+    heads = [index.select(q[g:g + 1], budget, n_cand)[:2] for g in range(q.shape[0])]
+    union = []
+    for ids, n in heads:
+        for p in ids[:n].tolist():
+            if p not in union:
+                union.append(p)
+    return np.asarray(union, dtype=np.int32), len(union), heads

@@ -1,6 +1,7 @@
 // C ABI of libice.so: argument checks, memory ownership and launch order.
 // See include/ice.h for the contract of each call.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -61,6 +62,7 @@ int check_params(const ice_params* p) {
     if (p->n_cand < 0) return ICE_ERR_INVALID_ARG;
     if (p->dtype != ICE_F32 && p->dtype != ICE_BF16) return ICE_ERR_INVALID_ARG;
     if (p->kv_location != ICE_KV_DEVICE && p->kv_location != ICE_KV_HOST) return ICE_ERR_INVALID_ARG;
+    if (p->dir_kind != ICE_DIR_RADEMACHER && p->dir_kind != ICE_DIR_GAUSSIAN) return ICE_ERR_INVALID_ARG;
     if (p->max_tokens < 0 || p->max_tokens > (1LL << 30)) return ICE_ERR_INVALID_ARG;
     const long long units = (long long)p->batch * p->n_layers * p->n_kv_heads;
     if (units > (1LL << 24)) return ICE_ERR_INVALID_ARG;
@@ -152,14 +154,27 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
     v.dtype = params->dtype;
     v.max_tokens = std::max<long long>(1, params->max_tokens);
 
-    // directions, on the host from splitmix64(seed): sign bit -> -1/16, else +1/16
+    // directions, on the host from splitmix64(seed) in the order (composite,
+    // direction, component). Rademacher: sign bit -> -1/16, else +1/16.
+    // Gaussian: z / 16 with z = sqrt(-2 ln u1) cos(2 pi u2) (Box-Muller) of the
+    // next two draws, u1 = ((x1 >> 11) + 1) 2^-53, u2 = (x2 >> 11) 2^-53, in double.
     std::vector<float> dirs((size_t)L * kM * kDirStride, 0.0f);
     {
         uint64_t s = params->seed;
+        const double two_pi = 2.0 * 3.14159265358979323846;
         for (int l = 0; l < L; ++l)
             for (int j = 0; j < kM; ++j)
-                for (int i = 0; i <= kD; ++i)
-                    dirs[((size_t)l * kM + j) * kDirStride + i] = (sm64(s) >> 63) ? -0.0625f : 0.0625f;
+                for (int i = 0; i <= kD; ++i) {
+                    float& c = dirs[((size_t)l * kM + j) * kDirStride + i];
+                    if (params->dir_kind == ICE_DIR_GAUSSIAN) {
+                        const uint64_t x1 = sm64(s), x2 = sm64(s);
+                        const double u1 = (double)((x1 >> 11) + 1) * 0x1.0p-53;
+                        const double u2 = (double)(x2 >> 11) * 0x1.0p-53;
+                        c = (float)(std::sqrt(-2.0 * std::log(u1)) * std::cos(two_pi * u2) / 16.0);
+                    } else {
+                        c = (sm64(s) >> 63) ? -0.0625f : 0.0625f;
+                    }
+                }
     }
     cudaError_t e = cudaSuccess;
     float* d_dirs = nullptr;
@@ -366,6 +381,24 @@ int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, in
                         st) != cudaSuccess)
         return ICE_ERR_CUDA;
     return res;
+}
+
+int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t* head_page_ids,
+                     int32_t* head_n_pages, int32_t* page_ids, int32_t* n_pages, void* stream) {
+    ApiRange range_("ice_select_heads");
+    const int a = select_args(ix, q, token_budget, page_ids, n_pages, nullptr);
+    if (a != ICE_OK) return a;
+    if (!head_page_ids || !head_n_pages) return ICE_ERR_INVALID_ARG;
+    const int n_sel = token_budget / ix->p.page_size;
+    if (ix->G * n_sel > 512) return ICE_ERR_UNSUPPORTED;  // the attention's page-list bound
+    const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (launch_select_heads(ix->v, q, n_sel, n_cand, head_page_ids, head_n_pages, st) != cudaSuccess)
+        return ICE_ERR_CUDA;
+    if (launch_union(ix->U, ix->G, n_sel, head_page_ids, head_n_pages, page_ids, n_pages, st) !=
+        cudaSuccess)
+        return ICE_ERR_CUDA;
+    return ICE_OK;
 }
 
 int ice_reuse_reset(ice_index* ix, void* stream) {

@@ -288,6 +288,12 @@ cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, lo
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
                           int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
                           const int32_t* reselect, cudaStream_t s);
+// Per-query-head selection (block = unit x head) and the union of each unit's
+// per-head page lists in head-major first-occurrence order.
+cudaError_t launch_select_heads(const IndexView& v, const void* q, int n_sel, int n_cand,
+                                int32_t* page_ids, int32_t* n_pages, cudaStream_t s);
+cudaError_t launch_union(int U, int G, int n_sel, const int32_t* head_ids, const int32_t* head_n,
+                         int32_t* ids, int32_t* n, cudaStream_t s);
 // Reuse decision per unit (query codes against the codes of the unit's last
 // selection, and the reuse age); writes reselect[U] and updates codes/age.
 cudaError_t launch_reuse(const IndexView& v, const void* q, int r, unsigned char* codes, int* age,

@@ -168,6 +168,7 @@ extern "C" int ice_key_codes_noalloc(const ice_params* params, const void* keys,
     if (params->d != kD || params->n_proj != kM) return ICE_ERR_UNSUPPORTED;
     if (params->n_composite < 1 || params->n_composite > kMaxL) return ICE_ERR_INVALID_ARG;
     if (params->dtype != ICE_F32 && params->dtype != ICE_BF16) return ICE_ERR_INVALID_ARG;
+    if (params->dir_kind != ICE_DIR_RADEMACHER) return ICE_ERR_UNSUPPORTED;  // drawn on the device
     if (params->batch < 1 || params->n_layers < 1 || params->n_kv_heads < 1 || n_tokens < 1)
         return ICE_ERR_INVALID_ARG;
     if (((uintptr_t)keys & 15u) != 0) return ICE_ERR_INVALID_ARG;

@@ -443,7 +443,8 @@ template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
     int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
-    int32_t* __restrict__ stats, T* __restrict__ attn_out, const int32_t* __restrict__ reselect) {
+    int32_t* __restrict__ stats, T* __restrict__ attn_out, const int32_t* __restrict__ reselect,
+    int head_div) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
@@ -453,7 +454,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     __shared__ int s_wsum[kMaxL][kSelWarps];
     __shared__ __align__(8) unsigned long long s_bar;
 
-    const int u = blockIdx.x;
+    // head_div > 1: per-query-head selection, block = (unit, head), row = block
+    const int u = blockIdx.x / head_div, row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = v.L, P = v.P;
     const long long C = v.C;
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int N[kMaxL] = {0, 0};
     for (int l = 0; l < L; ++l) N[l] = v.n_leaf[v.ul(u, l)];
     float qh[G][4];
-    const T* qu = q + (long long)u * G * kD;
+    const T* qu = q + (long long)row * G * kD;
 #pragma unroll
     for (int h = 0; h < G; ++h) load4(qu + (long long)h * kD + 4 * lane, qh[h]);
     float wdir[4] = {0.f, 0.f, 0.f, 0.f};
@@ -978,7 +980,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     __syncthreads();
     const int npg = s_npg;  // distinct pages among the candidates
     const int taken = min(n_sel, npg);
-    int32_t* out = page_ids + (long long)u * n_sel;
+    int32_t* out = page_ids + (long long)row * n_sel;
 
     // ---- 6. the n_sel smallest page keys in order ------------------------------------------
     // compact the occupied hash slots into (key, page) pairs
@@ -1066,17 +1068,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         }
     }
     __syncthreads();
-    if (tid == 0) n_pages_out[u] = taken;
+    if (tid == 0) n_pages_out[row] = taken;
     if (stats && warp == 0) {
         int tok_sel = 0;
         for (int r = lane; r < taken; r += 32) tok_sel += v.list_cnt[v.leaf_base(u, 0) + s_sel[r]];
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
         if (lane == 0) {
-            stats[4 * u + 0] = Ntot;
-            stats[4 * u + 1] = ncand;
-            stats[4 * u + 2] = tok_sel;
-            stats[4 * u + 3] = s_nraw;
+            stats[4 * row + 0] = Ntot;
+            stats[4 * row + 1] = ncand;
+            stats[4 * row + 2] = tok_sel;
+            stats[4 * row + 3] = s_nraw;
         }
     }
     if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
@@ -1114,11 +1116,11 @@ static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel,
     if (fused)
         select_kernel<T, G, true><<<v.U, kSelThreads, bytes, s>>>(
             v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, (T*)out,
-            reselect);
+            reselect, 1);
     else
         select_kernel<T, G, false><<<v.U, kSelThreads, bytes, s>>>(
             v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, nullptr,
-            reselect);
+            reselect, 1);
     return cudaGetLastError();
 }
 
@@ -1142,6 +1144,24 @@ cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_ca
         return launch_select_dt<__nv_bfloat16>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out,
                                                reselect, s);
     return launch_select_dt<float>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
+}
+
+// Per-query-head selection: one block per (unit, query head) selects with that
+// head's query alone (q_sel = q_h), through the single-head instantiation.
+cudaError_t launch_select_heads(const IndexView& v, const void* q, int n_sel, int n_cand,
+                                int32_t* page_ids, int32_t* n_pages, cudaStream_t s) {
+    int sort_cap, hcap;
+    select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
+    const int bytes = select_smem_bytes(v.C, v.L, v.P, n_cand, n_sel, 1, false);
+    if (v.dtype == ICE_BF16)
+        select_kernel<__nv_bfloat16, 1, false><<<v.U * v.G, kSelThreads, bytes, s>>>(
+            v, (const __nv_bfloat16*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages,
+            nullptr, nullptr, nullptr, v.G);
+    else
+        select_kernel<float, 1, false><<<v.U * v.G, kSelThreads, bytes, s>>>(
+            v, (const float*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, nullptr,
+            nullptr, nullptr, v.G);
+    return cudaGetLastError();
 }
 
 // Raise the dynamic shared memory limit of the select kernels once per device.

@@ -36,7 +36,7 @@ ICE_BF16 = 1
 EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_select_attn", "ice_sparse_attn", "ice_get_error",
            "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page",
            "ice_key_codes_noalloc", "ice_select_attn_reuse", "ice_reuse_reset",
-           "ice_debug_set_flags"]
+           "ice_debug_set_flags", "ice_select_heads"]
 
 
 class ice_params(ctypes.Structure):
@@ -46,9 +46,10 @@ class ice_params(ctypes.Structure):
                 ("n_proj", ctypes.c_int32), ("n_composite", ctypes.c_int32),
                 ("n_cand", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("max_tokens", ctypes.c_int64), ("seed", ctypes.c_uint64),
-                ("kv_location", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("kv_location", ctypes.c_int32), ("dir_kind", ctypes.c_int32)]
 
 
+DIR_RADEMACHER, DIR_GAUSSIAN = 0, 1  # ice_params.dir_kind
 KV_DEVICE, KV_HOST = 0, 1  # ice_params.kv_location
 DEBUG_STALL_ATTN = 1       # ice_debug_set_flags
 
@@ -103,6 +104,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_select_attn_reuse.restype = ctypes.c_int
     lib.ice_reuse_reset.argtypes = [vp, vp]
     lib.ice_reuse_reset.restype = ctypes.c_int
+    lib.ice_select_heads.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.ice_select_heads.restype = ctypes.c_int
     lib.ice_debug_set_flags.argtypes = [vp, i32]
     lib.ice_debug_set_flags.restype = ctypes.c_int
     return lib
@@ -155,7 +158,7 @@ class IceIndex:
     @classmethod
     def build(cls, keys: torch.Tensor, values: torch.Tensor, *, page_size: int, n_q_heads: int,
               n_composite: int = 2, n_proj: int = 8, n_cand: int = 0, max_tokens: int | None = None,
-              seed: int = 0, kv_host: bool = False, stream=None) -> "IceIndex":
+              seed: int = 0, kv_host: bool = False, dir_kind: int = 0, stream=None) -> "IceIndex":
         """ice_build over keys/values shaped [batch, layers, kv_heads, n, d].
 
         kv_host places the page pool in pinned host memory (ICE_KV_HOST)."""
@@ -165,7 +168,7 @@ class IceIndex:
         p = ice_params(d=d, n_kv_heads=H, n_q_heads=n_q_heads, n_layers=Ly, batch=B,
                        page_size=page_size, n_proj=n_proj, n_composite=n_composite, n_cand=n_cand,
                        dtype=_code(keys.dtype), max_tokens=n if max_tokens is None else max_tokens,
-                       seed=seed, kv_location=KV_HOST if kv_host else KV_DEVICE, reserved=0)
+                       seed=seed, kv_location=KV_HOST if kv_host else KV_DEVICE, dir_kind=dir_kind)
         h = ctypes.c_void_p()
         kp = _dev_ptr(keys, values.dtype, "keys") if n else 0
         vp = _dev_ptr(values, keys.dtype, "values") if n else 0
@@ -236,6 +239,21 @@ class IceIndex:
         """ice_debug_set_flags (tests only): DEBUG_STALL_ATTN forces the fused call's
         bounded wait to run out."""
         _check(_lib.ice_debug_set_flags(self._h, int(flags)), "ice_debug_set_flags")
+
+    def select_heads(self, q: torch.Tensor, token_budget: int, stream=None):
+        """ice_select_heads; returns (page_ids [units, G*n_sel] union, n_pages [units],
+        head_page_ids [units, G, n_sel], head_n_pages [units, G])."""
+        U, G = self.n_units, self.params.n_q_heads // self.params.n_kv_heads
+        n_sel = token_budget // self.params.page_size
+        dev = q.device
+        hid = torch.empty((U, G, n_sel), dtype=torch.int32, device=dev)
+        hn = torch.empty((U, G), dtype=torch.int32, device=dev)
+        ids = torch.empty((U, G * n_sel), dtype=torch.int32, device=dev)
+        n = torch.empty((U,), dtype=torch.int32, device=dev)
+        _check(_lib.ice_select_heads(self._h, _dev_ptr(q, self.dtype, "q"), int(token_budget),
+                                     hid.data_ptr(), hn.data_ptr(), ids.data_ptr(), n.data_ptr(),
+                                     _stream(stream)), "ice_select_heads")
+        return ids, n, hid, hn
 
     def reuse_reset(self, stream=None):
         _check(_lib.ice_reuse_reset(self._h, _stream(stream)), "ice_reuse_reset")

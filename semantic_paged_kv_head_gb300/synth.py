@@ -56,6 +56,7 @@ class Workload:
     n_proj: int = 8
     n_composite: int = 2
     seed: int = 0
+    dir_kind: int = 0  # projection directions of the index: 0 Rademacher, 1 Gaussian
     # dynamic-insert workloads
     n_insert: int = 0
     drift: float = 0.5

@@ -20,7 +20,7 @@ def unit_slices(w, u):
 def oracle_for_unit(w, keys, values, u, forced_e=None):
     from oracle.oracle import OracleIndex
     b, ly, h = unit_slices(w, u)
-    ix = OracleIndex(w.d, w.n_proj, w.n_composite, w.page_size, w.seed)
+    ix = OracleIndex(w.d, w.n_proj, w.n_composite, w.page_size, w.seed, w.dir_kind)
     ix.build(keys[b, ly, h].cpu(), values[b, ly, h].cpu(), forced_e=forced_e)
     return ix
 

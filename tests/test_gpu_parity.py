@@ -33,7 +33,8 @@ def _synth():
 def _run(ice, w, keys, values, q, max_tokens=None, kv_host=False):
     gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
                              n_q_heads=w.n_q_heads, n_composite=w.n_composite, n_proj=w.n_proj,
-                             seed=w.seed, max_tokens=max_tokens, kv_host=kv_host)
+                             seed=w.seed, max_tokens=max_tokens, kv_host=kv_host,
+                             dir_kind=w.dir_kind)
     qd = q.cuda().contiguous()
     stats = torch.zeros((gix.n_units, 4), dtype=torch.int32, device="cuda")
     ids, npg = gix.select(qd, w.budget, stats=stats)
@@ -167,6 +168,49 @@ def test_insert_matches_oracle(ice):
                 compare_index(gix.dump(u), orcs[u], f"step {s} unit {u}")
                 check_select_attn(w, orcs[u], q_of_unit(w, q, u), ids[u], npg[u],
                                   out.view(-1, w.group, w.d)[u], None, f"step {s} unit {u}")
+
+
+@pytest.mark.parametrize("G, dtype", [(4, torch.bfloat16), (2, torch.float32)])
+def test_select_heads_union(ice, G, dtype):
+    """Per-query-head selection with a union over the group: per-head lists and
+    the union bit-exact against the oracle, attention over the union within
+    tolerance."""
+    from oracle import oracle as O
+    synth = _synth()
+    w = synth.scaled(synth.WORKLOADS["llama8b_36k"], n_layers=2, n_kv_heads=2, group=G,
+                     n_tokens=2200, dtype=dtype, n_centers=24, seed=43)
+    keys, values, centers = synth.make_kv(w)
+    q = synth.make_queries(w, centers)
+    gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                             n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed)
+    qd = q.cuda()
+    ids, n, hid, hn = gix.select_heads(qd, w.budget)
+    out = gix.sparse_attn(qd, ids, n)
+    torch.cuda.synchronize()
+    assert gix.get_error() == 0
+    for u in range(w.n_units):
+        orc = oracle_for_unit(w, keys, values, u)
+        qu = q_of_unit(w, q, u)
+        uo, no, heads = O.select_heads(orc, qu, w.budget)
+        for g, (hi, hm) in enumerate(heads):
+            assert int(hn[u, g]) == hm, (u, g)
+            assert np.array_equal(hid[u, g, :hm].cpu().numpy(), hi[:hm]), (u, g)
+        assert int(n[u]) == no
+        assert np.array_equal(ids[u, :no].cpu().numpy(), uo)
+        assert (ids[u, no:] == -1).all()
+        ref = orc.attn(qu, uo, no)
+        got = out.view(-1, w.group, w.d)[u].float().cpu().numpy()
+        assert np.max(np.abs(got - ref)) <= (2e-2 if dtype == torch.bfloat16 else 1e-5)
+
+
+@pytest.mark.parametrize("L", [1, 2])
+def test_gaussian_directions(ice, L):
+    """The Gaussian-direction variant of the index: same build tables, pages and
+    attention as the oracle with the same directions."""
+    synth = _synth()
+    w = synth.scaled(synth.WORKLOADS["llama8b_36k"], n_layers=2, n_kv_heads=2, n_tokens=2500,
+                     n_composite=L, n_centers=32, seed=41, dir_kind=1)
+    _full_check(ice, w)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])

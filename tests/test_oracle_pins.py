@@ -449,3 +449,25 @@ def test_insert_split_keeps_old_id_for_left_child(oracle_mod):
                 old = [i for i in range(len(before["t"])) if before["id"][i] == after["id"][left]][0]
                 assert before["cnt"][old] == 8
                 assert after["cnt"][left] + after["cnt"][new] == 9
+
+
+def test_gaussian_directions_follow_box_muller():
+    """Gaussian directions: component (l, j, i) is z / 16 with z the Box-Muller
+    normal of the next two splitmix64 draws (recomputed here with Python's math
+    module from the generator's stream), and their spread matches the
+    Rademacher +-1/16 directions."""
+    import math
+    from oracle import oracle as O
+    seed, L, m, d = 99, 2, 8, 128
+    g = O.directions(seed, L, m, d, kind=1)
+    draws = O.splitmix64_stream(seed, 2 * 12)
+    for c in range(12):
+        x1, x2 = draws[2 * c], draws[2 * c + 1]
+        u1 = ((x1 >> 11) + 1) * 2.0 ** -53
+        u2 = (x2 >> 11) * 2.0 ** -53
+        z = math.sqrt(-2.0 * math.log(u1)) * math.cos(2.0 * math.pi * u2)
+        assert g.reshape(-1)[c] == np.float32(z / 16.0), c
+    flat = g.reshape(-1).astype(np.float64)
+    assert abs(flat.mean()) < 0.01 and abs(flat.std() - 1 / 16) < 0.005
+    r = O.directions(seed, L, m, d, kind=0)
+    assert set(np.unique(r).tolist()) == {-0.0625, 0.0625}

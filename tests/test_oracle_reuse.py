@@ -81,3 +81,21 @@ def test_reused_pages_see_inserted_tokens(unit):
     assert np.allclose(out, ix.attn(q, ids, npg))
     c_before, _ = ix.query(q)
     assert np.array_equal(c_before, ro.codes)
+
+
+def test_select_heads_union(unit):
+    """Per-head selection: one head equals the plain selection; identical heads
+    give one list; the union holds every head's pages once, head 0's first."""
+    K, V, q = unit
+    ix = _index(K, V)
+    ids1, n1, _ = ix.select(q[:1], 128)
+    u, n, heads = O.select_heads(ix, q[:1], 128)
+    assert n == n1 and np.array_equal(u, ids1[:n1])
+    same = np.repeat(q[:1], 4, axis=0)
+    u, n, heads = O.select_heads(ix, same, 128)
+    assert n == n1 and np.array_equal(u, ids1[:n1])
+    u, n, heads = O.select_heads(ix, q, 128)
+    assert len(set(u.tolist())) == n
+    assert np.array_equal(u[:heads[0][1]], heads[0][0][:heads[0][1]])
+    for ids, m in heads:
+        assert set(ids[:m].tolist()) <= set(u.tolist())
