@@ -426,9 +426,10 @@ def insert_run(ice, synth, dev, flush, timed, args):
     K = torch.stack(ks)
     V = torch.stack(vs)
     del ks, vs
+    n_graph = 512  # decode steps timed eagerly and as CUDA-graph replays after the inserts
     ix = ice.IceIndex.build(keys, values, page_size=w.page_size, n_q_heads=w.n_q_heads,
                             n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed,
-                            max_tokens=w.n_tokens + w.n_insert)
+                            max_tokens=w.n_tokens + w.n_insert + 2 * n_graph + 8)
     q0 = synth.make_queries(w, centers, step=0, drift_deltas=deltas)
     q1 = synth.make_queries(w, centers, step=w.n_insert, drift_deltas=deltas)
     out = torch.empty_like(q0)
@@ -456,6 +457,17 @@ def insert_run(ice, synth, dev, flush, timed, args):
     ix.check()
     leaves1 = [ix.dump(u)["n_leaf"] for u in range(U)]
     n_fin = w.n_tokens + w.n_insert
+    # whole decode steps (insert + select + attention): eager calls against the
+    # replay of one step captured in a CUDA graph
+    ids = torch.empty((U, w.budget // w.page_size), dtype=torch.int32, device=dev)
+    npg = torch.empty((U,), dtype=torch.int32, device=dev)
+    ks, vs = K[0].clone(), V[0].clone()
+    t_eager = timed(lambda: ix.decode_step(ks, vs, q1, w.budget, ids, npg, out), n_graph)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ix.decode_step(ks, vs, q1, w.budget, ids, npg, out)
+    t_graph = timed(g.replay, n_graph)
+    ix.check()
     pages0 = sum(x[0] for x in leaves0)
     pages1 = sum(x[0] for x in leaves1)
     ix.destroy()
@@ -469,7 +481,12 @@ def insert_run(ice, synth, dev, flush, timed, args):
             "occupancy_before": round(w.n_tokens * U / (pages0 * w.page_size), 4),
             "occupancy_after": round(n_fin * U / (pages1 * w.page_size), 4),
             "leaves_per_unit_after": [round(sum(x[l] for x in leaves1) / U, 1)
-                                      for l in range(w.n_composite)]}
+                                      for l in range(w.n_composite)],
+            "decode_step_us": {"eager": round(t_eager / n_graph * 1e3, 3),
+                               "cuda_graph": round(t_graph / n_graph * 1e3, 3),
+                               "note": ("ice_decode_step (insert + fused select/attention, all units) "
+                                        "back to back, no L2 flush; eager calls vs replays of one "
+                                        "captured step")}}
 
 
 def _oracle_worker(a):

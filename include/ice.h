@@ -200,6 +200,20 @@ int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, in
 int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t* head_page_ids,
                      int32_t* head_n_pages, int32_t* page_ids, int32_t* n_pages, void* stream);
 
+/*
+ * ice_decode_step - one decode step of every unit: ice_insert of the new
+ * token's k, v, then ice_select_attn for the query q (the new token is a
+ * candidate like any other). Two kernel launches on `stream`, no host
+ * synchronisation and no allocation, so a sequence of steps can be captured
+ * once in a CUDA graph and replayed: the insert takes the token index from a
+ * per-unit count kept on the device, which every replay advances (a unit at
+ * max_tokens reports ICE_ERR_CAPACITY through ice_get_error and is left
+ * unchanged). Arguments as in ice_insert and ice_select_attn.
+ */
+int ice_decode_step(ice_index* ix, const void* k, const void* v, const void* q,
+                    int32_t token_budget, int32_t* page_ids, int32_t* n_pages, void* out,
+                    void* stream);
+
 /* ice_reuse_reset - forget every unit's kept selection (the next
  * ice_select_attn_reuse selects everywhere). Asynchronous on `stream`. */
 int ice_reuse_reset(ice_index* ix, void* stream);

@@ -180,7 +180,13 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
     float* d_dirs = nullptr;
     int* d_status = nullptr;
     int* d_e = nullptr;
+    int* d_ntok = nullptr;
+    const std::vector<int> ntok0((size_t)U, (int)n);
     if ((e = dev_alloc(ix, &d_dirs, dirs.size())) != cudaSuccess) goto fail;
+    if ((e = dev_alloc(ix, &d_ntok, (size_t)U)) != cudaSuccess) goto fail;
+    if ((e = cudaMemcpyAsync(d_ntok, ntok0.data(), sizeof(int) * U, cudaMemcpyHostToDevice, st)) !=
+        cudaSuccess)
+        goto fail;
     if ((e = dev_alloc(ix, &d_status, 1)) != cudaSuccess) goto fail;
     if ((e = dev_alloc(ix, &d_e, (size_t)U)) != cudaSuccess) goto fail;
     if ((e = cudaMemcpyAsync(d_dirs, dirs.data(), dirs.size() * sizeof(float),
@@ -191,6 +197,7 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
     v.dirs = d_dirs;
     v.status = d_status;
     v.e_unit = d_e;
+    v.n_tok = d_ntok;
     {
         BuildScratch s;
         std::vector<int> nleaf((size_t)L * U, 0);
@@ -255,7 +262,7 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         }
         v.page_k = pk;
         v.page_v = pv;
-        if (select_prepare() != cudaSuccess) {
+        if (select_prepare() != cudaSuccess || insert_prepare(P, params->dtype) != cudaSuccess) {
             scratch_free(s, st);
             cudaGetLastError();
             free_all(ix);
@@ -285,7 +292,7 @@ int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
     ApiRange range_("ice_insert");
     if (!ix || !k || !v || !aligned16(k) || !aligned16(v)) return ICE_ERR_INVALID_ARG;
     if (ix->n_tok >= ix->v.max_tokens) return ICE_ERR_CAPACITY;
-    cudaError_t e = launch_insert(ix->v, k, v, ix->n_tok, (cudaStream_t)stream);
+    cudaError_t e = launch_insert(ix->v, k, v, (cudaStream_t)stream);
     if (e != cudaSuccess) return ICE_ERR_CUDA;
     ix->n_tok += 1;
     return ICE_OK;
@@ -383,6 +390,18 @@ int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, in
     return res;
 }
 
+int ice_decode_step(ice_index* ix, const void* k, const void* v, const void* q,
+                    int32_t token_budget, int32_t* page_ids, int32_t* n_pages, void* out,
+                    void* stream) {
+    ApiRange range_("ice_decode_step");
+    if (!ix || !out) return ICE_ERR_INVALID_ARG;
+    const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
+    if (a != ICE_OK) return a;
+    const int r = ice_insert(ix, k, v, stream);
+    if (r != ICE_OK) return r;
+    return ice_select_attn(ix, q, token_budget, page_ids, n_pages, nullptr, out, stream);
+}
+
 int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t* head_page_ids,
                      int32_t* head_n_pages, int32_t* page_ids, int32_t* n_pages, void* stream) {
     ApiRange range_("ice_select_heads");
@@ -446,7 +465,10 @@ int ice_debug_set_flags(ice_index* ix, int32_t flags) {
 int ice_get_info(const ice_index* ix, ice_info* info) {
     if (!ix || !info) return ICE_ERR_INVALID_ARG;
     info->n_units = ix->U;
-    info->n_tokens = ix->n_tok;
+    int nt = 0;  // the device count (inserts replayed from CUDA graphs included)
+    if (cudaMemcpy(&nt, ix->v.n_tok, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ICE_ERR_CUDA;
+    info->n_tokens = nt;
     info->max_tokens = ix->v.max_tokens;
     info->list_capacity = ix->C;
     info->pool_bytes = (int64_t)ix->bytes;
@@ -474,7 +496,10 @@ int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap,
     hdr[0] = L;
     hdr[1] = P;
     hdr[2] = C;
-    hdr[3] = ix->n_tok;
+    int nt = 0;
+    bool okn = cudaMemcpy(&nt, v.n_tok + unit, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess;
+    if (!okn) return ICE_ERR_CUDA;
+    hdr[3] = nt;
     int e = 0, nl[kMaxL] = {0, 0}, ni[kMaxL] = {0, 0};
     bool ok = cudaMemcpy(&e, v.e_unit + unit, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess;
     ok = ok && cudaMemcpy(nl, v.n_leaf + (long long)unit * L, sizeof(int) * L,

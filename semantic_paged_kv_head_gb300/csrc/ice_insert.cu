@@ -54,7 +54,7 @@ __device__ void shift_right(LeafKey* key, uint4* rec, unsigned long long* lo, un
 
 template <typename T>
 __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const T* __restrict__ knew,
-                                                            const T* __restrict__ vnew, int tok) {
+                                                            const T* __restrict__ vnew) {
     constexpr int ROW = kD;  // elements per row
     extern __shared__ __align__(16) unsigned char smem[];
     T* rows_k = reinterpret_cast<T*>(smem);                      // [P+1][D]
@@ -71,6 +71,13 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
     const int P = v.P;
     const T* kin = knew + (long long)u * kD;
     const T* vin = vnew + (long long)u * kD;
+    // the new token's index is the unit's count, kept on the device (so that a
+    // captured CUDA graph of inserts advances it on every replay)
+    const int tok = v.n_tok[u];
+    if (tok < 0 || tok >= v.max_tokens) {  // block-uniform
+        if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
+        return;
+    }
 
     // ---- key of the new token: frozen scale, projections, codes (warp 0) ----------
     if (warp == 0) {
@@ -333,26 +340,30 @@ __global__ void __launch_bounds__(kInsThreads) insert_kernel(IndexView v, const 
             __syncthreads();
         }
     }
+    if (tid == 0) v.n_tok[u] = tok + 1;  // every thread read the count at the start
 }
 
-cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, long long tok,
-                          cudaStream_t s) {
+cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, cudaStream_t s) {
     const size_t es = v.dtype == ICE_BF16 ? 2 : 4;
     const size_t bytes = (size_t)2 * (v.P + 1) * kD * es;
-    if (v.dtype == ICE_BF16) {
-        cudaError_t e = cudaFuncSetAttribute(insert_kernel<__nv_bfloat16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        if (e != cudaSuccess) return e;
+    if (v.dtype == ICE_BF16)
         insert_kernel<__nv_bfloat16><<<v.U, kInsThreads, bytes, s>>>(
-            v, (const __nv_bfloat16*)k, (const __nv_bfloat16*)val, (int)tok);
-    } else {
-        cudaError_t e = cudaFuncSetAttribute(insert_kernel<float>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        if (e != cudaSuccess) return e;
-        insert_kernel<float><<<v.U, kInsThreads, bytes, s>>>(v, (const float*)k, (const float*)val,
-                                                            (int)tok);
-    }
+            v, (const __nv_bfloat16*)k, (const __nv_bfloat16*)val);
+    else
+        insert_kernel<float><<<v.U, kInsThreads, bytes, s>>>(v, (const float*)k, (const float*)val);
     return cudaGetLastError();
+}
+
+// Dynamic shared memory limit of the insert kernel (the staged rows of a
+// split), set once at build so that inserts can be captured in CUDA graphs.
+cudaError_t insert_prepare(int P, int dtype) {
+    const size_t es = dtype == ICE_BF16 ? 2 : 4;
+    const int bytes = (int)((size_t)2 * (P + 1) * kD * es);
+    if (dtype == ICE_BF16)
+        return cudaFuncSetAttribute(insert_kernel<__nv_bfloat16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return cudaFuncSetAttribute(insert_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                bytes);
 }
 
 }  // namespace ice

@@ -64,6 +64,7 @@ struct IndexView {
     void* page_k;
     void* page_v;
     int* status;
+    int* n_tok;  // [U] tokens in each unit (build + inserts), advanced by the insert kernel
     int debug;  // ICE_DEBUG_* flags (tests only), 0 in normal use
 
     __host__ __device__ long long ul(int u, int l) const { return (long long)u * L + l; }
@@ -280,8 +281,8 @@ int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, b
 cudaError_t select_prepare();
 
 // ---- launchers (implemented in the .cu files) --------------------------------------
-cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, long long tok,
-                          cudaStream_t s);
+cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, cudaStream_t s);
+cudaError_t insert_prepare(int P, int dtype);
 // out == nullptr: select only; otherwise select and attend over the selection.
 // reselect: nullable [U]; a unit whose flag is 0 keeps its pages (page_ids,
 // n_pages unchanged) and, in the fused call, attends over them

@@ -36,7 +36,7 @@ ICE_BF16 = 1
 EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_select_attn", "ice_sparse_attn", "ice_get_error",
            "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page",
            "ice_key_codes_noalloc", "ice_select_attn_reuse", "ice_reuse_reset",
-           "ice_debug_set_flags", "ice_select_heads"]
+           "ice_debug_set_flags", "ice_select_heads", "ice_decode_step"]
 
 
 class ice_params(ctypes.Structure):
@@ -104,6 +104,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_select_attn_reuse.restype = ctypes.c_int
     lib.ice_reuse_reset.argtypes = [vp, vp]
     lib.ice_reuse_reset.restype = ctypes.c_int
+    lib.ice_decode_step.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.ice_decode_step.restype = ctypes.c_int
     lib.ice_select_heads.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
     lib.ice_select_heads.restype = ctypes.c_int
     lib.ice_debug_set_flags.argtypes = [vp, i32]
@@ -239,6 +241,18 @@ class IceIndex:
         """ice_debug_set_flags (tests only): DEBUG_STALL_ATTN forces the fused call's
         bounded wait to run out."""
         _check(_lib.ice_debug_set_flags(self._h, int(flags)), "ice_debug_set_flags")
+
+    def decode_step(self, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, token_budget: int,
+                    page_ids: torch.Tensor, n_pages: torch.Tensor, out: torch.Tensor, stream=None):
+        """ice_decode_step: insert (k, v) into every unit, then select + attend for q.
+        Capturable in a CUDA graph (all buffers preallocated by the caller)."""
+        _check(_lib.ice_decode_step(self._h, _dev_ptr(k, self.dtype, "k"), _dev_ptr(v, self.dtype, "v"),
+                                    _dev_ptr(q, self.dtype, "q"), int(token_budget),
+                                    _dev_ptr(page_ids, torch.int32, "page_ids"),
+                                    _dev_ptr(n_pages, torch.int32, "n_pages"),
+                                    _dev_ptr(out, self.dtype, "out"), _stream(stream)),
+               "ice_decode_step")
+        return out
 
     def select_heads(self, q: torch.Tensor, token_budget: int, stream=None):
         """ice_select_heads; returns (page_ids [units, G*n_sel] union, n_pages [units],

@@ -1,0 +1,76 @@
+"""A decode step (insert + select + attention) captured once in a CUDA graph and
+replayed gives, step by step, the pages, outputs and final index of the same
+steps run eagerly; replays past the token capacity report it on the device."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ice():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from semantic_paged_kv_head_gb300 import build
+    build.build_lib()
+    from semantic_paged_kv_head_gb300 import ice as m
+    return m
+
+
+def _dump_equal(a, b):
+    assert a["n"] == b["n"] and a["n_leaf"] == b["n_leaf"] and a["next_id"] == b["next_id"]
+    for ca, cb in zip(a["comp"], b["comp"]):
+        for key in ("pm", "pt", "t", "lo", "id", "cnt", "list_cnt", "slot_tok", "slot_key"):
+            assert np.array_equal(ca[key], cb[key]), key
+    assert np.array_equal(a["tok_loc"], b["tok_loc"])
+
+
+def test_graph_replay_equals_eager(ice):
+    from semantic_paged_kv_head_gb300 import synth
+    w = synth.scaled(synth.WORKLOADS["mistral7b_gen8k"], n_kv_heads=3, n_tokens=600, n_insert=40,
+                     n_centers=12, seed=47)
+    keys, values, centers = synth.make_kv(w)
+    deltas = synth.make_drift(w, centers)
+    steps = []
+    for t in range(w.n_insert):
+        k, v = synth.make_insert_token(w, centers, deltas, t)
+        q = synth.make_queries(w, centers, step=t, drift_deltas=deltas)
+        steps.append((k.cuda(), v.cuda(), q.cuda()))
+    cap = w.n_tokens + w.n_insert
+
+    def index():
+        return ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                                  n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed,
+                                  max_tokens=cap)
+
+    U, n_sel = w.n_units, w.budget // w.page_size
+    eager, graphed = index(), index()
+    ids_e = torch.empty((U, n_sel), dtype=torch.int32, device="cuda")
+    npg_e = torch.empty((U,), dtype=torch.int32, device="cuda")
+    out_e = torch.empty_like(steps[0][2])
+    ks, vs, qs = (torch.empty_like(x) for x in steps[0])
+    ids_g, npg_g, out_g = torch.empty_like(ids_e), torch.empty_like(npg_e), torch.empty_like(out_e)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        graphed.decode_step(ks, vs, qs, w.budget, ids_g, npg_g, out_g)
+    for t, (k, v, q) in enumerate(steps):
+        eager.decode_step(k, v, q, w.budget, ids_e, npg_e, out_e)
+        ks.copy_(k)
+        vs.copy_(v)
+        qs.copy_(q)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(npg_g, npg_e) and torch.equal(ids_g, ids_e), t
+        assert torch.equal(out_g, out_e), t
+    assert eager.get_error() == 0 and graphed.get_error() == 0
+    for u in range(U):
+        _dump_equal(graphed.dump(u), eager.dump(u))
+    assert graphed.info().n_tokens == cap
+    # past the capacity: the device count stops, the index is unchanged, the status says so
+    before = [graphed.dump(u) for u in range(U)]
+    g.replay()
+    torch.cuda.synchronize()
+    assert graphed.get_error() == ice.ICE_ERR_CAPACITY
+    for u in range(U):
+        _dump_equal(graphed.dump(u), before[u])
