@@ -741,7 +741,7 @@ def run_ice(args):
         line["reuse"] = reuse_run(ice, synth, ix, w, centers, flush, timed, args)
         line["recall"] = recall_run(ice, w, keys, values, q, flush, timed, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample_units = [0, 85, 170, 255][: max(1, min(4, U))]
+        sample_units = sorted({0, U // 3, (2 * U) // 3, U - 1})
         ku = [keys.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]
         vu = [values.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]
         qu = [q.view(U, w.group, w.d)[u].cpu() for u in sample_units]

@@ -309,7 +309,7 @@ static int select_args(const ice_index* ix, const void* q, int32_t token_budget,
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
     if (n_cand > (1 << 16)) return ICE_ERR_UNSUPPORTED;
     if (select_smem_bytes(ix->C, ix->p.n_composite, P, n_cand, n_sel, ix->G, out != nullptr) >
-        200 * 1024)
+        kSelSmemMax)
         return ICE_ERR_UNSUPPORTED;
     return ICE_OK;
 }

@@ -284,6 +284,9 @@ cudaError_t select_prepare();
 cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, cudaStream_t s);
 cudaError_t insert_prepare(int P, int dtype);
 // out == nullptr: select only; otherwise select and attend over the selection.
+// Largest dynamic shared memory of a select block: the opt-in maximum per block
+// of the GPU (227 KB) less room for the kernel's static shared variables.
+constexpr int kSelSmemMax = 220 * 1024;
 // reselect: nullable [U]; a unit whose flag is 0 keeps its pages (page_ids,
 // n_pages unchanged) and, in the fused call, attends over them
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,

@@ -1166,7 +1166,7 @@ cudaError_t launch_select_heads(const IndexView& v, const void* q, int n_sel, in
 
 // Raise the dynamic shared memory limit of the select kernels once per device.
 cudaError_t select_prepare() {
-    const int lim = 200 * 1024;
+    const int lim = kSelSmemMax;
     cudaError_t e = cudaSuccess;
 #define ICE_SET_SMEM(T, G)                                                                        \
     if (e == cudaSuccess)                                                                         \

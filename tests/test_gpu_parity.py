@@ -320,7 +320,9 @@ def test_bad_page_ids_report_bounds(ice):
 
 
 @pytest.mark.parametrize("name,units", [("llama8b_36k", [0, 77, 130, 255]),
-                                        ("llama8b_batch16_32k", [0, 64, 127])])
+                                        ("llama8b_batch16_32k", [0, 64, 127]),
+                                        ("mistral7b_gen8k", [0, 7]),
+                                        ("qwen3_4b_250k", [0, 143, 287])])
 def test_full_size_sampled_units(ice, name, units):
     """Full-size workloads in the launch configuration the benchmark times;
     sampled units are compared with the oracle in full."""
