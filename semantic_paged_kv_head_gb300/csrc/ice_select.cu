@@ -50,7 +50,6 @@ constexpr int kHistRow = 257;  // words per sub-histogram row (256 priorities + 
 constexpr int kRing = 3;      // scan chunks of 64 leaves in flight per warp
 constexpr int kSlotB = 640;   // one chunk: 64 corners (8 B) + 64 (t | count << 7) (2 B)
 constexpr int kRingB = kSelWarps * kRing * kSlotB;
-constexpr int kTieCap = 256;  // leaves at pi* ordered by rank counting; more -> range scan
 constexpr int kTopK = 32;     // warp top-k width
 constexpr int kFusedSmem = 108 * 1024;  // fused blocks grow to this (two blocks per SM)
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // bounded barrier wait
@@ -65,7 +64,7 @@ struct SelSmem {
     int sel, toff;
     int keys, vals, hpage, hkey, top, ring;
     int free;
-    int prio, cnt, chosen, cmeta, coff, tie, tcnt, bm0, hist;
+    int prio, cnt, chosen, cmeta, coff, tieb, bm0, hist;
     int end;
 };
 
@@ -91,8 +90,7 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
     s.chosen = o; o = align16(o + L * n_cand * 4);
     s.cmeta = o; o = align16(o + L * n_cand * 4);
     s.coff = o; o = align16(o + L * (n_cand + 1) * 4);
-    s.tie = o; o = align16(o + L * kTieCap * 4);
-    s.tcnt = o; o = align16(o + L * kTieCap * 4);
+    s.tieb = o; o = align16(o + L * (int)((C + 31) / 32) * 4);
     s.bm0 = o; o = align16(o + (int)((C + 31) / 32) * 4);
     s.hist = o; o = align16(o + L * kSubH * kHistRow * 4);
     s.end = o > min_total ? o : min_total;
@@ -449,9 +447,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     __shared__ __align__(16) float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
-    __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL], s_ntie[kMaxL];
+    __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL];
     __shared__ int s_ncand, s_nraw, s_npg, s_ntok, s_fail, s_cmp;
-    __shared__ int s_wsum[kMaxL][kSelWarps];
     __shared__ __align__(8) unsigned long long s_bar;
 
     // head_div > 1: per-query-head selection, block = (unit, head), row = block
@@ -469,8 +466,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int* chosen = reinterpret_cast<int*>(smem + lay.chosen);          // [L][n_cand] leaf index
     unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);  // [L][n_cand] id|count
     int* coff = reinterpret_cast<int*>(smem + lay.coff);              // [L][n_cand + 1]
-    int* tie = reinterpret_cast<int*>(smem + lay.tie);                // [L][kTieCap]
-    int* tcnt = reinterpret_cast<int*>(smem + lay.tcnt);              // [L][kTieCap]
+    unsigned* tieb = reinterpret_cast<unsigned*>(smem + lay.tieb);    // [L][nwords] leaves at pi*
     unsigned* bm0 = reinterpret_cast<unsigned*>(smem + lay.bm0);
     unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.keys);
     int* sval = reinterpret_cast<int*>(smem + lay.vals);
@@ -574,10 +570,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     }
     for (int i = tid; i < L * kSubH * kHistRow; i += kSelThreads) hist[i] = 0;
     for (int i = tid; i < nwords; i += kSelThreads) bm0[i] = 0u;
+    for (int i = tid; i < L * nwords; i += kSelThreads) tieb[i] = 0u;
     if (tid < kMaxL) {
         s_nch[tid] = 0;
         s_tot[tid] = 0;
-        s_ntie[tid] = 0;
     }
     if (tid == 0) {
         s_ncand = 0;
@@ -683,7 +679,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     }
     __syncthreads();
 
-    // ---- 3b. leaves below pi* are taken (records requested now); leaves at pi* listed ---
+    // ---- 3b. leaves below pi* are taken; leaves at pi* are marked in a bitmap ------------
     // (the page table takes over the scan ring's memory)
     for (int i = tid; i < hcap; i += kSelThreads) {
         hpage[i] = -1;
@@ -694,7 +690,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         if (l >= L) break;
         const int ps = s_pstar[l];
         const unsigned* p32 = reinterpret_cast<const unsigned*>(prio + l * Cp);
-        const uint4* lrec = recs + v.leaf_base(u, l);
         const int nw = (N[l] + 3) >> 2;
         for (int w4 = tid; w4 < nw; w4 += kSelThreads) {
             const unsigned word = p32[w4];
@@ -705,115 +700,67 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 const int pr = (int)((word >> (8 * b)) & 0xFFu);
                 if (pr < ps) {
                     const int slot = atomicAdd(&s_nch[l], 1);
-                    if (slot < n_cand) {
-                        chosen[l * n_cand + slot] = i;
-                        cmeta[l * n_cand + slot] = __ldg(lrec + i).z;
-                    }
+                    if (slot < n_cand) chosen[l * n_cand + slot] = i;
                 } else if (pr == ps) {
-                    const int slot = atomicAdd(&s_ntie[l], 1);
-                    if (slot < kTieCap) tie[l * kTieCap + slot] = i;
+                    atomicOr(&tieb[l * nwords + (i >> 5)], 1u << (i & 31));
                 }
             }
         }
     }
     __syncthreads();
     // ---- 3c. leaves at pi*, in position order, while tokens taken before them < need ------
-    // Both composites at once: threads [256 l, 256 l + ntie_l) rank composite l's
-    // ties by counting, warp l walks them in order. A composite with more than
-    // kTieCap ties is handled afterwards by a range walk over its positions.
-    {
-        const int l = tid >> 8, t = tid & 255;  // kSelThreads = 2 * kTieCap
-        const int ntie = l < L ? s_ntie[l] : 0;
-        int* tl = tie + l * kTieCap;
-        int* tc = tcnt + l * kTieCap;
-        const bool act = l < L && ntie <= kTieCap && t < ntie;
-        int mine = 0, r = 0, mc = 0;
-        if (act) {
-            mine = tl[t];
-            mc = cnts[l * Cp + mine];
-            for (int j = 0; j < ntie; ++j) r += tl[j] < mine;
-        }
-        __syncthreads();
-        if (act) {
-            tl[r] = mine;
-            tc[r] = mc;
-        }
-        __syncthreads();
-        if (warp < L) {
-            const int lw = warp;
-            const int nt = s_ntie[lw];
-            if (nt > 0 && nt <= kTieCap) {
-                const int* tlw = tie + lw * kTieCap;
-                const int* tcw = tcnt + lw * kTieCap;
-                const uint4* lrec = recs + v.leaf_base(u, lw);
-                const int need = s_need[lw];
-                int run = 0;
-                for (int k0 = 0; k0 < nt && run < need; k0 += 32) {
-                    const int k = k0 + lane;
-                    const int li = k < nt ? tlw[k] : 0;
-                    const int c = k < nt ? tcw[k] : 0;
-                    int inc = c;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-                        if (lane >= o) inc += y;
-                    }
-                    const bool take = k < nt && run + inc - c < need;
-                    const unsigned tm = __ballot_sync(0xffffffffu, take);
-                    int base = 0;
-                    if (lane == 0 && tm) base = atomicAdd(&s_nch[lw], __popc(tm));
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    if (take) {
-                        const int slot = base + __popc(tm & ((1u << lane) - 1u));
-                        if (slot < n_cand) {
-                            chosen[lw * n_cand + slot] = li;
-                            cmeta[lw * n_cand + slot] = __ldg(lrec + li).z;
-                        }
-                    }
-                    run += __shfl_sync(0xffffffffu, inc, 31);
-                }
-            }
-        }
-    }
-    for (int l = 0; l < L; ++l) {
-        const int ntie = s_ntie[l];
-        if (ntie <= kTieCap) continue;  // block-uniform
-        // many leaves at pi*: each thread walks a contiguous range of positions
-        const uint4* lrec = recs + v.leaf_base(u, l);
-        const int per = (N[l] + kSelThreads - 1) / kSelThreads;
-        const int lo_i = min(N[l], tid * per), hi_i = min(N[l], lo_i + per);
-        const int ps = s_pstar[l], need = s_need[l];
-        int mine = 0;
-        for (int i = lo_i; i < hi_i; ++i)
-            if (prio[l * Cp + i] == ps) mine += cnts[l * Cp + i];
-        int incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) s_wsum[l][warp] = incl;
-        __syncthreads();
-        int run = incl - mine;
-        for (int w = 0; w < warp; ++w) run += s_wsum[l][w];
-        for (int i = lo_i; i < hi_i; ++i) {
-            if (prio[l * Cp + i] != ps) continue;
-            if (run < need) {
-                const int slot = atomicAdd(&s_nch[l], 1);
-                if (slot < n_cand) {
-                    chosen[l * n_cand + slot] = i;
-                    cmeta[l * n_cand + slot] = __ldg(lrec + i).z;
-                }
-            }
-            run += cnts[l * Cp + i];
-        }
-    }
-    __syncthreads();
-
-    // ---- 3d. slot offsets of the taken leaves (warp l), composite-0 page bitmap ------------
+    // Warp l walks composite l's tie bitmap 32 words (1024 leaves) at a time, in
+    // position order: each lane sums the tokens of its word's ties, a warp scan
+    // gives every lane the tokens taken before it, and the lane takes its ties
+    // while that running count is below the need. The same warp then computes the
+    // slot offsets of all taken leaves (3d), and warp 0 marks composite 0's taken
+    // pages, so one block barrier closes both steps.
     if (warp < L) {
         const int l = warp;
-        const int nch = min(s_nch[l], n_cand);
+        const int need = s_need[l];
+        const unsigned* tb = tieb + l * nwords;
+        const unsigned char* cl = cnts + l * Cp;
+        const uint4* lrec = recs + v.leaf_base(u, l);
+        const int nbelow = min(s_nch[l], n_cand);
+        int run = 0, ntaken = 0;  // tie tokens and tie leaves taken so far (warp-uniform)
+        for (int w0 = 0; w0 < nwords && run < need; w0 += 32) {
+            const int wi = w0 + lane;
+            const unsigned bits = wi < nwords ? tb[wi] : 0u;
+            int tot = 0;
+            for (unsigned b = bits; b; b &= b - 1u) tot += cl[wi * 32 + __ffs(b) - 1];
+            int inc = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            int acc = run + inc - tot, mine = 0;
+            unsigned take = 0u;
+            for (unsigned b = bits; b && acc < need; b &= b - 1u) {
+                const int bit = __ffs(b) - 1;
+                take |= 1u << bit;
+                acc += cl[wi * 32 + bit];
+                ++mine;
+            }
+            int tinc = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, tinc, o);
+                if (lane >= o) tinc += y;
+            }
+            int slot = nbelow + ntaken + tinc - mine;
+            for (unsigned b = take; b; b &= b - 1u, ++slot)
+                if (slot < n_cand) chosen[l * n_cand + slot] = wi * 32 + __ffs(b) - 1;
+            ntaken += __shfl_sync(0xffffffffu, tinc, 31);
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        __syncwarp();
+        // the records of all taken leaves, requested together (one memory latency)
+        for (int k = lane; k < min(nbelow + ntaken, n_cand); k += 32)
+            cmeta[l * n_cand + k] = __ldg(lrec + chosen[l * n_cand + k]).z;
+        __syncwarp();
+        // ---- 3d. slot offsets of the taken leaves ----------------------------------------
+        const int nch = min(nbelow + ntaken, n_cand);
         int carry = 0;
         for (int k0 = 0; k0 < nch; k0 += 32) {
             const int k = k0 + lane;
@@ -830,13 +777,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         if (lane == 0) {
             coff[l * (n_cand + 1) + nch] = carry;
             s_tot[l] = carry;
+            s_nch[l] = nbelow + ntaken;
         }
-    }
-    {
-        const int nch0 = min(s_nch[0], n_cand);
-        for (int k = tid; k < nch0; k += kSelThreads) {
-            const int id = (int)(cmeta[k] >> 8);
-            if (id < C) atomicOr(&bm0[id >> 5], 1u << (id & 31));
+        if (l == 0) {  // composite-0 pages already taken whole
+            for (int k = lane; k < nch; k += 32) {
+                const int id = (int)(cmeta[k] >> 8);
+                if (id < C) atomicOr(&bm0[id >> 5], 1u << (id & 31));
+            }
         }
     }
     __syncthreads();
