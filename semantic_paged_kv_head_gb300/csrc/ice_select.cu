@@ -837,43 +837,53 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     const int ncand = min(s_ncand, sort_cap);
 
     // ---- 5. exact rescoring, one candidate row per thread; per-page minimum key ------------
-    // Candidate rows are staged in the free region with cp.async: each thread
-    // requests the 16-byte chunks of one row, and all rows of a round are in
-    // flight at once. Chunk c of row r is stored at chunk position
-    // c ^ (r mod chunks-per-row), so the eight rows that one shared-memory
+    // Candidate rows are staged in the free region with cp.async, in chunks that
+    // alternate between two halves of it: the next chunk is in flight while the
+    // current one is scored. Consecutive lanes request consecutive 16-byte pieces
+    // of a row (coalesced); piece c of row r is stored at piece position
+    // c ^ (r mod pieces-per-row), so the eight rows that one shared-memory
     // wavefront serves fall in distinct banks. Each thread then evaluates the
-    // fixed-order dot of its row by itself: virtual lane l accumulates elements
-    // 4l..4l+3, and the pairwise tree first adds lanes l and l+16, so chunks c
-    // and c + chunks-per-row/2 (elements 64 apart) are taken together.
+    // fixed-order dot of one row by itself: virtual lane l accumulates elements
+    // 4l..4l+3, and the pairwise tree first adds lanes l and l+16, so pieces c
+    // and c + pieces-per-row/2 (elements 64 apart) are taken together.
     {
-        constexpr int EPC = 16 / (int)sizeof(T);  // elements per chunk
-        constexpr int CPR = kD / EPC;             // chunks per row
-        constexpr int VPC = EPC / 4;              // virtual lanes per chunk
+        constexpr int EPC = 16 / (int)sizeof(T);  // elements per piece
+        constexpr int CPR = kD / EPC;             // pieces per row
+        constexpr int VPC = EPC / 4;              // virtual lanes per piece
         constexpr int ROWB = kD * (int)sizeof(T);
         unsigned char* stg = smem + lay.free;
-        const int rows_cap = min((smem_total - lay.free) / ROWB, kSelThreads);
+        const int half = min((smem_total - lay.free) / (2 * ROWB), kSelThreads);  // rows per half
+        const int nchunk = (ncand + half - 1) / half;
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = hcap - 1;
-        for (int rb0 = 0; rb0 < ncand; rb0 += rows_cap) {  // block-uniform rounds
-            const int nr = min(rows_cap, ncand - rb0);
+        auto issue = [&](int ch) {  // chunk ch into half ch & 1; every thread commits a group
+            if (ch < nchunk) {
+                const int rb = ch * half, nr = min(half, ncand - rb);
+                unsigned char* buf = stg + (ch & 1) * half * ROWB;
+                for (int k = tid; k < nr * CPR; k += kSelThreads) {
+                    const int r = k / CPR, c = k % CPR;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                     smem_u32(buf + r * ROWB + 16 * (c ^ (r & (CPR - 1))))),
+                                 "l"(pk + (long long)sval[rb + r] * ROWB + 16 * c)
+                                 : "memory");
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        issue(0);
+        issue(1);
+        for (int ch = 0; ch < nchunk; ++ch) {  // block-uniform
+            const int rb0 = ch * half, nr = min(half, ncand - rb0);
+            const unsigned char* stgc = stg + (ch & 1) * half * ROWB;
+            asm volatile("cp.async.wait_group 1;" ::: "memory");  // chunk ch has landed
+            __syncthreads();
             const int r = tid;
             const bool ok = r < nr;
             const int sw = r & (CPR - 1);
-            if (ok) {
-                const char* src = pk + (long long)sval[rb0 + r] * ROWB;
-                const unsigned dst = smem_u32(stg + r * ROWB);
-#pragma unroll
-                for (int c = 0; c < CPR; ++c)
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * (c ^ sw)),
-                                 "l"(src + 16 * c)
-                                 : "memory");
-            }
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            __syncthreads();
             int pg = -1;
             unsigned long long key = ~0ull;
             if (ok) {
-                const unsigned char* row = stg + r * ROWB;
+                const unsigned char* row = stgc + r * ROWB;
                 float s16[16];
 #pragma unroll
                 for (int c = 0; c < CPR / 2; ++c) {
@@ -921,8 +931,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                     h = (h + 1) & (unsigned)hmask;
                 }
             }
-            __syncthreads();  // the round's rows are read before the next round lands
+            __syncthreads();  // the chunk's rows are read before the next chunk lands there
+            issue(ch + 2);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     __syncthreads();
     const int npg = s_npg;  // distinct pages among the candidates
