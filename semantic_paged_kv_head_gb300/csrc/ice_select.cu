@@ -841,18 +841,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     // alternate between two halves of it: the next chunk is in flight while the
     // current one is scored. Consecutive lanes request consecutive 16-byte pieces
     // of a row (coalesced); piece c of row r is stored at piece position
-    // c ^ (r mod pieces-per-row), so the eight rows that one shared-memory
-    // wavefront serves fall in distinct banks. Each thread then evaluates the
-    // fixed-order dot of one row by itself: virtual lane l accumulates elements
-    // 4l..4l+3, and the pairwise tree first adds lanes l and l+16, so pieces c
-    // and c + pieces-per-row/2 (elements 64 apart) are taken together.
+    // c ^ 2 (r mod pieces-per-row/2), so that the pieces the threads of one
+    // shared-memory wavefront read (four rows, two threads per row) fall in
+    // distinct banks. The fixed-order dot of a row is split over two threads:
+    // virtual lane l accumulates elements 4l..4l+3, and the pairwise tree adds
+    // lanes l and l+16 first, then l+8, l+4, l+2, l+1.
     {
         constexpr int EPC = 16 / (int)sizeof(T);  // elements per piece
         constexpr int CPR = kD / EPC;             // pieces per row
-        constexpr int VPC = EPC / 4;              // virtual lanes per piece
         constexpr int ROWB = kD * (int)sizeof(T);
         unsigned char* stg = smem + lay.free;
-        const int half = min((smem_total - lay.free) / (2 * ROWB), kSelThreads);  // rows per half
+        const int half = min((smem_total - lay.free) / (2 * ROWB), kSelThreads / 2);  // rows per half (two threads a row)
         const int nchunk = (ncand + half - 1) / half;
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = hcap - 1;
@@ -862,8 +861,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 unsigned char* buf = stg + (ch & 1) * half * ROWB;
                 for (int k = tid; k < nr * CPR; k += kSelThreads) {
                     const int r = k / CPR, c = k % CPR;
+                    const int pos = c ^ ((r & (CPR / 2 - 1)) << 1);
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                                     smem_u32(buf + r * ROWB + 16 * (c ^ (r & (CPR - 1))))),
+                                     smem_u32(buf + r * ROWB + 16 * pos)),
                                  "l"(pk + (long long)sval[rb + r] * ROWB + 16 * c)
                                  : "memory");
                 }
@@ -877,59 +877,79 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             const unsigned char* stgc = stg + (ch & 1) * half * ROWB;
             asm volatile("cp.async.wait_group 1;" ::: "memory");  // chunk ch has landed
             __syncthreads();
-            const int r = tid;
+            // two threads per row: thread t of the pair owns the virtual lanes l with
+            // bit 1 of l equal to t, so the tree's levels 16, 8 and 4 stay inside
+            // the thread and level 2 is one exchange with the partner
+            const int r = tid >> 1, t = tid & 1;
             const bool ok = r < nr;
-            const int sw = r & (CPR - 1);
+            const int sw = (r & (CPR / 2 - 1)) << 1;
             int pg = -1;
             unsigned long long key = ~0ull;
+            float s4[2] = {0.0f, 0.0f};
             if (ok) {
-                const unsigned char* row = stgc + r * ROWB;
-                float s16[16];
+                const unsigned char* rowp = stgc + r * ROWB;
+                float s16[8];  // s16 of the owned lanes l < 16, in increasing order
 #pragma unroll
-                for (int c = 0; c < CPR / 2; ++c) {
-                    float lo[EPC], hi[EPC];
-                    load_chunk<T>(row + 16 * (c ^ sw), lo);
-                    load_chunk<T>(row + 16 * ((c + CPR / 2) ^ sw), hi);
+                for (int j = 0; j < 8; ++j) {
+                    const int l = ((j >> 1) << 2) | (t << 1) | (j & 1);  // 4(j/2) + 2t + (j mod 2)
+                    const int e0 = 4 * l, e1 = 4 * (l + 16);
+                    const int c0 = e0 / EPC, c1 = e1 / EPC;  // pieces holding the two groups
+                    float x0[EPC], x1[EPC];
+                    load_chunk<T>(rowp + 16 * (c0 ^ sw), x0);
+                    load_chunk<T>(rowp + 16 * (c1 ^ sw), x1);
+                    const int o0 = e0 % EPC, o1 = e1 % EPC;
+                    float a = 0.0f, b = 0.0f;
 #pragma unroll
-                    for (int z = 0; z < VPC; ++z) {
-                        const int e0 = 4 * (c * VPC + z);
-                        float a = 0.0f, b = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            a = __fmaf_rn(s_qsel[e0 + i], lo[4 * z + i], a);
-                            b = __fmaf_rn(s_qsel[e0 + 64 + i], hi[4 * z + i], b);
-                        }
-                        s16[c * VPC + z] = __fadd_rn(a, b);
+                    for (int i = 0; i < 4; ++i) {
+                        a = __fmaf_rn(s_qsel[e0 + i], x0[o0 + i], a);
+                        b = __fmaf_rn(s_qsel[e1 + i], x1[o1 + i], b);
                     }
+                    s16[j] = __fadd_rn(a, b);
                 }
+                // level 8: l + 8 is owned entry j + 4; level 4: l + 4 is entry j + 2
 #pragma unroll
-                for (int o = 8; o >= 1; o >>= 1)
-#pragma unroll
-                    for (int l = 0; l < o; ++l) s16[l] = __fadd_rn(s16[l], s16[l + o]);
-                pg = sval[rb0 + r] / P;
-                key = ((unsigned long long)score_key_desc(s16[0]) << 32) | (unsigned)skey[rb0 + r];
+                for (int j = 0; j < 4; ++j) s16[j] = __fadd_rn(s16[j], s16[j + 4]);
+                s4[0] = __fadd_rn(s16[0], s16[2]);  // lane 2t
+                s4[1] = __fadd_rn(s16[1], s16[3]);  // lane 2t + 1
+            }
+            {
+                const float p0 = __shfl_xor_sync(0xffffffffu, s4[0], 1);
+                const float p1 = __shfl_xor_sync(0xffffffffu, s4[1], 1);
+                // level 2: lane 0 + lane 2, lane 1 + lane 3; level 1: their sum
+                const float a0 = t ? p0 : s4[0], a2 = t ? s4[0] : p0;
+                const float a1 = t ? p1 : s4[1], a3 = t ? s4[1] : p1;
+                const float sc = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
+                if (ok) {
+                    pg = sval[rb0 + r] / P;
+                    key = ((unsigned long long)score_key_desc(sc) << 32) | (unsigned)skey[rb0 + r];
+                }
             }
             // rows of one page are adjacent in the candidate list: a segmented
-            // minimum over runs of equal pages leaves each run's minimum in its
-            // last lane, which alone updates the table
+            // minimum over runs of equal pages (rows two lanes apart) leaves each
+            // run's minimum in its last row, which alone updates the table
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
+            for (int o = 2; o < 32; o <<= 1) {
                 const int opg = __shfl_up_sync(0xffffffffu, pg, o);
                 const unsigned long long okey = __shfl_up_sync(0xffffffffu, key, o);
                 if (lane >= o && opg == pg && okey < key) key = okey;
             }
-            const int next_pg = __shfl_down_sync(0xffffffffu, pg, 1);
-            if (ok && (lane == 31 || next_pg != pg)) {
+            const int next_pg = __shfl_down_sync(0xffffffffu, pg, 2);
+            bool fresh = false;
+            if (ok && t == 0 && (lane >= 30 || next_pg != pg)) {
                 unsigned h = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
                 for (int probe = 0; probe < hcap; ++probe) {
                     const int old = atomicCAS(&hpage[h], -1, pg);
                     if (old == -1 || old == pg) {
-                        if (old == -1) atomicAdd(&s_npg, 1);
+                        fresh = old == -1;
                         atomicMin(&hkey[h], key);
                         break;
                     }
                     h = (h + 1) & (unsigned)hmask;
                 }
+            }
+            {
+                const unsigned nf = __ballot_sync(0xffffffffu, fresh);
+                if (lane == 0 && nf) atomicAdd(&s_npg, __popc(nf));
             }
             __syncthreads();  // the chunk's rows are read before the next chunk lands there
             issue(ch + 2);
