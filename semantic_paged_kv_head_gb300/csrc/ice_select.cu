@@ -536,6 +536,30 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         if (64LL * k < C) ring_issue(k, sidx);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
+    // tables and counters that need nothing from memory, while the loads are in flight
+    if (tid < 97) {
+        __half2 w[4];
+        cell_widths(tid, w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s_width[tid * 4 + k] = w[k];
+    }
+    for (int i = tid; i < L * kSubH * kHistRow; i += kSelThreads) hist[i] = 0;
+    for (int i = tid; i < nwords; i += kSelThreads) bm0[i] = 0u;
+    for (int i = tid; i < L * nwords; i += kSelThreads) tieb[i] = 0u;
+    if (tid < kMaxL) {
+        s_nch[tid] = 0;
+        s_tot[tid] = 0;
+    }
+    if (tid == 0) {
+        s_ncand = 0;
+        s_nraw = 0;
+        s_npg = 0;
+        s_fail = 0;
+        if (FUSED) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+    }
     for (int l = 0; l < L; ++l) N[l] = N[l] < 0 ? 0 : (N[l] > C ? (int)C : N[l]);
     const int Ntot = N[0] + N[1];
 
@@ -560,29 +584,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         if (warp == 0) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) s_qsel[4 * lane + k] = qs[k];
-        }
-    }
-    if (tid < 97) {
-        __half2 w[4];
-        cell_widths(tid, w);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) s_width[tid * 4 + k] = w[k];
-    }
-    for (int i = tid; i < L * kSubH * kHistRow; i += kSelThreads) hist[i] = 0;
-    for (int i = tid; i < nwords; i += kSelThreads) bm0[i] = 0u;
-    for (int i = tid; i < L * nwords; i += kSelThreads) tieb[i] = 0u;
-    if (tid < kMaxL) {
-        s_nch[tid] = 0;
-        s_tot[tid] = 0;
-    }
-    if (tid == 0) {
-        s_ncand = 0;
-        s_nraw = 0;
-        s_npg = 0;
-        s_fail = 0;
-        if (FUSED) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
     }
     __syncthreads();
