@@ -184,7 +184,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 4), "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 select (fixed-order fp32 dot), f64 attention",
-            "data": "synthetic", "config": _config(w),
+            "data": "synthetic", "config": dict(_config(w), l2="not applicable (host oracle)"),
             "cpu_baseline": {"value": round(us_layer, 3), "unit": UNIT, "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(us_layer, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
