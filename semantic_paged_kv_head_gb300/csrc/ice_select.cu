@@ -691,6 +691,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         if (l >= L) break;
         const int ps = s_pstar[l];
         const unsigned* p32 = reinterpret_cast<const unsigned*>(prio + l * Cp);
+        const uint4* lrec = recs + v.leaf_base(u, l);
         const int nw = (N[l] + 3) >> 2;
         for (int w4 = tid; w4 < nw; w4 += kSelThreads) {
             const unsigned word = p32[w4];
@@ -701,7 +702,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 const int pr = (int)((word >> (8 * b)) & 0xFFu);
                 if (pr < ps) {
                     const int slot = atomicAdd(&s_nch[l], 1);
-                    if (slot < n_cand) chosen[l * n_cand + slot] = i;
+                    if (slot < n_cand) {
+                        chosen[l * n_cand + slot] = i;
+                        // the leaf's id | count, copied while the ties are walked
+                        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                         smem_u32(cmeta + l * n_cand + slot)),
+                                     "l"(&lrec[i].z)
+                                     : "memory");
+                    }
                 } else if (pr == ps) {
                     atomicOr(&tieb[l * nwords + (i >> 5)], 1u << (i & 31));
                 }
@@ -714,8 +722,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     // position order: each lane sums the tokens of its word's ties, a warp scan
     // gives every lane the tokens taken before it, and the lane takes its ties
     // while that running count is below the need. The same warp then computes the
-    // slot offsets of all taken leaves (3d), and warp 0 marks composite 0's taken
-    // pages, so one block barrier closes both steps.
+    // slot offsets of all taken leaves (3d) from the count bytes of the scan, while
+    // the taken leaves' records (list ids) are still being copied.
     if (warp < L) {
         const int l = warp;
         const int need = s_need[l];
@@ -751,21 +759,24 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             }
             int slot = nbelow + ntaken + tinc - mine;
             for (unsigned b = take; b; b &= b - 1u, ++slot)
-                if (slot < n_cand) chosen[l * n_cand + slot] = wi * 32 + __ffs(b) - 1;
+                if (slot < n_cand) {
+                    const int i = wi * 32 + __ffs(b) - 1;
+                    chosen[l * n_cand + slot] = i;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                     smem_u32(cmeta + l * n_cand + slot)),
+                                 "l"(&lrec[i].z)
+                                 : "memory");
+                }
             ntaken += __shfl_sync(0xffffffffu, tinc, 31);
             run += __shfl_sync(0xffffffffu, inc, 31);
         }
         __syncwarp();
-        // the records of all taken leaves, requested together (one memory latency)
-        for (int k = lane; k < min(nbelow + ntaken, n_cand); k += 32)
-            cmeta[l * n_cand + k] = __ldg(lrec + chosen[l * n_cand + k]).z;
-        __syncwarp();
-        // ---- 3d. slot offsets of the taken leaves ----------------------------------------
+        // ---- 3d. slot offsets of the taken leaves (counts from the scan's bytes) -----------
         const int nch = min(nbelow + ntaken, n_cand);
         int carry = 0;
         for (int k0 = 0; k0 < nch; k0 += 32) {
             const int k = k0 + lane;
-            const int c = k < nch ? (int)(cmeta[l * n_cand + k] & 0xFFu) : 0;
+            const int c = k < nch ? (int)cl[chosen[l * n_cand + k]] : 0;
             int inc = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -780,11 +791,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             s_tot[l] = carry;
             s_nch[l] = nbelow + ntaken;
         }
-        if (l == 0) {  // composite-0 pages already taken whole
-            for (int k = lane; k < nch; k += 32) {
-                const int id = (int)(cmeta[k] >> 8);
-                if (id < C) atomicOr(&bm0[id >> 5], 1u << (id & 31));
-            }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // the taken leaves' records
+    __syncthreads();
+    {  // composite-0 pages already taken whole
+        const int nch0 = min(s_nch[0], n_cand);
+        for (int k = tid; k < nch0; k += kSelThreads) {
+            const int id = (int)(cmeta[k] >> 8);
+            if (id < C) atomicOr(&bm0[id >> 5], 1u << (id & 31));
         }
     }
     __syncthreads();
