@@ -61,8 +61,8 @@ constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // bounded barrier
 // there, and the fused attention stages pages there (from `keys` on, after the
 // ranking) and finally the warps' partial results.
 struct SelSmem {
-    int sel, toff;
-    int keys, vals, hpage, hkey, top, ring;
+    int sel, toff, qf;
+    int keys, vals, hpage, hkey, hcnt, top, ring;
     int free;
     int prio, cnt, chosen, cmeta, coff, tieb, bm0, hist;
     int end;
@@ -76,10 +76,12 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
     int o = 0;
     s.sel = o; o = align16(o + n_sel * 4);
     s.toff = o; o = align16(o + (n_sel + 1) * 4);
+    s.qf = o; o = align16(o + kMaxG * kD * 4);
     s.keys = o; o = align16(o + sort_cap * 8);
     s.vals = o; o = align16(o + sort_cap * 4);
     s.hpage = o; o = align16(o + hcap * 4);
     s.hkey = o; o = align16(o + hcap * 8);
+    s.hcnt = o; o = align16(o + hcap * 4);
     s.top = o; o = align16(o + kSelWarps * kTopK * 12);
     s.ring = s.keys;  // the scan's copy ring, dead before the candidates are written
     if (o < s.ring + kRingB) o = s.ring + kRingB;
@@ -273,7 +275,8 @@ template <> struct Chunk<float> {
 // costs one warp instruction per step and log2(32/G) shuffles per head.
 template <typename T, int G>
 __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T* __restrict__ q,
-                                              int npg, const int* s_sel, int* s_toff,
+                                              const float* s_q, const int* hpage, const int* hcnt,
+                                              int hcap, int npg, const int* s_sel, int* s_toff,
                                               int* s_ntok, unsigned char* stage,
                                               int stage_bytes, unsigned bar, int* s_fail,
                                               T* __restrict__ out) {
@@ -291,7 +294,20 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
             int c = 0;
             if (r < npg) {
                 const int pg = s_sel[r];
-                if (pg >= 0 && pg < v.C) c = v.list_cnt[v.leaf_base(u, 0) + pg];
+                if (hcnt != nullptr) {  // the count copied into the page table with the page
+                    unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)(hcap - 1);
+                    for (int probe = 0; probe < hcap; ++probe) {
+                        const int hp = hpage[hh];
+                        if (hp == pg) {
+                            c = hcnt[hh];
+                            break;
+                        }
+                        if (hp == -1) break;
+                        hh = (hh + 1) & (unsigned)(hcap - 1);
+                    }
+                } else if (pg >= 0 && pg < v.C) {
+                    c = v.list_cnt[v.leaf_base(u, 0) + pg];
+                }
                 c = c < 0 ? 0 : (c > P ? P : c);
             }
             int inc = c;
@@ -311,13 +327,18 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
     float qa[DPL];
     {
         const float sc = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
-        const T* qh = q + ((long long)u * G + h) * kD + g * DPL;
+        if (s_q != nullptr) {  // the query rows kept in shared memory since the start
 #pragma unroll
-        for (int k = 0; k < DPL; k += 4) {
-            float x[4];
-            load4(qh + k, x);
+            for (int k = 0; k < DPL; ++k) qa[k] = s_q[h * kD + g * DPL + k] * sc;
+        } else {
+            const T* qh = q + ((long long)u * G + h) * kD + g * DPL;
 #pragma unroll
-            for (int z = 0; z < 4; ++z) qa[k + z] = x[z] * sc;
+            for (int k = 0; k < DPL; k += 4) {
+                float x[4];
+                load4(qh + k, x);
+#pragma unroll
+                for (int z = 0; z < 4; ++z) qa[k + z] = x[z] * sc;
+            }
         }
     }
     __syncthreads();
@@ -471,6 +492,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.keys);
     int* sval = reinterpret_cast<int*>(smem + lay.vals);
     int* hpage = reinterpret_cast<int*>(smem + lay.hpage);
+    int* hcnt = reinterpret_cast<int*>(smem + lay.hcnt);
     unsigned long long* hkey = reinterpret_cast<unsigned long long*>(smem + lay.hkey);
     unsigned long long* topk = reinterpret_cast<unsigned long long*>(smem + lay.top);
     int* topv = reinterpret_cast<int*>(smem + lay.top + kSelWarps * kTopK * 8);
@@ -489,8 +511,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             }
             __syncthreads();
-            attend_staged<T, G>(v, u, q, taken, s_sel, s_toff, &s_ntok, smem + lay.keys,
-                                smem_total - lay.keys, smem_u32(&s_bar), &s_fail, attn_out);
+            attend_staged<T, G>(v, u, q, nullptr, nullptr, nullptr, 0, taken, s_sel, s_toff, &s_ntok,
+                                smem + lay.keys, smem_total - lay.keys, smem_u32(&s_bar), &s_fail,
+                                attn_out);
         }
         return;
     }
@@ -584,6 +607,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         if (warp == 0) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) s_qsel[4 * lane + k] = qs[k];
+            if (FUSED) {  // the query rows, for the attention tail
+                float* qf = reinterpret_cast<float*>(smem + lay.qf);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) qf[hh * kD + 4 * lane + k] = qh[hh][k];
+            }
         }
     }
     __syncthreads();
@@ -956,6 +986,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                     const int old = atomicCAS(&hpage[h], -1, pg);
                     if (old == -1 || old == pg) {
                         fresh = old == -1;
+                        if (FUSED && fresh)  // the page's token count, for the attention tail
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                             smem_u32(hcnt + h)),
+                                         "l"(v.list_cnt + v.leaf_base(u, 0) + pg)
+                                         : "memory");
                         atomicMin(&hkey[h], key);
                         break;
                     }
@@ -1077,7 +1112,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     }
     if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
     if constexpr (FUSED)
-        attend_staged<T, G>(v, u, q, taken, s_sel, s_toff, &s_ntok, smem + lay.keys,
+        attend_staged<T, G>(v, u, q, reinterpret_cast<const float*>(smem + lay.qf), hpage, hcnt,
+                            hcap, taken, s_sel, s_toff, &s_ntok, smem + lay.keys,
                             smem_total - lay.keys, smem_u32(&s_bar), &s_fail, attn_out);
 }
 
