@@ -86,6 +86,10 @@ def test_tiny_fp32_4k_workload(ice):
     (5000, 16, 1, 2, torch.float32, 256),
     (777, 8, 2, 1, torch.bfloat16, 64),
     (4097, 16, 2, 8, torch.bfloat16, 128),
+    (3500, 64, 2, 4, torch.bfloat16, 1024),  # the largest page size
+    (2600, 8, 2, 4, torch.bfloat16, 512),    # 64 pages: block-wide ranking instead of warp top-32
+    (2600, 8, 1, 2, torch.float32, 512),
+    (1200, 16, 2, 4, torch.bfloat16, 16),    # one page
 ])
 def test_scaled_llama_shapes(ice, n, P, L, G, dtype, budget):
     synth = _synth()
@@ -93,6 +97,32 @@ def test_scaled_llama_shapes(ice, n, P, L, G, dtype, budget):
                      n_tokens=n, dtype=dtype, page_size=P, n_composite=L, budget=budget,
                      n_centers=32, seed=n)
     _full_check(ice, w)
+
+
+@pytest.mark.parametrize("mult", [2, 4])
+def test_larger_candidate_counts(ice, mult):
+    """n_cand = 2 and 4 x the budget (the recall curve's settings)."""
+    synth = _synth()
+    w = synth.scaled(synth.WORKLOADS["llama8b_36k"], n_layers=1, n_kv_heads=2, n_tokens=3000,
+                     n_centers=24, seed=53 + mult)
+    keys, values, centers = synth.make_kv(w)
+    q = synth.make_queries(w, centers)
+    n_cand = mult * w.budget
+    gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                             n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed,
+                             n_cand=n_cand)
+    stats = torch.zeros((gix.n_units, 4), dtype=torch.int32, device="cuda")
+    out, ids, npg = gix.select_attn(q.cuda(), w.budget, stats=stats)
+    torch.cuda.synchronize()
+    assert gix.get_error() == 0
+    for u in range(w.n_units):
+        orc = oracle_for_unit(w, keys, values, u)
+        qu = q_of_unit(w, q, u)
+        rid, rn, tr = orc.select(qu, w.budget, n_cand)
+        assert int(npg[u]) == rn and np.array_equal(ids[u].cpu().numpy(), rid)
+        assert int(stats[u, 1]) == tr["cands"] and int(stats[u, 0]) == tr["leaves"]
+        err = np.max(np.abs(out.view(-1, w.group, w.d)[u].float().cpu().numpy() - orc.attn(qu, rid, rn)))
+        assert err <= 2e-2
 
 
 @pytest.mark.parametrize("n", [1, 15, 16, 17, 40])
