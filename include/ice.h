@@ -203,7 +203,9 @@ int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t
 /*
  * ice_decode_step - one decode step of every unit: ice_insert of the new
  * token's k, v, then ice_select_attn for the query q (the new token is a
- * candidate like any other). Two kernel launches on `stream`, no host
+ * candidate like any other). One kernel launch on `stream` (each block inserts
+ * its unit's token, then selects and attends; with a host-resident pool, or
+ * when the split's staging does not fit, the separate launches), no host
  * synchronisation and no allocation, so a sequence of steps can be captured
  * once in a CUDA graph and replayed: the insert takes the token index from a
  * per-unit count kept on the device, which every replay advances (a unit at

@@ -397,6 +397,21 @@ int ice_decode_step(ice_index* ix, const void* k, const void* v, const void* q,
     if (!ix || !out) return ICE_ERR_INVALID_ARG;
     const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
     if (a != ICE_OK) return a;
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return ICE_ERR_INVALID_ARG;
+    if (ix->n_tok >= ix->v.max_tokens) return ICE_ERR_CAPACITY;
+    const int P = ix->p.page_size;
+    const int n_sel = token_budget / P;
+    const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
+    const int es = ix->p.dtype == ICE_BF16 ? 2 : 4;
+    if (ix->p.kv_location == ICE_KV_DEVICE &&
+        select_insert_fits(ix->C, ix->p.n_composite, P, n_cand, n_sel, es)) {
+        // one launch: every block inserts its unit's token, then selects and attends
+        cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, nullptr, out,
+                                      nullptr, (cudaStream_t)stream, k, v);
+        if (e != cudaSuccess) return ICE_ERR_CUDA;
+        ix->n_tok += 1;
+        return ICE_OK;
+    }
     const int r = ice_insert(ix, k, v, stream);
     if (r != ICE_OK) return r;
     return ice_select_attn(ix, q, token_budget, page_ids, n_pages, nullptr, out, stream);

@@ -1,0 +1,342 @@
+// Dynamic insertion of one generated token into one unit, by a block of NT
+// threads ("IceCache" abstract: a hierarchical, dynamically updatable
+// structure; the blog: no rebuild when a new token appears). Used by the
+// insert kernel (one 128-thread block per unit) and by the fused decode step
+// (the select kernel's block inserts its unit's token before it selects).
+//
+// The trie over 96-bit keys is history independent: a node is a leaf iff its
+// parent holds more than P keys. Adding key x therefore changes only the leaf
+// on x's path:
+//  * x carries the prefix of an existing leaf holding < P tokens: append;
+//  * that leaf holds P tokens: its P+1 keys share exactly lambda = lcp(min, max)
+//    bits, so it splits into the two children at bit lambda (left keeps the
+//    page id, right takes the next free id);
+//  * x carries no leaf prefix: x opens a new leaf one bit below its longest
+//    common prefix with any existing key (its neighbours in key order).
+// Composites are handled one after the other.
+#pragma once
+#include "ice_internal.cuh"
+
+namespace ice {
+
+// Shift leaf keys, records and the records' scan copies [from, N) one place to
+// the right (backwards, in chunks of one element per thread of the NT-thread block).
+template <int NT>
+__device__ void shift_right(LeafKey* key, uint4* rec, unsigned long long* lo, unsigned short* tc,
+                            int from, int N) {
+    for (int end = N; end > from; end -= NT) {
+        const int start = max(from, end - NT);
+        const int i = start + (int)threadIdx.x;
+        LeafKey k;
+        uint4 r;
+        unsigned long long a = 0;
+        unsigned short c = 0;
+        const bool act = i < end;
+        if (act) {
+            k = key[i];
+            r = rec[i];
+            a = lo[i];
+            c = tc[i];
+        }
+        __syncthreads();
+        if (act) {
+            key[i + 1] = k;
+            rec[i + 1] = r;
+            lo[i + 1] = a;
+            tc[i + 1] = c;
+        }
+        __syncthreads();
+    }
+}
+
+// The new token of unit u: key kin, value vin (device rows of kD elements);
+// rows: shared memory for 2 (P + 1) rows of T (the staged K and V of a split).
+// Every thread of the block calls it; the token index is the unit's count.
+template <typename T, int NT>
+__device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin,
+                            const T* __restrict__ vin, unsigned char* rows) {
+    constexpr int ROW = kD;  // elements per row
+    T* rows_k = reinterpret_cast<T*>(rows);                      // [P+1][D]
+    T* rows_v = rows_k + (size_t)(v.P + 1) * ROW;                // [P+1][D]
+    __shared__ unsigned long long s_mk[kMaxL];
+    __shared__ unsigned long long e_m[kMaxP + 1];
+    __shared__ unsigned int e_t[kMaxP + 1];
+    __shared__ int e_slot[kMaxP + 1];  // original slot (P = the new token)
+    __shared__ int s_sorted[kMaxP + 1];
+    __shared__ int s_lo, s_hi, s_cnt, s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = v.P;
+    // the new token's index is the unit's count, kept on the device (so that a
+    // captured CUDA graph of inserts advances it on every replay)
+    const int tok = v.n_tok[u];
+    if (tok < 0 || tok >= v.max_tokens) {  // block-uniform
+        if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
+        return;
+    }
+
+    // ---- key of the new token: frozen scale, projections, codes (warp 0) ----------
+    if (warp == 0) {
+        float k4[4];
+        load4(kin + 4 * lane, k4);
+        const float nrm2 = warp_dot_fixed(k4, k4);
+        const int e = v.e_unit[u];
+        const float sc = ldexpf(1.0f, -e), sc2 = ldexpf(1.0f, -2 * e);
+        float kt[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kt[i] = __fmul_rn(k4[i], sc);
+        float r = __fsub_rn(1.0f, __fmul_rn(nrm2, sc2));
+        r = r > 0.0f ? r : 0.0f;
+        const float tail = __fsqrt_rn(r);
+        for (int l = 0; l < v.L; ++l) {
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float* ud = v.dirs + (long long)(l * kM + j) * kDirStride;
+                float w[4];
+                load4(ud + 4 * lane, w);
+                const float p = __fmaf_rn(ud[kD], tail, warp_dot_fixed(w, kt));
+                c[j] = quantise_code(p);
+            }
+            if (lane == 0) s_mk[l] = morton8(c);
+        }
+    }
+    if (tid == 0) s_abort = 0;
+    __syncthreads();
+
+    for (int l = 0; l < v.L; ++l) {
+        const unsigned long long xm = s_mk[l];
+        const unsigned int xt = (unsigned)tok;
+        LeafKey* lk = v.leaf_key + v.leaf_base(u, l);
+        const long long lb0 = v.leaf_base(u, l);
+        uint4* lr = v.leaf_rec + lb0;
+        unsigned long long* llo = v.leaf_lo + lb0;
+        unsigned short* ltc = v.leaf_tc + lb0;
+        int* cntl = v.list_cnt + v.leaf_base(u, l);
+        int* stok = v.slot_tok + v.slot_base(u, l);
+        unsigned long long* skey = v.slot_key + v.slot_base(u, l);
+        const int N = v.n_leaf[v.ul(u, l)];
+        const int nid = v.next_id[v.ul(u, l)];
+
+        // ---- a = number of leaves whose prefix <= x (k-ary search) --------------------
+        if (tid == 0) {
+            s_lo = 0;
+            s_hi = N;
+        }
+        __syncthreads();
+        int a = -1;
+        while (a < 0) {
+            const int lo = s_lo, hi = s_hi;
+            if (hi - lo <= NT) {
+                const int i = lo + tid;
+                bool le = false;
+                if (i < hi) {
+                    const LeafKey k = lk[i];
+                    le = !key_less(xm, xt, k.pm, k.pt);
+                }
+                a = lo + __syncthreads_count(le);
+                break;
+            }
+            const int step = (hi - lo + NT - 1) / NT;
+            const int i = lo + tid * step;
+            bool le = false;
+            if (i < hi) {
+                const LeafKey k = lk[i];
+                le = !key_less(xm, xt, k.pm, k.pt);
+            }
+            const int c = __syncthreads_count(le);
+            if (c == 0) {
+                a = lo;
+                break;
+            }
+            if (tid == 0) {
+                const int pc = lo + (c - 1) * step;
+                s_lo = pc + 1;
+                s_hi = min(hi, pc + step);
+            }
+            __syncthreads();
+        }
+        const int pos = a - 1;  // last leaf with prefix <= x, or -1
+        bool member = false;
+        uint4 rc = make_uint4(0u, 0u, 0u, 0u);
+        if (pos >= 0) {
+            const LeafKey k = lk[pos];
+            unsigned long long pm;
+            unsigned int pt;
+            prefix96(xm, xt, (int)k.t, pm, pt);
+            member = pm == k.pm && pt == k.pt;
+            rc = lr[pos];
+        }
+        const int id = rec_id(rc), cnt = rec_cnt(rc);
+        const bool split = member && cnt >= P;
+        __syncthreads();  // every thread has read the record before any thread updates it
+        // capacity: a split or a new leaf needs one more leaf record and list id
+        if (!(member && !split) && (N + 1 > v.C || nid + 1 > v.C)) {
+            if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
+            __syncthreads();
+            break;
+        }
+
+        if (member && !split) {
+            // ---- append to the leaf ---------------------------------------------------
+            if (tid == 0) {
+                const long long sb = (long long)id * P + cnt;
+                stok[sb] = tok;
+                skey[sb] = xm;
+                cntl[id] = cnt + 1;
+                uint4 r2 = rc;
+                r2.z = ((unsigned)id << 8) | (unsigned)(cnt + 1);
+                put_leaf(v, lb0 + pos, r2);
+                if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = id * P + cnt;
+            }
+            if (l == 0) {
+                T* pk = reinterpret_cast<T*>(v.page_k) + v.page_row(u, id, cnt) * kD;
+                T* pv = reinterpret_cast<T*>(v.page_v) + v.page_row(u, id, cnt) * kD;
+                for (int i = tid; i < kD; i += NT) {
+                    pk[i] = kin[i];
+                    pv[i] = vin[i];
+                }
+            }
+            __syncthreads();
+            continue;
+        }
+
+        if (split) {
+            // ---- split the full leaf in two ---------------------------------------------
+            for (int j = tid; j <= P; j += NT) {
+                if (j < P) {
+                    e_m[j] = skey[(long long)id * P + j];
+                    e_t[j] = (unsigned)stok[(long long)id * P + j];
+                } else {
+                    e_m[j] = xm;
+                    e_t[j] = xt;
+                }
+                e_slot[j] = j;
+            }
+            if (l == 0) {  // stage the P old rows and the new row, K and V
+                const T* pk = reinterpret_cast<const T*>(v.page_k) + v.page_row(u, id, 0) * kD;
+                const T* pv = reinterpret_cast<const T*>(v.page_v) + v.page_row(u, id, 0) * kD;
+                for (int i = tid; i < (P + 1) * kD; i += NT) {
+                    const int r = i / kD, c = i % kD;
+                    rows_k[i] = r < P ? pk[(long long)r * kD + c] : kin[c];
+                    rows_v[i] = r < P ? pv[(long long)r * kD + c] : vin[c];
+                }
+            }
+            __syncthreads();
+            // rank of each key among the P+1 (keys are distinct)
+            for (int j = tid; j <= P; j += NT) {
+                int r = 0;
+                for (int k = 0; k <= P; ++k) r += key_less(e_m[k], e_t[k], e_m[j], e_t[j]);
+                s_sorted[r] = j;
+            }
+            __syncthreads();
+            const int f = s_sorted[0], g = s_sorted[P];
+            const int lam = lcp96(e_m[f], e_t[f], e_m[g], e_t[g]);
+            if (tid == 0) {
+                int nl = 0;
+                for (int r = 0; r <= P; ++r) nl += key_bit96(e_m[s_sorted[r]], e_t[s_sorted[r]], lam) == 0;
+                s_cnt = nl;
+            }
+            __syncthreads();
+            const int nl = s_cnt, nr = P + 1 - nl;
+            const int rid = nid;  // right child takes the next free id
+            for (int r = tid; r <= P; r += NT) {
+                const int j = s_sorted[r];
+                const int dst = r < nl ? id : rid;
+                const int slot = r < nl ? r : r - nl;
+                stok[(long long)dst * P + slot] = (int)e_t[j];
+                skey[(long long)dst * P + slot] = e_m[j];
+                if (l == 0) v.tok_loc[(long long)u * v.max_tokens + e_t[j]] = dst * P + slot;
+            }
+            if (l == 0) {
+                for (int i = tid; i < (P + 1) * kD; i += NT) {
+                    const int r = i / kD, c = i % kD;
+                    const int j = s_sorted[r];
+                    const int dst = r < nl ? id : rid;
+                    const int slot = r < nl ? r : r - nl;
+                    const long long o = v.page_row(u, dst, slot) * kD + c;
+                    reinterpret_cast<T*>(v.page_k)[o] = rows_k[(long long)j * kD + c];
+                    reinterpret_cast<T*>(v.page_v)[o] = rows_v[(long long)j * kD + c];
+                }
+            }
+            __syncthreads();
+            shift_right<NT>(lk, lr, llo, ltc, pos + 1, N);
+            if (tid == 0) {
+                cntl[id] = nl;
+                cntl[rid] = nr;
+                const int t = lam + 1;
+                LeafKey kl, kr;
+                prefix96(e_m[f], e_t[f], t, kl.pm, kl.pt);
+                prefix96(e_m[g], e_t[g], t, kr.pm, kr.pt);
+                kl.t = kr.t = (unsigned)t;
+                lk[pos] = kl;
+                put_leaf(v, lb0 + pos, make_leaf_rec(kl.pm, (unsigned)t, id, nl));
+                lk[pos + 1] = kr;
+                put_leaf(v, lb0 + pos + 1, make_leaf_rec(kr.pm, (unsigned)t, rid, nr));
+                v.n_leaf[v.ul(u, l)] = N + 1;
+                v.next_id[v.ul(u, l)] = nid + 1;
+            }
+            __syncthreads();
+            continue;
+        }
+
+        // ---- x lies where no leaf exists: a new leaf below its longest common
+        //      prefix with the neighbouring keys -------------------------------------------
+        {
+            int best = -1;
+            // predecessor leaf `pos` and successor leaf `pos + 1`: all their keys
+            for (int side = 0; side < 2; ++side) {
+                const int li = pos + side;
+                if (li < 0 || li >= N) continue;
+                const uint4 r2 = lr[li];
+                const int id2 = rec_id(r2), c2 = rec_cnt(r2);
+                int bl = -1;
+                if (tid < c2) {
+                    const unsigned long long km = skey[(long long)id2 * P + tid];
+                    const unsigned int kt = (unsigned)stok[(long long)id2 * P + tid];
+                    bl = lcp96(xm, xt, km, kt);
+                }
+                for (int o = 16; o >= 1; o >>= 1) bl = max(bl, __shfl_xor_sync(0xffffffffu, bl, o));
+                best = max(best, bl);
+            }
+            // combine the warps (P <= 64 keys live in warps 0 and 1)
+            __shared__ int s_best[NT / 32];
+            if (lane == 0) s_best[warp] = best;
+            __syncthreads();
+            if (tid == 0) {
+                int b = -1;
+                for (int w = 0; w < NT / 32; ++w) b = max(b, s_best[w]);
+                s_cnt = b + 1;  // depth of the new leaf
+            }
+            __syncthreads();
+            const int t = s_cnt;
+            const int nidl = nid;
+            if (l == 0) {
+                T* pk = reinterpret_cast<T*>(v.page_k) + v.page_row(u, nidl, 0) * kD;
+                T* pv = reinterpret_cast<T*>(v.page_v) + v.page_row(u, nidl, 0) * kD;
+                for (int i = tid; i < kD; i += NT) {
+                    pk[i] = kin[i];
+                    pv[i] = vin[i];
+                }
+            }
+            shift_right<NT>(lk, lr, llo, ltc, pos + 1, N);
+            if (tid == 0) {
+                stok[(long long)nidl * P] = tok;
+                skey[(long long)nidl * P] = xm;
+                cntl[nidl] = 1;
+                if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = nidl * P;
+                LeafKey k;
+                prefix96(xm, xt, t, k.pm, k.pt);
+                k.t = (unsigned)t;
+                lk[pos + 1] = k;
+                put_leaf(v, lb0 + pos + 1, make_leaf_rec(k.pm, (unsigned)t, nidl, 1));
+                v.n_leaf[v.ul(u, l)] = N + 1;
+                v.next_id[v.ul(u, l)] = nid + 1;
+            }
+            __syncthreads();
+        }
+    }
+    if (tid == 0) v.n_tok[u] = tok + 1;  // every thread read the count at the start
+}
+
+}  // namespace ice

@@ -278,6 +278,7 @@ cudaError_t build_phase2(const IndexView& v, const void* keys, const void* value
 cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st);
 void scratch_free(BuildScratch& s, cudaStream_t st);
 int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, bool fused);
+bool select_insert_fits(long long C, int L, int P, int n_cand, int n_sel, int es);
 cudaError_t select_prepare();
 
 // ---- launchers (implemented in the .cu files) --------------------------------------
@@ -289,9 +290,12 @@ cudaError_t insert_prepare(int P, int dtype);
 constexpr int kSelSmemMax = 220 * 1024;
 // reselect: nullable [U]; a unit whose flag is 0 keeps its pages (page_ids,
 // n_pages unchanged) and, in the fused call, attends over them
+// knew, vnew: nullable; with the fused kernel, each block first inserts its
+// unit's new token (the decode step in one launch)
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
                           int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                          const int32_t* reselect, cudaStream_t s);
+                          const int32_t* reselect, cudaStream_t s, const void* knew = nullptr,
+                          const void* vnew = nullptr);
 // Per-query-head selection (block = unit x head) and the union of each unit's
 // per-head page lists in head-major first-occurrence order.
 cudaError_t launch_select_heads(const IndexView& v, const void* q, int n_sel, int n_cand,

@@ -38,6 +38,7 @@
 //     dimensions' group), one token per warp instruction, fp32 online softmax
 //     per warp, warps merged in a fixed order.
 #include "ice_internal.cuh"
+#include "ice_insert.cuh"
 
 #include <cuda_fp16.h>
 
@@ -248,24 +249,6 @@ __device__ __forceinline__ void load_chunk<float>(const unsigned char* p, float 
     x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
 }
 
-template <typename T> struct Chunk;
-template <> struct Chunk<__nv_bfloat16> {
-    uint2 r;
-    __device__ __forceinline__ void load(const __nv_bfloat16* p) { r = __ldg(reinterpret_cast<const uint2*>(p)); }
-    __device__ __forceinline__ void get(float (&x)[4]) const {
-        x[0] = __uint_as_float(r.x << 16);
-        x[1] = __uint_as_float(r.x & 0xFFFF0000u);
-        x[2] = __uint_as_float(r.y << 16);
-        x[3] = __uint_as_float(r.y & 0xFFFF0000u);
-    }
-};
-template <> struct Chunk<float> {
-    float4 r;
-    __device__ __forceinline__ void load(const float* p) { r = __ldg(reinterpret_cast<const float4*>(p)); }
-    __device__ __forceinline__ void get(float (&x)[4]) const {
-        x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
-    }
-};
 
 // Attention of the G query heads of unit u over every token of the selected
 // pages (the fused tail). Pages are staged in rounds that fit the staging
@@ -458,12 +441,20 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
     }
 }
 
+// The decode step's insert, kept out of line so that the select path's code and
+// register allocation stay those of the plain fused call.
+template <typename T>
+__device__ __noinline__ void insert_unit_call(const IndexView& v, int u, const T* kin, const T* vin,
+                                              unsigned char* rows) {
+    insert_unit<T, kSelThreads>(v, u, kin, vin, rows);
+}
+
 template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
     int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
     int32_t* __restrict__ stats, T* __restrict__ attn_out, const int32_t* __restrict__ reselect,
-    int head_div) {
+    int head_div, const T* __restrict__ knew, const T* __restrict__ vnew) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float s_qsel[kD];
     __shared__ int s_qcode[kMaxL][kM];
@@ -498,6 +489,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int* topv = reinterpret_cast<int*>(smem + lay.top + kSelWarps * kTopK * 8);
     const int nwords = (int)((C + 31) / 32);
     const uint4* recs = v.leaf_rec;
+
+    // the fused decode step: this block first inserts its unit's new token
+    if constexpr (FUSED) {
+        if (knew != nullptr) {  // block-uniform
+            insert_unit_call<T>(v, u, knew + (long long)u * kD, vnew + (long long)u * kD,
+                                smem + lay.free);
+            // the new rows reach the bulk copies of the attention (async proxy)
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __syncthreads();
+        }
+    }
 
     // the unit keeps the pages it selected before (reuse across steps): no
     // selection, and the fused call attends over the pages in page_ids
@@ -854,12 +856,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 const int slot = jj - off[lo];
                 const int id = (int)(cmeta[l * n_cand + lo] >> 8);
                 if (id < C && slot < P) {
-                    tok = __ldg(v.slot_tok + v.slot_base(u, l) + (long long)id * P + slot);
+                    // plain loads: a fused decode step has just written these lists
+                    tok = v.slot_tok[v.slot_base(u, l) + (long long)id * P + slot];
                     if (l == 0) {
                         loc = id * P + slot;
                         keep = true;
                     } else if (tok >= 0 && tok < v.max_tokens) {
-                        loc = __ldg(v.tok_loc + (long long)u * v.max_tokens + tok);
+                        loc = v.tok_loc[(long long)u * v.max_tokens + tok];
                         const int pg = loc / P;
                         keep = loc >= 0 && pg < C && !((bm0[pg >> 5] >> (pg & 31)) & 1u);
                     }
@@ -1127,6 +1130,15 @@ static void select_caps(int L, int P, int n_cand, int* sort_cap, int* hcap) {
 
 // Dynamic shared memory of a launch (fused blocks are padded up to kFusedSmem so
 // that the page staging region is as large as two blocks per SM allow).
+// Whether the fused kernel's free region holds the rows a decode-step insert
+// stages for a split (2 (P + 1) rows of es bytes per element).
+bool select_insert_fits(long long C, int L, int P, int n_cand, int n_sel, int es) {
+    int sc, hc;
+    select_caps(L, P, n_cand, &sc, &hc);
+    const SelSmem lay = sel_layout(C, L, n_cand, sc, hc, n_sel, kFusedSmem);
+    return (long long)2 * (P + 1) * kD * es <= (long long)(lay.end - lay.free);
+}
+
 int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, bool fused) {
     (void)G;
     int sc, hc;
@@ -1138,7 +1150,8 @@ int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, b
 template <typename T, int G>
 static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel, int n_cand,
                                    int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                                   const int32_t* reselect, cudaStream_t s) {
+                                   const int32_t* reselect, const void* knew, const void* vnew,
+                                   cudaStream_t s) {
     int sort_cap, hcap;
     select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
     const bool fused = out != nullptr;
@@ -1146,34 +1159,37 @@ static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel,
     if (fused)
         select_kernel<T, G, true><<<v.U, kSelThreads, bytes, s>>>(
             v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, (T*)out,
-            reselect, 1);
+            reselect, 1, (const T*)knew, (const T*)vnew);
     else
         select_kernel<T, G, false><<<v.U, kSelThreads, bytes, s>>>(
             v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, nullptr,
-            reselect, 1);
+            reselect, 1, nullptr, nullptr);
     return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t launch_select_dt(const IndexView& v, const void* q, int n_sel, int n_cand,
                                     int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                                    const int32_t* reselect, cudaStream_t s) {
+                                    const int32_t* reselect, const void* knew, const void* vnew,
+                                    cudaStream_t s) {
     switch (v.G) {
-        case 1: return launch_select_g<T, 1>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
-        case 2: return launch_select_g<T, 2>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
-        case 4: return launch_select_g<T, 4>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
-        case 8: return launch_select_g<T, 8>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
+        case 1: return launch_select_g<T, 1>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, knew, vnew, s);
+        case 2: return launch_select_g<T, 2>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, knew, vnew, s);
+        case 4: return launch_select_g<T, 4>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, knew, vnew, s);
+        case 8: return launch_select_g<T, 8>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, knew, vnew, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_cand,
                           int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                          const int32_t* reselect, cudaStream_t s) {
+                          const int32_t* reselect, cudaStream_t s, const void* knew,
+                          const void* vnew) {
     if (v.dtype == ICE_BF16)
         return launch_select_dt<__nv_bfloat16>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out,
-                                               reselect, s);
-    return launch_select_dt<float>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect, s);
+                                               reselect, knew, vnew, s);
+    return launch_select_dt<float>(v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect,
+                                   knew, vnew, s);
 }
 
 // Per-query-head selection: one block per (unit, query head) selects with that
@@ -1186,11 +1202,11 @@ cudaError_t launch_select_heads(const IndexView& v, const void* q, int n_sel, in
     if (v.dtype == ICE_BF16)
         select_kernel<__nv_bfloat16, 1, false><<<v.U * v.G, kSelThreads, bytes, s>>>(
             v, (const __nv_bfloat16*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages,
-            nullptr, nullptr, nullptr, v.G);
+            nullptr, nullptr, nullptr, v.G, nullptr, nullptr);
     else
         select_kernel<float, 1, false><<<v.U * v.G, kSelThreads, bytes, s>>>(
             v, (const float*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, nullptr,
-            nullptr, nullptr, v.G);
+            nullptr, nullptr, v.G, nullptr, nullptr);
     return cudaGetLastError();
 }
 

@@ -74,3 +74,48 @@ def test_graph_replay_equals_eager(ice):
     assert graphed.get_error() == ice.ICE_ERR_CAPACITY
     for u in range(U):
         _dump_equal(graphed.dump(u), before[u])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_fused_decode_step_equals_separate_calls(ice, dtype):
+    """The one-launch decode step (each block inserts its unit's token, then
+    selects and attends) gives the index, pages and outputs of ice_insert
+    followed by ice_select_attn, and the oracle's pages."""
+    from oracle import oracle as O  # noqa: F401
+    from semantic_paged_kv_head_gb300 import synth
+    from tests.parity_helpers import check_select_attn, compare_index, oracle_for_unit, q_of_unit
+    w = synth.scaled(synth.WORKLOADS["mistral7b_gen8k"], n_kv_heads=3, n_tokens=700, n_insert=90,
+                     n_centers=12, dtype=dtype, seed=59)
+    keys, values, centers = synth.make_kv(w)
+    deltas = synth.make_drift(w, centers)
+    cap = w.n_tokens + w.n_insert
+
+    def index():
+        return ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                                  n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed,
+                                  max_tokens=cap)
+
+    U, n_sel = w.n_units, w.budget // w.page_size
+    fused, sep = index(), index()
+    orcs = [oracle_for_unit(w, keys, values, u) for u in range(U)]
+    ids_f = torch.empty((U, n_sel), dtype=torch.int32, device="cuda")
+    npg_f = torch.empty((U,), dtype=torch.int32, device="cuda")
+    for t in range(w.n_insert):
+        k, v = synth.make_insert_token(w, centers, deltas, t)
+        q = synth.make_queries(w, centers, step=t, drift_deltas=deltas)
+        kc, vc, qc = k.cuda(), v.cuda(), q.cuda()
+        out_f = torch.empty_like(qc)
+        fused.decode_step(kc, vc, qc, w.budget, ids_f, npg_f, out_f)
+        sep.insert(kc, vc)
+        out_s, ids_s, npg_s = sep.select_attn(qc, w.budget)
+        for u in range(U):
+            orcs[u].insert(k.view(-1, w.d)[u], v.view(-1, w.d)[u])
+        torch.cuda.synchronize()
+        assert torch.equal(ids_f, ids_s) and torch.equal(npg_f, npg_s), t
+        assert torch.equal(out_f, out_s), t
+        if t % 30 == 29:
+            for u in range(U):
+                compare_index(fused.dump(u), orcs[u], f"step {t} unit {u}")
+                check_select_attn(w, orcs[u], q_of_unit(w, q, u), ids_f[u], npg_f[u],
+                                  out_f.view(-1, w.group, w.d)[u], None, f"step {t} unit {u}")
+    assert fused.get_error() == 0 and sep.get_error() == 0
