@@ -214,6 +214,24 @@ def _traffic_for(kernel, src_file):
     return ent.get("dram_bytes_per_launch_full")
 
 
+def reduce_max(values, device, world):
+    """Element-wise maximum over the ranks (the step time of the job is its
+    slowest replica); identity with one rank."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def us_per_layer(ms_step, w, world):
+    """Whole-job µs per layer: every rank runs a replica of the workload, so one
+    step processes world x batch x n_layers layers."""
+    return ms_step * 1e3 / (w.n_layers * w.batch * world)
+
+
 def per_layer_serial(ice, w, keys, values, q, flush, timed, args):
     """One launch per layer, in sequence, as a decode loop issues them: an index per
     layer (its KV heads), and the step = n_layers fused calls after an L2 flush."""
@@ -653,12 +671,9 @@ def run_ice(args):
     ms_att = (t_fsa - t_fs) / n_steps
     ms_sep = (t_fsa - t_f) / n_steps
     ms_fused = (t_fx - t_f) / n_steps  # the fused call: one launch per step
+    ms_sel, ms_att, ms_sep, ms_fused = reduce_max([ms_sel, ms_att, ms_sep, ms_fused], dev, world)
     fused_faster = ms_fused <= ms_sep
     ms_step = min(ms_fused, ms_sep)
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
     ix.check()
 
     # end to end through the public API: pinned host q in, host out back, every step
@@ -680,7 +695,7 @@ def run_ice(args):
         out_host.copy_(out, non_blocking=True)
         ev2[k][1].record(stream)
     torch.cuda.synchronize()
-    ms_e2e = sum(e[0].elapsed_time(e[1]) for e in ev2) / n_e2e
+    ms_e2e = reduce_max([sum(e[0].elapsed_time(e[1]) for e in ev2) / n_e2e], dev, world)[0]
 
     peak, peak_kind = _peaks()
     sel_gbs = sel_bytes / (ms_sel * 1e-3) / 1e9
@@ -696,7 +711,7 @@ def run_ice(args):
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
     # every rank runs its own replica of the workload: the job processes
     # world x n_layers layers per step
-    us_layer = ms_step * 1e3 / (w.n_layers * w.batch * world)
+    us_layer = us_per_layer(ms_step, w, world)
     line = {
         "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world,
         "steps": n_steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
@@ -719,7 +734,7 @@ def run_ice(args):
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": _traffic_for(dom, src), "algorithmic_bytes": int(dom_bytes)},
-        "e2e": {"value": round(ms_e2e * 1e3 / (w.n_layers * w.batch * world), 4), "unit": UNIT,
+        "e2e": {"value": round(us_per_layer(ms_e2e, w, world), 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(q.numel() * q.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size())},
         "gpu_launches": 4 * n_steps,
@@ -731,10 +746,11 @@ def run_ice(args):
         "clocks": clk.summary(),
     }
     # warm L2 (no flush): the same fused step repeated on resident data
-    t_w = timed(lambda: ix.select_attn(q, w.budget, out, page_ids, n_pages), max(100, args.steps // 3))
-    line["warm"] = {"value": round(t_w / max(100, args.steps // 3) * 1e3 / (w.n_layers * w.batch), 4),
+    n_w = max(100, args.steps // 3)
+    t_w = reduce_max([timed(lambda: ix.select_attn(q, w.budget, out, page_ids, n_pages), n_w)], dev, world)[0]
+    line["warm"] = {"value": round(us_per_layer(t_w / n_w, w, world), 4),
                     "unit": UNIT, "note": "no L2 flush between steps"}
-    if not args.no_extras:
+    if not args.no_extras and world == 1:  # single-replica extras (not part of scaling runs)
         line["per_layer_serial"] = per_layer_serial(ice, w, keys, values, q, flush, timed, args)
         line["insert"] = insert_run(ice, synth, dev, flush, timed, args)
         line["host_kv"] = host_kv_run(ice, w, keys, values, q, flush, timed, args, st)
