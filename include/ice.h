@@ -280,6 +280,11 @@ int ice_get_info(const ice_index* ix, ice_info* info);
  *     slot token [C][P] x int32 (token of each slot of list/page id)
  *     slot key   [C][P] x uint64 (Morton key of that token)
  *   token location [max_tokens] x int32 (page id * P + slot, composite 0)
+ *   only when L = 2:
+ *     slot location [C][P] x int32 (token location of the token in each
+ *                   composite-1 slot; meaningful where the slot holds a token)
+ *     token slot    [max_tokens] x int32 (composite-1 list id * P + slot of
+ *                   each token, -1 for none)
  * Only the first n_leaf[l] leaf records and the first next_id[l] lists are
  * meaningful. Returns the byte size required when host_buf is NULL or cap is
  * too small (as a positive number), ICE_OK after a copy, or an error.

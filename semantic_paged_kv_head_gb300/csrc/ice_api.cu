@@ -243,6 +243,10 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         okc = okc && dev_alloc(ix, &v.slot_tok, (size_t)U * L * C * P) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.slot_key, (size_t)U * L * C * P) == cudaSuccess;
         okc = okc && dev_alloc(ix, &v.tok_loc, (size_t)U * v.max_tokens) == cudaSuccess;
+        if (L > 1) {
+            okc = okc && dev_alloc(ix, &v.slot_loc1, (size_t)U * C * P) == cudaSuccess;
+            okc = okc && dev_alloc(ix, &v.tok_slot1, (size_t)U * v.max_tokens) == cudaSuccess;
+        }
         unsigned char* pk = nullptr;
         unsigned char* pv = nullptr;
         const size_t pool = (size_t)U * C * P * kD * es;
@@ -274,6 +278,10 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         if (e == cudaSuccess) e = cudaMemsetAsync(v.list_cnt, 0, sizeof(int) * U * L * C, st);
         if (e == cudaSuccess)  // -1: token not placed yet
             e = cudaMemsetAsync(v.tok_loc, 0xFF, sizeof(int) * U * v.max_tokens, st);
+        if (e == cudaSuccess && L > 1)
+            e = cudaMemsetAsync(v.slot_loc1, 0xFF, sizeof(int) * U * C * P, st);
+        if (e == cudaSuccess && L > 1)  // -1: token in no composite-1 list yet
+            e = cudaMemsetAsync(v.tok_slot1, 0xFF, sizeof(int) * U * v.max_tokens, st);
         if (e == cudaSuccess && n > 0) e = build_phase2(v, keys, values, n, s, cur, st);
         scratch_free(s, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -502,7 +510,8 @@ int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap,
     const int L = ix->p.n_composite, P = ix->p.page_size;
     const long long C = ix->C;
     const int64_t per_l = C * 16 + C * 16 + C * 4 + C * P * 4 + C * P * 8;
-    const int64_t need = 16 * 8 + L * per_l + ix->v.max_tokens * 4;
+    const int64_t loc1 = L > 1 ? C * P * 4 + ix->v.max_tokens * 4 : 0;
+    const int64_t need = 16 * 8 + L * per_l + ix->v.max_tokens * 4 + loc1;
     if (!host_buf || cap < need) return need;
     cudaStream_t st = (cudaStream_t)stream;
     if (cudaStreamSynchronize(st) != cudaSuccess) return ICE_ERR_CUDA;
@@ -544,6 +553,14 @@ int64_t ice_debug_dump(ice_index* ix, int32_t unit, void* host_buf, int64_t cap,
     }
     ok = ok && cudaMemcpy(o, v.tok_loc + (long long)unit * v.max_tokens, v.max_tokens * 4,
                           cudaMemcpyDeviceToHost) == cudaSuccess;
+    o += v.max_tokens * 4;
+    if (L > 1) {
+        ok = ok && cudaMemcpy(o, v.slot_loc1 + v.loc1_base(unit), C * P * 4, cudaMemcpyDeviceToHost) ==
+                       cudaSuccess;
+        o += C * P * 4;
+        ok = ok && cudaMemcpy(o, v.tok_slot1 + (long long)unit * v.max_tokens, v.max_tokens * 4,
+                              cudaMemcpyDeviceToHost) == cudaSuccess;
+    }
     return ok ? ICE_OK : ICE_ERR_CUDA;
 }
 

@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(256) leaf_write_kernel(
     v.slot_tok[sb] = t;
     v.slot_key[sb] = m;
     if (l == 0) v.tok_loc[(long long)u * v.max_tokens + t] = leaf * v.P + slot;
+    if (l == 1) v.tok_slot1[(long long)u * v.max_tokens + t] = leaf * v.P + slot;
     if (slot == 0) {
         const int depth = tdepth[g];
         unsigned long long pm;
@@ -398,6 +399,19 @@ __global__ void __launch_bounds__(256) leaf_write_kernel(
         v.n_leaf[v.ul(u, l)] = nl;
         v.next_id[v.ul(u, l)] = nl;
     }
+}
+
+// ---------------------------------------------------------------------------
+// K3b (L = 2): the composite-1 slot of every token gets the token's page row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) loc1_kernel(IndexView v, long long n) {
+    const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // u * n + t
+    if (g >= (long long)v.U * n) return;
+    const int u = (int)(g / n);
+    const long long t = g % n;
+    const int s1 = v.tok_slot1[(long long)u * v.max_tokens + t];
+    if (s1 < 0 || (long long)s1 >= v.C * v.P) return;  // not placed (reported earlier)
+    v.slot_loc1[v.loc1_base(u) + s1] = v.tok_loc[(long long)u * v.max_tokens + t];
 }
 
 // ---------------------------------------------------------------------------
@@ -481,6 +495,10 @@ cudaError_t build_phase2(const IndexView& v, const void* keys, const void* value
     leaf_write_kernel<<<(int)((total + 255) / 256), 256, 0, st>>>(
         v, s.mk[cur], s.tk[cur], n, s.leaf_of, s.leaf_start, s.tdepth, s.nleaf);
     ICE_TRY(cudaGetLastError());
+    if (v.L > 1) {
+        loc1_kernel<<<(int)(((long long)v.U * n + 255) / 256), 256, 0, st>>>(v, n);
+        ICE_TRY(cudaGetLastError());
+    }
     const int es = v.dtype == ICE_BF16 ? 2 : 4;
     const long long vec = (long long)v.U * n * (kD * es / 16);
     const int nb = (int)((vec + 255) / 256);

@@ -19,6 +19,13 @@
 
 namespace ice {
 
+// Token tok now sits in composite-1 slot s1 (list id * P + slot): record the
+// slot and copy the token's page row (composite 0 is updated first) into it.
+__device__ __forceinline__ void place_loc1(const IndexView& v, int u, int tok, int s1) {
+    v.tok_slot1[(long long)u * v.max_tokens + tok] = s1;
+    v.slot_loc1[v.loc1_base(u) + s1] = v.tok_loc[(long long)u * v.max_tokens + tok];
+}
+
 // Shift leaf keys, records and the records' scan copies [from, N) one place to
 // the right (backwards, in chunks of one element per thread of the NT-thread block).
 template <int NT>
@@ -188,6 +195,7 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                 r2.z = ((unsigned)id << 8) | (unsigned)(cnt + 1);
                 put_leaf(v, lb0 + pos, r2);
                 if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = id * P + cnt;
+                if (l == 1) place_loc1(v, u, tok, (int)sb);
             }
             if (l == 0) {
                 T* pk = reinterpret_cast<T*>(v.page_k) + v.page_row(u, id, cnt) * kD;
@@ -246,7 +254,15 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                 const int slot = r < nl ? r : r - nl;
                 stok[(long long)dst * P + slot] = (int)e_t[j];
                 skey[(long long)dst * P + slot] = e_m[j];
-                if (l == 0) v.tok_loc[(long long)u * v.max_tokens + e_t[j]] = dst * P + slot;
+                if (l == 0) {
+                    v.tok_loc[(long long)u * v.max_tokens + e_t[j]] = dst * P + slot;
+                    // the token's composite-1 slot follows it to its new row
+                    if (v.tok_slot1 != nullptr) {
+                        const int s1 = v.tok_slot1[(long long)u * v.max_tokens + e_t[j]];
+                        if (s1 >= 0) v.slot_loc1[v.loc1_base(u) + s1] = dst * P + slot;
+                    }
+                }
+                if (l == 1) place_loc1(v, u, (int)e_t[j], dst * P + slot);
             }
             if (l == 0) {
                 for (int i = tid; i < (P + 1) * kD; i += NT) {
@@ -325,6 +341,7 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                 skey[(long long)nidl * P] = xm;
                 cntl[nidl] = 1;
                 if (l == 0) v.tok_loc[(long long)u * v.max_tokens + tok] = nidl * P;
+                if (l == 1) place_loc1(v, u, tok, nidl * P);
                 LeafKey k;
                 prefix96(xm, xt, t, k.pm, k.pt);
                 k.t = (unsigned)t;

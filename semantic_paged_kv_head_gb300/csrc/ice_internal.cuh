@@ -15,6 +15,12 @@
 //   slot_tok   [U][L][C][P] i32     token of each slot
 //   slot_key   [U][L][C][P] u64     Morton key of each slot's token
 //   tok_loc    [U][max_tokens] i32  page * P + slot of each token (composite 0)
+//   slot_loc1  [U][C][P] i32        tok_loc of the token of each composite-1 slot
+//                                   (L = 2 only), so that the selection finds a
+//                                   composite-1 candidate's row in one lookup
+//   tok_slot1  [U][max_tokens] i32  composite-1 slot (list id * P + slot) of each
+//                                   token, -1 if none: the insert updates
+//                                   slot_loc1 through it when a page splits
 //   page_k/v   [U][C][P][D] T       the physical pages (composite-0 lists)
 // The select kernel streams leaf_rec (16 B per leaf); insert is the only
 // reader of leaf_key and slot_key.
@@ -61,6 +67,8 @@ struct IndexView {
     int* slot_tok;
     unsigned long long* slot_key;
     int* tok_loc;
+    int* slot_loc1;  // nullptr when L = 1
+    int* tok_slot1;  // nullptr when L = 1
     void* page_k;
     void* page_v;
     int* status;
@@ -70,6 +78,7 @@ struct IndexView {
     __host__ __device__ long long ul(int u, int l) const { return (long long)u * L + l; }
     __host__ __device__ long long leaf_base(int u, int l) const { return ul(u, l) * C; }
     __host__ __device__ long long slot_base(int u, int l) const { return ul(u, l) * C * P; }
+    __host__ __device__ long long loc1_base(int u) const { return (long long)u * C * P; }
     __host__ __device__ long long page_row(int u, long long page, int slot) const {
         return ((long long)u * C + page) * P + slot;
     }

@@ -856,15 +856,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                 const int slot = jj - off[lo];
                 const int id = (int)(cmeta[l * n_cand + lo] >> 8);
                 if (id < C && slot < P) {
-                    // plain loads: a fused decode step has just written these lists
+                    // plain loads: a fused decode step has just written these lists.
+                    // A composite-1 slot carries its token's page row, requested
+                    // together with the token.
                     tok = v.slot_tok[v.slot_base(u, l) + (long long)id * P + slot];
                     if (l == 0) {
                         loc = id * P + slot;
                         keep = true;
-                    } else if (tok >= 0 && tok < v.max_tokens) {
-                        loc = v.tok_loc[(long long)u * v.max_tokens + tok];
-                        const int pg = loc / P;
-                        keep = loc >= 0 && pg < C && !((bm0[pg >> 5] >> (pg & 31)) & 1u);
+                    } else {
+                        loc = v.slot_loc1[v.loc1_base(u) + (long long)id * P + slot];
+                        const int pg = loc >= 0 ? loc / P : 0;
+                        keep = tok >= 0 && loc >= 0 && pg < C && !((bm0[pg >> 5] >> (pg & 31)) & 1u);
                     }
                 }
             }

@@ -350,7 +350,13 @@ class IceIndex:
                                 "lo": lo, "hi": hi,
                                 "id": (meta >> 8).astype(np.int32), "cnt": (meta & 0xFF).astype(np.int32),
                                 "list_cnt": cnt.copy(), "slot_tok": stok.copy(), "slot_key": skey.copy()})
-        out["tok_loc"] = buf[o:o + 4 * self.info().max_tokens].view(np.int32).copy()
+        mt = self.info().max_tokens
+        out["tok_loc"] = buf[o:o + 4 * mt].view(np.int32).copy()
+        o += 4 * mt
+        if L > 1:
+            out["slot_loc1"] = buf[o:o + C * P * 4].view(np.int32).reshape(C, P).copy()
+            o += C * P * 4
+            out["tok_slot1"] = buf[o:o + 4 * mt].view(np.int32).copy()
         return out
 
     def page(self, unit: int, page_id: int, stream=None):

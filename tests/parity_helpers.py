@@ -60,6 +60,9 @@ def compare_index(gdump, orc, unit_label=""):
             assert np.array_equal(comp["slot_key"][lid, :c], mk[toks]), (unit_label, l, i)
             if l == 0:
                 assert np.array_equal(tok_loc[toks], lid * P + np.arange(c)), (unit_label, i)
+            if l == 1:  # composite-1 slots carry their token's page row, both ways
+                assert np.array_equal(gdump["slot_loc1"][lid, :c], tok_loc[toks]), (unit_label, i)
+                assert np.array_equal(gdump["tok_slot1"][toks], lid * P + np.arange(c)), (unit_label, i)
 
 
 def compare_pages(gix, w, keys, values, gdump, u, max_pages=8):
