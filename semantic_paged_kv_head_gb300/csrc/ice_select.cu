@@ -112,19 +112,20 @@ __device__ __forceinline__ unsigned smem_u32(const void* p) {
 
 // Returns true once phase `parity` of the mbarrier has completed, false if it
 // has not within kWaitNs of wall time (the caller then reports a timeout).
+// try_wait suspends the thread until the phase completes or a hardware time
+// limit passes, so a waiting warp resumes as soon as the copies have landed.
 __device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity) {
     const unsigned long long t0 = global_ns();
-    for (int i = 0;; ++i) {
+    for (;;) {
         unsigned done;
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
             " selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
-        if ((i & 15) == 15 && global_ns() - t0 > kWaitNs) return false;
-        __nanosleep(i < 64 ? 20 : 200);
+        if (global_ns() - t0 > kWaitNs) return false;
     }
 }
 
@@ -385,21 +386,30 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
 #pragma unroll
                     for (int z = 0; z < 4; ++z) kx[k + z] = x[z];
                 }
-                float s = 0.0f;
+                // even and odd dimensions in the two halves of packed fp32 pairs
+                float2 s2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int k = 0; k < DPL; ++k) s = fmaf(qa[k], kx[k], s);
+                for (int k = 0; k < DPL; k += 2)
+                    s2 = __ffma2_rn(make_float2(qa[k], qa[k + 1]), make_float2(kx[k], kx[k + 1]), s2);
+                float s = s2.x + s2.y;
 #pragma unroll
                 for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 const float mn = fmaxf(m, s);
                 const float corr = exp2f(m - mn);
                 const float p = exp2f(s - mn);
                 lsum = lsum * corr + p;
+                const float2 c2 = make_float2(corr, corr), p2 = make_float2(p, p);
 #pragma unroll
                 for (int k = 0; k < DPL; k += 4) {
                     float x[4];
                     load4(sv + (size_t)j * kD + g * DPL + k, x);
 #pragma unroll
-                    for (int z = 0; z < 4; ++z) acc[k + z] = fmaf(p, x[z], acc[k + z] * corr);
+                    for (int z = 0; z < 4; z += 2) {
+                        const float2 a = __ffma2_rn(p2, make_float2(x[z], x[z + 1]),
+                                                    __fmul2_rn(make_float2(acc[k + z], acc[k + z + 1]), c2));
+                        acc[k + z] = a.x;
+                        acc[k + z + 1] = a.y;
+                    }
                 }
                 m = mn;
             }
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int32_t* __restrict__ stats, T* __restrict__ attn_out, const int32_t* __restrict__ reselect,
     int head_div, const T* __restrict__ knew, const T* __restrict__ vnew) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(16) float s_qsel[kD];
+    __shared__ __align__(16) float2 s_qp[kD / 2];  // (q_sel[e], q_sel[e + 64]), e < 64
     __shared__ int s_qcode[kMaxL][kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
     __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL];
@@ -608,7 +618,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         }
         if (warp == 0) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) s_qsel[4 * lane + k] = qs[k];
+            for (int k = 0; k < 4; ++k) {
+                const int e = 4 * lane + k;
+                if (e < kD / 2) s_qp[e].x = qs[k];
+                else s_qp[e - kD / 2].y = qs[k];
+            }
             if (FUSED) {  // the query rows, for the attention tail
                 float* qf = reinterpret_cast<float*>(smem + lay.qf);
 #pragma unroll
@@ -948,13 +962,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                     load_chunk<T>(rowp + 16 * (c0 ^ sw), x0);
                     load_chunk<T>(rowp + 16 * (c1 ^ sw), x1);
                     const int o0 = e0 % EPC, o1 = e1 % EPC;
-                    float a = 0.0f, b = 0.0f;
+                    // the partials of lanes l and l + 16 (elements e0 + i and
+                    // e1 + i = e0 + 64 + i) as the two halves of a packed pair
+                    float2 ab = make_float2(0.0f, 0.0f);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        a = __fmaf_rn(s_qsel[e0 + i], x0[o0 + i], a);
-                        b = __fmaf_rn(s_qsel[e1 + i], x1[o1 + i], b);
-                    }
-                    s16[j] = __fadd_rn(a, b);
+                    for (int i = 0; i < 4; ++i)
+                        ab = __ffma2_rn(s_qp[e0 + i], make_float2(x0[o0 + i], x1[o1 + i]), ab);
+                    s16[j] = __fadd_rn(ab.x, ab.y);
                 }
                 // level 8: l + 8 is owned entry j + 4; level 4: l + 4 is entry j + 2
 #pragma unroll
