@@ -139,6 +139,19 @@ __device__ __forceinline__ __half2 bytes_to_h2(unsigned x, unsigned s) {
     return h;
 }
 
+// 0xFF in byte k of the result where bit k of the 4-bit mask m is set.
+__device__ __forceinline__ unsigned nibble_bytes(unsigned m) {
+    return ((m * 0x00204081u) & 0x01010101u) * 0xFFu;
+}
+
+// Word k (0..7) of eight registers, without indexing local memory.
+__device__ __forceinline__ unsigned byte_word(const unsigned (&w)[8], int k) {
+    const unsigned a = (k & 1) ? w[1] : w[0], b = (k & 1) ? w[3] : w[2];
+    const unsigned c = (k & 1) ? w[5] : w[4], d = (k & 1) ? w[7] : w[6];
+    const unsigned ab = (k & 2) ? b : a, cd = (k & 2) ? d : c;
+    return (k & 4) ? cd : ab;
+}
+
 // Widths hi - lo of the 8 code intervals of a prefix of length t, as fp16x2.
 __device__ __forceinline__ void cell_widths(int t, __half2 (&w)[4]) {
 #pragma unroll
@@ -781,8 +794,18 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         for (int w0 = 0; w0 < nwords && run < need; w0 += 32) {
             const int wi = w0 + lane;
             const unsigned bits = wi < nwords ? tb[wi] : 0u;
-            int tot = 0;
-            for (unsigned b = bits; b; b &= b - 1u) tot += cl[wi * 32 + __ffs(b) - 1];
+            // the count bytes of the word's 32 leaves, in registers
+            uint4 ca = make_uint4(0u, 0u, 0u, 0u), cb = ca;
+            if (bits) {
+                ca = *reinterpret_cast<const uint4*>(cl + wi * 32);
+                cb = *reinterpret_cast<const uint4*>(cl + wi * 32 + 16);
+            }
+            const unsigned cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+            unsigned tsum = 0u;  // tokens of the word's ties: count bytes under the tie mask
+#pragma unroll
+            for (int qd = 0; qd < 8; ++qd)
+                tsum = __dp4a(cw[qd] & nibble_bytes((bits >> (4 * qd)) & 0xFu), 0x01010101u, tsum);
+            const int tot = (int)tsum;
             int inc = tot;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -791,11 +814,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             }
             int acc = run + inc - tot, mine = 0;
             unsigned take = 0u;
-            for (unsigned b = bits; b && acc < need; b &= b - 1u) {
-                const int bit = __ffs(b) - 1;
-                take |= 1u << bit;
-                acc += cl[wi * 32 + bit];
-                ++mine;
+            if (acc + tot <= need) {  // every tie of the word is taken (counts are >= 1)
+                take = bits;
+                mine = __popc(bits);
+            } else {  // the word where the need is reached (or none is taken)
+                for (unsigned b = bits; b && acc < need; b &= b - 1u) {
+                    const int bit = __ffs(b) - 1;
+                    take |= 1u << bit;
+                    acc += (int)((byte_word(cw, bit >> 2) >> (8 * (bit & 3))) & 0xFFu);
+                    ++mine;
+                }
             }
             int tinc = mine;
 #pragma unroll
