@@ -676,26 +676,42 @@ def run_ice(args):
     ms_step = min(ms_fused, ms_sep)
     ix.check()
 
-    # end to end through the public API: pinned host q in, host out back, every step
+    # end to end through the public API with host buffers, every step: q in page-locked
+    # host memory, the result back in page-locked host memory. (a) the call reads q and
+    # writes out in place over the CPU-GPU link; (b) explicit copies around the call.
     q_host = q.cpu().pin_memory()
     out_host = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     q_in = torch.empty_like(q)
     n_e2e = max(10, args.steps // 4)
-    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
-    for _ in range(3):
+
+    def e2e_loop(step):
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        for k in range(n_e2e):
+            flush.zero_()
+            ev2[k][0].record(stream)
+            step()
+            ev2[k][1].record(stream)
+        torch.cuda.synchronize()
+        return reduce_max([sum(e[0].elapsed_time(e[1]) for e in ev2) / n_e2e], dev, world)[0]
+
+    def step_in_place():
+        ix.select_attn(q_host, w.budget, out_host, page_ids, n_pages)
+
+    def step_copies():
         q_in.copy_(q_host, non_blocking=True)
         ix.select_attn(q_in, w.budget, out, page_ids, n_pages)
         out_host.copy_(out, non_blocking=True)
+
+    ms_e2e = e2e_loop(step_in_place)
     torch.cuda.synchronize()
-    for k in range(n_e2e):
-        flush.zero_()
-        ev2[k][0].record(stream)
-        q_in.copy_(q_host, non_blocking=True)
-        ix.select_attn(q_in, w.budget, out, page_ids, n_pages)
-        out_host.copy_(out, non_blocking=True)
-        ev2[k][1].record(stream)
+    ref_out = out_host.clone()
+    ms_e2e_copies = e2e_loop(step_copies)
     torch.cuda.synchronize()
-    ms_e2e = reduce_max([sum(e[0].elapsed_time(e[1]) for e in ev2) / n_e2e], dev, world)[0]
+    if not torch.equal(ref_out, out_host):
+        raise RuntimeError("in-place host-buffer call and the copied call disagree")
 
     peak, peak_kind = _peaks()
     sel_gbs = sel_bytes / (ms_sel * 1e-3) / 1e9
@@ -736,7 +752,12 @@ def run_ice(args):
                      "traffic": _traffic_for(dom, src), "algorithmic_bytes": int(dom_bytes)},
         "e2e": {"value": round(us_per_layer(ms_e2e, w, world), 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(q.numel() * q.element_size()),
-                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "how": ("ice_select_attn on page-locked host q and out: the kernel reads q and "
+                        "writes the result over the CPU-GPU link; L2 flushed before each step"),
+                "with_copies": {"value": round(us_per_layer(ms_e2e_copies, w, world), 4),
+                                "unit": UNIT, "how": "cudaMemcpyAsync of q in and out back "
+                                "around ice_select_attn on device buffers"}},
         "gpu_launches": 4 * n_steps,
         "timing": ("device time of back-to-back loops (host runs ahead), each step after an L2 "
                    "flush: step = [flush+select_attn] - [flush]; separate calls: select = "

@@ -4,8 +4,8 @@
  * IceCache ("IceCache", arXiv 2604.10539) keeps the KV cache of each attention
  * head in pages that are the leaves of a DCI-tree built over the keys in a
  * transformed key space (Figure 2 step 1; Figure 3 maps tree nodes to physical
- * pages). Generated tokens are inserted without a rebuild (abstract:
- * "dynamically updatable"). At each decode step a prioritised tree search
+ * pages). Generated tokens are inserted without a rebuild (the abstract
+ * describes the structure as updatable in place). At each decode step a prioritised tree search
  * finds the query's top keys, the pages holding them are selected (Figure 2
  * steps 2-3), and attention runs over every token of those pages.
  *
@@ -19,6 +19,17 @@
  * Conventions for every call:
  *  - Pointers named as device pointers must point to device memory of the
  *    current CUDA device; the caller owns them. Host pointers are named so.
+ *  - The calls that run a decode step (ice_insert, ice_select,
+ *    ice_select_attn, ice_select_attn_reuse, ice_decode_step,
+ *    ice_select_heads, ice_sparse_attn) also take page-locked host memory
+ *    (cudaHostAlloc, cudaMallocHost, cudaHostRegister) for any of their
+ *    device buffers: the kernels read and write it in place over the CPU-GPU
+ *    link, with no staging copy. Each buffer pointer is checked before
+ *    anything is launched, and memory the GPU cannot address (pageable host
+ *    memory, another GPU's memory) gives ICE_ERR_INVALID_ARG. While `stream`
+ *    is being captured into a CUDA graph the pointers are not checked (the
+ *    eager calls before a capture check the same buffers). ice_build and
+ *    ice_key_codes_noalloc take device memory only.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Calls enqueue work on it and return without waiting, except where stated.
  *  - Return value: ICE_OK (0) or a negative ICE_ERR_* code. Argument errors
@@ -44,7 +55,7 @@ extern "C" {
 #define ICE_ERR_INVALID_ARG (-1) /* bad argument; nothing was launched          */
 #define ICE_ERR_CAPACITY (-2)    /* token / page / leaf capacity exhausted        */
 #define ICE_ERR_CUDA (-3)        /* a CUDA runtime call failed                    */
-#define ICE_ERR_TIMEOUT (-4)     /* reserved: a bounded device wait ran out       */
+#define ICE_ERR_TIMEOUT (-4)     /* a bounded device wait ran out (device status) */
 #define ICE_ERR_BOUNDS (-5)      /* a page id or count given to a kernel is bad   */
 #define ICE_ERR_UNSUPPORTED (-6) /* valid request this build does not implement  */
 

@@ -71,6 +71,40 @@ int check_params(const ice_params* p) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// The address a kernel dereferences for a caller's buffer: device memory of the
+// index's GPU (or managed memory) as given, page-locked host memory through its
+// device mapping (the kernels then read or write it over the CPU-GPU link).
+// False for anything the GPU cannot address (pageable host memory, memory of
+// another GPU, a bad pointer): the call is refused before any launch. While
+// `stream` is being captured into a CUDA graph the pointer is taken as given
+// (no driver query is made during a capture; the eager calls that precede a
+// capture check the same buffers).
+bool kernel_addr(const ice_index* ix, const void* p, void* stream, const void** out) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing((cudaStream_t)stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (cs != cudaStreamCaptureStatusNone) {
+        *out = p;
+        return true;
+    }
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if ((a.type == cudaMemoryTypeDevice && a.device == ix->device) || a.type == cudaMemoryTypeManaged) {
+        *out = p;
+        return true;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+        *out = a.devicePointer;
+        return true;
+    }
+    return false;
+}
+
 template <typename T>
 cudaError_t dev_alloc(ice_index* ix, T** out, size_t count) {
     void* p = nullptr;
@@ -107,6 +141,16 @@ void free_all(ice_index* ix) {
 }
 
 }  // namespace
+
+// Replaces a non-null buffer argument by its kernel address, or refuses the call.
+#define ICE_KERNEL_ADDR(ptr)                                                   \
+    do {                                                                       \
+        if ((ptr) != nullptr) {                                                \
+            const void* d_ = nullptr;                                          \
+            if (!kernel_addr(ix, (ptr), stream, &d_)) return ICE_ERR_INVALID_ARG; \
+            (ptr) = (decltype(ptr))(d_);                                       \
+        }                                                                      \
+    } while (0)
 
 extern "C" {
 
@@ -299,6 +343,8 @@ fail:
 int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
     ApiRange range_("ice_insert");
     if (!ix || !k || !v || !aligned16(k) || !aligned16(v)) return ICE_ERR_INVALID_ARG;
+    ICE_KERNEL_ADDR(k);
+    ICE_KERNEL_ADDR(v);
     if (ix->n_tok >= ix->v.max_tokens) return ICE_ERR_CAPACITY;
     cudaError_t e = launch_insert(ix->v, k, v, (cudaStream_t)stream);
     if (e != cudaSuccess) return ICE_ERR_CUDA;
@@ -327,6 +373,11 @@ static int select_common(ice_index* ix, const void* q, int32_t token_budget, int
                          const int32_t* reselect = nullptr) {
     const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
     if (a != ICE_OK) return a;
+    ICE_KERNEL_ADDR(q);
+    ICE_KERNEL_ADDR(page_ids);
+    ICE_KERNEL_ADDR(n_pages);
+    ICE_KERNEL_ADDR(stats);
+    ICE_KERNEL_ADDR(out);
     const int P = ix->p.page_size;
     const int n_sel = token_budget / P;
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
@@ -363,6 +414,11 @@ int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, in
     if (!ix || !out || r < 0) return ICE_ERR_INVALID_ARG;
     const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
     if (a != ICE_OK) return a;
+    ICE_KERNEL_ADDR(q);
+    ICE_KERNEL_ADDR(page_ids);
+    ICE_KERNEL_ADDR(n_pages);
+    ICE_KERNEL_ADDR(reselected);
+    ICE_KERNEL_ADDR(out);
     cudaStream_t st = (cudaStream_t)stream;
     const int U = ix->U;
     if (!ix->reuse_age) {
@@ -392,8 +448,8 @@ int ice_select_attn_reuse(ice_index* ix, const void* q, int32_t token_budget, in
                             ix->reuse_flag);
     }
     if (res == ICE_OK && reselected &&
-        cudaMemcpyAsync(reselected, ix->reuse_flag, sizeof(int32_t) * U, cudaMemcpyDeviceToDevice,
-                        st) != cudaSuccess)
+        cudaMemcpyAsync(reselected, ix->reuse_flag, sizeof(int32_t) * U, cudaMemcpyDefault, st) !=
+            cudaSuccess)
         return ICE_ERR_CUDA;
     return res;
 }
@@ -407,6 +463,12 @@ int ice_decode_step(ice_index* ix, const void* k, const void* v, const void* q,
     if (a != ICE_OK) return a;
     if (!k || !v || !aligned16(k) || !aligned16(v)) return ICE_ERR_INVALID_ARG;
     if (ix->n_tok >= ix->v.max_tokens) return ICE_ERR_CAPACITY;
+    ICE_KERNEL_ADDR(k);
+    ICE_KERNEL_ADDR(v);
+    ICE_KERNEL_ADDR(q);
+    ICE_KERNEL_ADDR(page_ids);
+    ICE_KERNEL_ADDR(n_pages);
+    ICE_KERNEL_ADDR(out);
     const int P = ix->p.page_size;
     const int n_sel = token_budget / P;
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
@@ -431,6 +493,11 @@ int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t
     const int a = select_args(ix, q, token_budget, page_ids, n_pages, nullptr);
     if (a != ICE_OK) return a;
     if (!head_page_ids || !head_n_pages) return ICE_ERR_INVALID_ARG;
+    ICE_KERNEL_ADDR(q);
+    ICE_KERNEL_ADDR(head_page_ids);
+    ICE_KERNEL_ADDR(head_n_pages);
+    ICE_KERNEL_ADDR(page_ids);
+    ICE_KERNEL_ADDR(n_pages);
     const int n_sel = token_budget / ix->p.page_size;
     if (ix->G * n_sel > 512) return ICE_ERR_UNSUPPORTED;  // the attention's page-list bound
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
@@ -457,6 +524,10 @@ int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const
     if (!ix || !q || !page_ids || !n_pages || !out || !aligned16(q) || !aligned16(out))
         return ICE_ERR_INVALID_ARG;
     if (page_stride < 1 || page_stride > 512) return ICE_ERR_INVALID_ARG;
+    ICE_KERNEL_ADDR(q);
+    ICE_KERNEL_ADDR(page_ids);
+    ICE_KERNEL_ADDR(n_pages);
+    ICE_KERNEL_ADDR(out);
     cudaError_t e = launch_attn(ix->v, q, page_ids, n_pages, page_stride, out, (cudaStream_t)stream);
     return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
 }

@@ -130,14 +130,25 @@ def _stream(stream=None) -> int:
     return s.cuda_stream
 
 
-def _dev_ptr(t: torch.Tensor, dtype=None, name="tensor") -> int:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _dev_ptr(t: torch.Tensor, dtype=None, name="tensor", host_ok=True) -> int:
+    """Address of a buffer argument: a CUDA tensor or, where the call allows it,
+    a page-locked CPU tensor that the kernels read or write in place."""
+    ok = isinstance(t, torch.Tensor) and (
+        t.is_cuda or (host_ok and t.device.type == "cpu" and t.is_pinned()))
+    if not ok:
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or page-locked CPU tensor" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
+
+
+def _like(t: torch.Tensor) -> torch.Tensor:
+    """An uninitialised buffer like t, page-locked when t is a CPU tensor."""
+    if t.is_cuda:
+        return torch.empty_like(t)
+    return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
 
 
 def _code(dtype: torch.dtype) -> int:
@@ -172,8 +183,8 @@ class IceIndex:
                        dtype=_code(keys.dtype), max_tokens=n if max_tokens is None else max_tokens,
                        seed=seed, kv_location=KV_HOST if kv_host else KV_DEVICE, dir_kind=dir_kind)
         h = ctypes.c_void_p()
-        kp = _dev_ptr(keys, values.dtype, "keys") if n else 0
-        vp = _dev_ptr(values, keys.dtype, "values") if n else 0
+        kp = _dev_ptr(keys, values.dtype, "keys", host_ok=False) if n else 0
+        vp = _dev_ptr(values, keys.dtype, "values", host_ok=False) if n else 0
         _check(_lib.ice_build(ctypes.byref(p), kp, vp, n, _stream(stream), ctypes.byref(h)),
                "ice_build")
         return cls(h.value, p, keys.dtype)
@@ -188,7 +199,7 @@ class IceIndex:
         """ice_select; returns (page_ids [units, n_sel] int32, n_pages [units] int32)."""
         U = self.n_units
         n_sel = token_budget // self.params.page_size
-        dev = q.device
+        dev = q.device if q.is_cuda else torch.device("cuda")  # q may be page-locked host memory
         if page_ids is None:
             page_ids = torch.empty((U, n_sel), dtype=torch.int32, device=dev)
         if n_pages is None:
@@ -206,13 +217,13 @@ class IceIndex:
         """ice_select_attn; returns (out, page_ids, n_pages)."""
         U = self.n_units
         n_sel = token_budget // self.params.page_size
-        dev = q.device
+        dev = q.device if q.is_cuda else torch.device("cuda")  # q may be page-locked host memory
         if page_ids is None:
             page_ids = torch.empty((U, n_sel), dtype=torch.int32, device=dev)
         if n_pages is None:
             n_pages = torch.empty((U,), dtype=torch.int32, device=dev)
         if out is None:
-            out = torch.empty_like(q)
+            out = _like(q)
         sp = _dev_ptr(stats, torch.int32, "stats") if stats is not None else None
         _check(_lib.ice_select_attn(self._h, _dev_ptr(q, self.dtype, "q"), int(token_budget),
                                     _dev_ptr(page_ids, torch.int32, "page_ids"),
@@ -227,7 +238,7 @@ class IceIndex:
         """ice_select_attn_reuse; page_ids/n_pages carry the selection between calls
         (pass the same tensors every step). Returns (out, page_ids, n_pages)."""
         if out is None:
-            out = torch.empty_like(q)
+            out = _like(q)
         _check(_lib.ice_select_attn_reuse(self._h, _dev_ptr(q, self.dtype, "q"), int(token_budget),
                                           int(r), _dev_ptr(page_ids, torch.int32, "page_ids"),
                                           _dev_ptr(n_pages, torch.int32, "n_pages"),
@@ -259,7 +270,7 @@ class IceIndex:
         head_page_ids [units, G, n_sel], head_n_pages [units, G])."""
         U, G = self.n_units, self.params.n_q_heads // self.params.n_kv_heads
         n_sel = token_budget // self.params.page_size
-        dev = q.device
+        dev = q.device if q.is_cuda else torch.device("cuda")
         hid = torch.empty((U, G, n_sel), dtype=torch.int32, device=dev)
         hn = torch.empty((U, G), dtype=torch.int32, device=dev)
         ids = torch.empty((U, G * n_sel), dtype=torch.int32, device=dev)
@@ -276,7 +287,7 @@ class IceIndex:
                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
         """ice_sparse_attn; returns out shaped like q."""
         if out is None:
-            out = torch.empty_like(q)
+            out = _like(q)
         _check(_lib.ice_sparse_attn(self._h, _dev_ptr(q, self.dtype, "q"),
                                     _dev_ptr(page_ids, torch.int32, "page_ids"),
                                     _dev_ptr(n_pages, torch.int32, "n_pages"),
@@ -385,9 +396,10 @@ def key_codes_noalloc(keys: torch.Tensor, *, n_composite: int = 2, n_proj: int =
         morton_out = torch.empty((n_composite, U, n), dtype=torch.int64, device=keys.device)
     if e_out is None:
         e_out = torch.empty((U,), dtype=torch.int32, device=keys.device)
-    _check(_lib.ice_key_codes_noalloc(ctypes.byref(p), _dev_ptr(keys, None, "keys"), n,
-                                      _dev_ptr(morton_out, torch.int64, "morton_out"),
-                                      _dev_ptr(e_out, torch.int32, "e_out"), _stream(stream)),
+    _check(_lib.ice_key_codes_noalloc(ctypes.byref(p), _dev_ptr(keys, None, "keys", host_ok=False), n,
+                                      _dev_ptr(morton_out, torch.int64, "morton_out", host_ok=False),
+                                      _dev_ptr(e_out, torch.int32, "e_out", host_ok=False),
+                                      _stream(stream)),
            "ice_key_codes_noalloc")
     return morton_out, e_out
 
