@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import tempfile
 import statistics
 import subprocess
 import sys
@@ -72,7 +73,9 @@ class ClockSampler:
 
     def __init__(self, device_index=0, out_path=None):
         self.proc = None
-        self.path = out_path or os.path.join(ROOT, "gpurun_out", "clocks.csv")
+        # ICE_BENCH_CLOCKS names a file to keep the raw samples in
+        self.path = out_path or os.environ.get("ICE_BENCH_CLOCKS") or os.path.join(
+            tempfile.gettempdir(), f"ice_bench_clocks_{os.getpid()}.csv")
         self.dev = device_index
 
     def __enter__(self):

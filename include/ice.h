@@ -57,7 +57,7 @@ extern "C" {
 #define ICE_ERR_CUDA (-3)        /* a CUDA runtime call failed                    */
 #define ICE_ERR_TIMEOUT (-4)     /* a bounded device wait ran out (device status) */
 #define ICE_ERR_BOUNDS (-5)      /* a page id or count given to a kernel is bad   */
-#define ICE_ERR_UNSUPPORTED (-6) /* valid request this build does not implement  */
+#define ICE_ERR_UNSUPPORTED (-6) /* valid request the library does not implement */
 
 /* ---- element types ----------------------------------------------------- */
 #define ICE_F32 0
@@ -67,7 +67,7 @@ typedef struct ice_index ice_index; /* opaque; owns the page pool and the index 
 
 /* Shape and method parameters of an index. */
 typedef struct ice_params {
-    int32_t d;           /* head dimension; this build supports 128                  */
+    int32_t d;           /* head dimension; the kernels support 128                  */
     int32_t n_kv_heads;  /* KV heads per layer (>= 1)                                */
     int32_t n_q_heads;   /* query heads per layer, a multiple of n_kv_heads; G <= 8  */
     int32_t n_layers;    /* layers (>= 1)                                            */
@@ -82,7 +82,7 @@ typedef struct ice_params {
     int32_t kv_location; /* ICE_KV_DEVICE: the page pool in device memory (HBM);     */
                          /* ICE_KV_HOST: in pinned host memory mapped into the       */
                          /* GPU's address space, read by the kernels over the        */
-                         /* CPU-GPU link (the pages' offloaded KV tier)              */
+                         /* CPU-GPU link (the paper's offloaded KV tier)             */
     int32_t dir_kind;    /* projection directions: ICE_DIR_RADEMACHER (+-1/16 per   */
                          /* component, one splitmix64 draw each) or ICE_DIR_GAUSSIAN */
                          /* (z/16, z from the Box-Muller transform of two draws)     */
@@ -121,8 +121,8 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
               void* stream, ice_index** out);
 
 /*
- * ice_insert - add one generated token to every unit without a rebuild
- * (abstract: "dynamically updatable").
+ * ice_insert - add one generated token to every unit without a rebuild (the
+ * abstract's in-place update of the index).
  *
  * k, v: device, [batch][n_layers][n_kv_heads][d], dtype. The token gets index
  * n (the unit's current token count). Its key is transformed with the frozen
@@ -174,8 +174,8 @@ int ice_select_attn(ice_index* ix, const void* q, int32_t token_budget, int32_t*
 
 /*
  * ice_select_attn_reuse - ice_select_attn that keeps a unit's pages across
- * calls ("IceCache" paper, the IceCache(r) variant, whose mechanism the pages
- * leave open). Reading: a unit reuses the pages of its last selection for up
+ * calls ("IceCache" paper, the IceCache(r) variant, whose mechanism the paper
+ * leaves open). Reading: a unit reuses the pages of its last selection for up
  * to r further calls while its query codes (the 8-bit codes of the group
  * query on every projection direction, which the selection computes first)
  * are exactly those of the call that selected the pages. Any changed code, r
@@ -323,7 +323,7 @@ int ice_debug_set_flags(ice_index* ix, int32_t flags);
  * ice_key_codes_noalloc - the key transform of ice_build (squared norms, the
  * frozen scale exponent per unit, the 8-bit codes of every key on the L x 8
  * random directions, their Morton interleave) without allocating any memory.
- * The pages have no counterpart of this call; it exists for callers that
+ * The paper has no counterpart of this call; it exists for callers that
  * cannot allocate device memory while they run (a process whose memory is all
  * handed to its own pool allocator, or a latency-critical loop where a
  * cudaMalloc, which can synchronise the device, is not acceptable).

@@ -1,10 +1,11 @@
 // IceCache decode-time path: CPU ORACLE (test infrastructure only).
 //
 // A plain, slow, single-threaded statement of what the GPU library computes,
-// written from the IceCache pages ("IceCache", arXiv 2604.10539): the DCI-tree
-// page index built at prefill (Figure 2 step 1, Figure 3), dynamic insertion
-// of generated tokens without a rebuild (abstract: "hierarchical, dynamically
-// updatable data structure"), the P-DCI prioritised query that finds the pages
+// written from the IceCache paper ("IceCache", arXiv 2604.10539) and its blog
+// post: the DCI-tree page index built at prefill (Figure 2 step 1, Figure 3),
+// dynamic insertion of generated tokens without a rebuild (the abstract's
+// hierarchical structure that is updated in place), the P-DCI prioritised
+// query that finds the pages
 // holding the query's top keys (Figure 2 steps 2-3), and sparse GQA attention
 // over every token of the selected pages (Figure 2 step 3).
 //
@@ -13,8 +14,8 @@
 // with -O2 -ffp-contract=off so that every float operation written here is the
 // one that runs (no fused multiply-add except where std::fma is spelled out).
 //
-// Readings where the pages are silent (each one is listed with its reason in
-// the design notes of the repository):
+// Readings where the paper and the blog are silent (each one is listed with its
+// reason in the design notes of the repository):
 //  * transformed key space: keys are scaled by 2^-e, c = 2^e the smallest power
 //    of two with c^2 >= max ||k||^2 (frozen at build), and augmented with
 //    sqrt(1 - ||k||^2 / c^2), so that the nearest neighbour of the normalised

@@ -292,7 +292,7 @@ class OracleIndex:
 
 class ReuseOracle:
     """Selection reuse across decode steps ("IceCache" paper, the IceCache(r)
-    variant; the pages name it but give no mechanism).
+    variant; the paper names it but gives no mechanism).
 
     Reading: a unit keeps the pages of its last selection for up to r further
     steps while its query codes (``OracleIndex.query``: the 8-bit codes of the

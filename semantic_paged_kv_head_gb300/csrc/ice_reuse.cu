@@ -1,5 +1,5 @@
 // Reuse of a unit's page selection across decode steps ("IceCache" paper:
-// the IceCache(r) variant, whose mechanism the pages do not describe).
+// the IceCache(r) variant, whose mechanism the paper does not describe).
 //
 // Reading taken here: a unit keeps the pages of its last selection for up to
 // r further steps while the query codes (the 8-bit codes of the group query
