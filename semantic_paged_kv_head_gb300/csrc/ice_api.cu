@@ -251,7 +251,8 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
                 scratch_free(s, st);
                 goto fail;
             }
-            e = build_phase1(params->dtype, keys, U, L, P, n, d_dirs, d_e, s, st, &cur);
+            e = build_phase1(params->dtype, keys, U, L, P, n, d_dirs,
+                             params->dir_kind == ICE_DIR_RADEMACHER, d_e, s, st, &cur);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(nleaf.data(), s.nleaf, sizeof(int) * L * U,
                                     cudaMemcpyDeviceToHost, st);

@@ -151,6 +151,150 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// K1c: the same codes with the projection on tensor cores, for bf16 keys and
+// +-1/16 directions (both exact in bf16; bf16 x bf16 products are exact in
+// fp32). mma.sync m16n8k16 (bf16 in, fp32 accumulate) gives P = K U^T for 16
+// tokens per warp; the tensor cores add the products in an order of their own,
+// so a value whose (p + 1) * 128 lies within kCodeGuard of an integer (a code
+// boundary) is recomputed with the fixed-order dot of K1b, and every code
+// equals K1b's. The k index of each 16-wide step is permuted so that a lane's
+// A and B fragments for two steps are one 16-byte load: logical k of step
+// 2m + s maps to dimension 32m + 8(k mod 8 div 2) + 4s + 2(k div 8) + k mod 2,
+// the same for keys and directions, which leaves the dot unchanged.
+// ---------------------------------------------------------------------------
+constexpr int kPmWarps = 8;
+constexpr int kPmTok = kPmWarps * 16;  // tokens per block
+constexpr float kCodeGuard = 1.0f / 256.0f;
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], unsigned a0, unsigned a1, unsigned a2,
+                                               unsigned a3, unsigned b0, unsigned b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The code of key row krow (bf16, scaled by sc) on direction ud with the
+// fixed-order dot of K1b, evaluated by one warp: lane l forms the partial of
+// elements 4l..4l+3 and the partials are added pairwise over lanes l and
+// l + 16, 8, 4, 2, 1 (the order of K1b's per-thread tree). Every lane returns it.
+__device__ __forceinline__ int exact_code_warp(const __nv_bfloat16* krow, float sc, const float* ud,
+                                              float tail, int lane) {
+    float x[4];
+    load4_nc(krow + 4 * lane, x);
+    const float4 w = __ldg(reinterpret_cast<const float4*>(ud + 4 * lane));
+    float s = 0.0f;
+    s = __fmaf_rn(w.x, __fmul_rn(x[0], sc), s);
+    s = __fmaf_rn(w.y, __fmul_rn(x[1], sc), s);
+    s = __fmaf_rn(w.z, __fmul_rn(x[2], sc), s);
+    s = __fmaf_rn(w.w, __fmul_rn(x[3], sc), s);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+    return quantise_code(__fmaf_rn(ud[kD], tail, s));
+}
+
+// bf16 pair (lo, hi) of two fp32 values that are exact in bf16.
+__device__ __forceinline__ unsigned bf16_pair(float lo, float hi) {
+    return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+}
+
+__global__ void __launch_bounds__(kPmWarps * 32) project_mma_kernel(
+    const __nv_bfloat16* __restrict__ keys, const float* __restrict__ nrm2,
+    const int* __restrict__ e_unit, const float* __restrict__ dirs, int L, long long n,
+    int tiles_per_unit, unsigned long long* __restrict__ mk_out, int* __restrict__ tok_out, int U) {
+    __shared__ float tail_s[kPmTok];
+    __shared__ unsigned char codes[kPmTok][kMaxL * kM];
+    __shared__ unsigned short queue[kPmTok * kMaxL * kM];  // (token << 4 | direction) to recompute
+    __shared__ int qn;
+    const int ndir = L * kM;
+    const int u = blockIdx.x / tiles_per_unit;
+    const long long t0 = (long long)(blockIdx.x % tiles_per_unit) * kPmTok;
+    const int e = e_unit[u];
+    const float sc = ldexpf(1.0f, -e), sc2 = ldexpf(1.0f, -2 * e);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const __nv_bfloat16* ku = keys + (long long)u * n * kD;
+    if (tid == 0) qn = 0;
+
+    // warp w: tokens 16w .. 16w + 15 of the block; lane (r, q) = (lane / 4, lane % 4)
+    const int r = lane >> 2, q = lane & 3;
+    const int la = 16 * warp + r, lb = la + 8;  // the lane's two token rows (block-local)
+    const long long ta = t0 + la, tb = t0 + lb;
+    float tail[2];
+#pragma unroll
+    for (int z = 0; z < 2; ++z) {
+        const long long t = z ? tb : ta;
+        float rr = 0.0f;
+        if (t < n) {
+            rr = __fsub_rn(1.0f, __fmul_rn(nrm2[(long long)u * n + t], sc2));
+            rr = rr > 0.0f ? rr : 0.0f;
+        }
+        tail[z] = __fsqrt_rn(rr);
+    }
+    if (q == 0) {
+        tail_s[la] = tail[0];
+        tail_s[lb] = tail[1];
+    }
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
+        if (ta < n) xa = __ldg(reinterpret_cast<const uint4*>(ku + ta * kD + 32 * m + 8 * q));
+        if (tb < n) xb = __ldg(reinterpret_cast<const uint4*>(ku + tb * kD + 32 * m + 8 * q));
+#pragma unroll
+        for (int nt = 0; nt < kMaxL; ++nt) {
+            if (nt * kM >= ndir) break;
+            // direction nt * 8 + r, dimensions 32m + 8q .. + 7, as bf16 pairs
+            const float* ud = dirs + (long long)(nt * kM + r) * kDirStride + 32 * m + 8 * q;
+            const float4 w0 = __ldg(reinterpret_cast<const float4*>(ud));
+            const float4 w1 = __ldg(reinterpret_cast<const float4*>(ud + 4));
+            mma_bf16_16816(acc[nt], xa.x, xb.x, xa.y, xb.y, bf16_pair(w0.x, w0.y), bf16_pair(w0.z, w0.w));
+            mma_bf16_16816(acc[nt], xa.z, xb.z, xa.w, xb.w, bf16_pair(w1.x, w1.y), bf16_pair(w1.z, w1.w));
+        }
+    }
+    __syncthreads();  // qn is cleared
+    // codes from the tensor-core values; values near a code boundary are queued
+#pragma unroll
+    for (int nt = 0; nt < kMaxL; ++nt) {
+        if (nt * kM >= ndir) break;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int lt = i < 2 ? la : lb;
+            const int dir = nt * kM + 2 * q + (i & 1);
+            if (t0 + lt < n) {
+                const float p = __fmaf_rn(dirs[(long long)dir * kDirStride + kD], tail[i >> 1],
+                                          __fmul_rn(acc[nt][i], sc));
+                const float y = __fmul_rn(__fadd_rn(p, 1.0f), 128.0f);
+                const float fr = y - floorf(y);
+                codes[lt][dir] = (unsigned char)quantise_code(p);
+                if (fr < kCodeGuard || fr > 1.0f - kCodeGuard)
+                    queue[atomicAdd(&qn, 1)] = (unsigned short)((lt << 4) | dir);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = warp; i < qn; i += kPmWarps) {  // warp-uniform
+        const int lt = queue[i] >> 4, dir = queue[i] & 15;
+        const int c = exact_code_warp(ku + (t0 + lt) * kD, sc, dirs + (long long)dir * kDirStride,
+                                      tail_s[lt], lane);
+        if (lane == 0) codes[lt][dir] = (unsigned char)c;
+    }
+    __syncthreads();
+    if (tid < kPmTok * L) {
+        const int rr = tid / L, l = tid % L;
+        const long long t = t0 + rr;
+        if (t < n) {
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = codes[rr][l * kM + j];
+            const long long o = ((long long)l * U + u) * n + t;
+            mk_out[o] = morton8(c);
+            tok_out[o] = (int)t;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // K2: stable LSD radix sort of (Morton key, token) within each segment
 // (composite, unit), 8 bits per pass. Input order is ascending token, so equal
 // Morton keys stay in token order and the result is sorted by the 96-bit key.
@@ -447,8 +591,8 @@ __global__ void __launch_bounds__(256) pack_kernel(IndexView v, const T* __restr
 
 // Phase 1: keys -> sorted 96-bit keys and leaf numbering in scratch.
 cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long long n,
-                         const float* dirs, int* e_unit, BuildScratch& s, cudaStream_t st,
-                         int* final_buf) {
+                         const float* dirs, bool dirs_bf16_exact, int* e_unit, BuildScratch& s,
+                         cudaStream_t st, int* final_buf) {
     const long long total = (long long)U * n;
     const int S = L * U;
     ICE_TRY(cudaMemsetAsync(s.umax, 0, sizeof(unsigned) * U, st));
@@ -463,7 +607,11 @@ cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long 
     ICE_TRY(cudaGetLastError());
     const int tpb = kProjThreads / (L * kM);
     const int tiles_u = (int)((n + tpb - 1) / tpb);
-    if (dtype == ICE_BF16)
+    if (dtype == ICE_BF16 && dirs_bf16_exact) {
+        const int tiles_m = (int)((n + kPmTok - 1) / kPmTok);
+        project_mma_kernel<<<U * tiles_m, kPmWarps * 32, 0, st>>>(
+            (const __nv_bfloat16*)keys, s.nrm2, e_unit, dirs, L, n, tiles_m, s.mk[0], s.tk[0], U);
+    } else if (dtype == ICE_BF16)
         project_kernel<__nv_bfloat16><<<U * tiles_u, kProjThreads, 0, st>>>(
             (const __nv_bfloat16*)keys, s.nrm2, e_unit, dirs, L, n, tiles_u, s.mk[0], s.tk[0], U);
     else

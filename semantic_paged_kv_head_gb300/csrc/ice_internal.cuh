@@ -279,9 +279,11 @@ struct BuildScratch {
     unsigned char* tdepth = nullptr;   // [L][U][n] leaf depth of each sorted position
     int* nleaf = nullptr;              // [L][U] leaves per segment
 };
+// dirs_bf16_exact: every direction component is exact in bf16 (the +-1/16
+// directions); bf16 keys then take the tensor-core projection.
 cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long long n,
-                         const float* dirs, int* e_unit, BuildScratch& s, cudaStream_t st,
-                         int* final_buf);
+                         const float* dirs, bool dirs_bf16_exact, int* e_unit, BuildScratch& s,
+                         cudaStream_t st, int* final_buf);
 cudaError_t build_phase2(const IndexView& v, const void* keys, const void* values, long long n,
                          BuildScratch& s, int cur, cudaStream_t st);
 cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st);
