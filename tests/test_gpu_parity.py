@@ -84,6 +84,7 @@ def test_tiny_fp32_4k_workload(ice):
     (3001, 16, 2, 4, torch.bfloat16, 256),   # several tiles + ragged tail
     (2049, 32, 2, 4, torch.bfloat16, 1024),  # P = 32, large budget
     (5000, 16, 1, 2, torch.float32, 256),
+    (1800, 16, 1, 4, torch.bfloat16, 256),   # one composite in bf16 (tensor-core projection, 8 directions)
     (777, 8, 2, 1, torch.bfloat16, 64),
     (4097, 16, 2, 8, torch.bfloat16, 128),
     (3500, 64, 2, 4, torch.bfloat16, 1024),  # the largest page size
