@@ -1,7 +1,9 @@
 """ctypes binding of libice.so (the C ABI declared in include/ice.h).
 
-Argument marshalling only: torch supplies device memory and the current CUDA
-stream; every step of the decode path runs in the library's CUDA kernels.
+Argument marshalling only: torch supplies device memory (or, for the decode-step
+calls, page-locked CPU tensors that the kernels read and write in place) and the
+current CUDA stream; every step of the decode path runs in the library's CUDA
+kernels.
 There is no CPU fallback. If libice.so is missing or cannot be loaded the
 import of this module raises.
 
