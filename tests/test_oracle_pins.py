@@ -471,3 +471,224 @@ def test_gaussian_directions_follow_box_muller():
     assert abs(flat.mean()) < 0.01 and abs(flat.std() - 1 / 16) < 0.005
     r = O.directions(seed, L, m, d, kind=0)
     assert set(np.unique(r).tolist()) == {-0.0625, 0.0625}
+
+
+# --------------------------------------------------------------------------
+# Query preparation (Figure 2 step 2: the query is mapped into the same
+# projected code space as the keys). q_sel is the fp32 sum of the group's heads
+# taken in head order, q~ = [q_sel / ||q_sel||, 0] (the query side of the
+# MIPS-to-NN transform has tail 0), and its codes quantise u . q~.
+# --------------------------------------------------------------------------
+def _codes_fp64(u, qsel):
+    """Codes of the query from the definition, in fp64: q~ = q_sel / ||q_sel||
+    with tail 0, p = u[:d] . q~, code = clamp(floor((p + 1) 128), 0, 255).
+    Also returns the distance of (p + 1) 128 to the nearest integer."""
+    q64 = np.asarray(qsel, np.float64)
+    qt = q64 / np.linalg.norm(q64)
+    p = u[..., :-1].astype(np.float64) @ qt
+    y = (p + 1.0) * 128.0
+    return np.clip(np.floor(y), 0, 255).astype(np.int32), np.abs(y - np.round(y))
+
+
+def _index_for_query(seed, L=2, m=8):
+    from oracle.oracle import OracleIndex
+    rng = np.random.default_rng(seed)
+    K = _clustered(rng, 50, 128, 4)
+    return OracleIndex(128, m, L, 16, seed).build(K, K)
+
+
+def test_query_codes_one_axis_closed_form(oracle_mod):
+    """q_sel = 3 e_5: q~ = e_5 exactly, so p_j = u_j[5] = +-1/16 and the code is
+    (1 +- 1/16) 128 = 136 or 120 exactly. Without the normalisation the codes
+    would be 152 / 104; with a tail of 1 instead of 0 they would move by
+    u_j[d] 128 = +-8."""
+    ix = _index_for_query(31)
+    u = oracle_mod.directions(31, 2, 8, 128)
+    q = np.zeros((4, 128), np.float32)
+    q[2, 5] = 3.0
+    codes, qsel = ix.query(q)
+    assert qsel[5] == 3.0 and np.count_nonzero(qsel) == 1
+    expect = np.where(u[:, :, 5] > 0, 136, 120)
+    assert np.array_equal(codes, expect)
+
+
+def test_query_heads_summed_in_head_order(oracle_mod):
+    """q_sel = ((q_0 + q_1) + q_2) + q_3 in fp32: with 2^24, 1, 1 in one
+    component, each addition rounds back to 2^24 (ties to even), whereas any
+    order that adds the two ones first gives 2^24 + 2."""
+    ix = _index_for_query(32)
+    q = np.zeros((4, 128), np.float32)
+    q[0, 7], q[1, 7], q[2, 7] = 2.0 ** 24, 1.0, 1.0
+    q[3, 9] = -5.0
+    _, qsel = ix.query(q)
+    assert qsel[7] == 2.0 ** 24 and qsel[9] == -5.0
+    assert np.count_nonzero(qsel) == 2
+
+
+def test_query_heads_cancel_to_known_vector(oracle_mod):
+    """Heads a, b - a, 0, 0 (small integers, so every fp32 sum is exact) give
+    q_sel = b, and the codes are those of b / ||b|| from the definition."""
+    rng = np.random.default_rng(33)
+    ix = _index_for_query(33)
+    u = oracle_mod.directions(33, 2, 8, 128)
+    checked = 0
+    for _ in range(20):
+        a = rng.integers(-50, 50, 128).astype(np.float32)
+        b = rng.integers(-50, 50, 128).astype(np.float32)
+        q = np.stack([a, b - a, np.zeros(128), np.zeros(128)]).astype(np.float32)
+        codes, qsel = ix.query(q)
+        assert np.array_equal(qsel, b)
+        ref, gap = _codes_fp64(u, b)
+        safe = gap > 1e-3  # away from a code boundary, fp32 and fp64 agree
+        assert np.array_equal(codes[safe], ref[safe])
+        checked += int(safe.sum())
+    assert checked >= 300
+
+
+def test_query_codes_match_definition_random(oracle_mod):
+    """Random group queries (G = 1, 2, 4, 8): q_sel is the sequential fp32 sum
+    of the heads, and every code away from a boundary is the fp64 definition's.
+    Checked against a reading that skips the normalisation and one that puts 1
+    in the query's tail: both disagree with the oracle on these inputs."""
+    rng = np.random.default_rng(34)
+    ix = _index_for_query(34)
+    u = oracle_mod.directions(34, 2, 8, 128)
+    for G in (1, 2, 4, 8):
+        for _ in range(8):
+            q = (rng.standard_normal((G, 128)) * rng.uniform(0.1, 4.0)).astype(np.float32)
+            codes, qsel = ix.query(q)
+            acc = q[0].copy()
+            for h in range(1, G):
+                acc = (acc + q[h]).astype(np.float32)
+            assert np.array_equal(qsel, acc)
+            ref, gap = _codes_fp64(u, acc)
+            safe = gap > 1e-3
+            assert safe.sum() >= 12
+            assert np.array_equal(codes[safe], ref[safe])
+            # the two wrong readings give other codes on these queries
+            raw = np.clip(np.floor((u[..., :-1].astype(np.float64) @ acc.astype(np.float64) + 1)
+                                   * 128), 0, 255)
+            tail1 = np.clip(np.floor((u[..., :-1].astype(np.float64)
+                                      @ (acc / np.linalg.norm(acc.astype(np.float64)))
+                                      + u[..., -1] + 1) * 128), 0, 255)
+            assert not np.array_equal(codes, raw) or np.linalg.norm(acc) == 1.0
+            assert not np.array_equal(codes, tail1)
+
+
+def test_zero_query_has_centre_codes(oracle_mod):
+    """A group whose heads sum to zero has no direction: q~ = 0, every
+    projection is 0 and every code is the centre code 128."""
+    ix = _index_for_query(35)
+    q = np.zeros((4, 128), np.float32)
+    q[0, 3], q[1, 3] = 2.5, -2.5
+    codes, qsel = ix.query(q)
+    assert not np.any(qsel)
+    assert np.all(codes == 128)
+
+
+# --------------------------------------------------------------------------
+# Stop rule of the prioritised search (Figure 2 step 2, the P-DCI query):
+# leaves are taken whole, in increasing (priority, position) order, and the
+# search stops after the first leaf at which the running token count reaches
+# n_cand. Expected sets are derived here from the leaf table (counts and cells
+# of the dump, pinned by the partition tests) and the query codes (pinned
+# above); the priority is the L-infinity cell distance (pinned by brute force).
+# --------------------------------------------------------------------------
+def _expected_order(dmp, qc):
+    lo, hi = dmp["lo"], dmp["hi"]
+    below = np.maximum(lo - qc[None, :], 0)
+    above = np.maximum(qc[None, :] - hi, 0)
+    prio = np.max(np.maximum(below, above), axis=1)
+    order = np.lexsort((np.arange(len(prio)), prio))
+    return order, prio
+
+
+@pytest.mark.parametrize("m,P,seed", [(8, 4, 41), (2, 4, 42), (8, 16, 43), (2, 8, 44)])
+def test_stop_rule_takes_whole_leaves_until_n_cand(oracle_mod, m, P, seed):
+    from oracle.oracle import OracleIndex
+    rng = np.random.default_rng(seed)
+    n = 700
+    K = _clustered(rng, n, 128, 10, 0.5)
+    ix = OracleIndex(128, m, 2, P, seed).build(K, K)
+    boundary_hits = 0
+    for trial in range(3):
+        q = (K[rng.integers(0, n)] + 0.3 * rng.standard_normal((4, 128))).astype(np.float32)
+        codes, _ = ix.query(q)
+        for l in range(2):
+            dmp = ix.dump(l)
+            order, prio = _expected_order(dmp, codes[l])
+            cum = np.cumsum(dmp["cnt"][order])
+            _, oprio = ix.leaf_order(q, l, 1)
+            assert np.array_equal(oprio, prio)
+            ks = sorted({0, 1, 2, 3, len(cum) // 4, len(cum) // 2, len(cum) - 2, len(cum) - 1})
+            for k in ks:
+                for n_cand in (int(cum[k]) - 1, int(cum[k]), int(cum[k]) + 1):
+                    if n_cand < 1:
+                        continue
+                    # the first position whose running count reaches n_cand
+                    stop = int(np.searchsorted(cum, n_cand, side="left"))
+                    expect = order[:min(stop + 1, len(order))]
+                    flat, _ = ix.leaf_order(q, l, n_cand)
+                    tree, _ = ix.leaf_order(q, l, n_cand, tree=True)
+                    assert np.array_equal(flat, expect), (l, k, n_cand)
+                    assert np.array_equal(tree, expect), (l, k, n_cand)
+                    if n_cand == int(cum[k]):
+                        boundary_hits += 1
+                        assert len(flat) == k + 1  # landing on a leaf end: no leaf more
+    assert boundary_hits >= 20
+
+
+def test_stop_rule_through_selection_trace(oracle_mod):
+    """With one composite the candidates are exactly the taken leaves' tokens:
+    for n_cand on a leaf boundary the selection rescores cum[k] tokens, one
+    past it cum[k + 1]."""
+    from oracle.oracle import OracleIndex
+    rng = np.random.default_rng(45)
+    K = _clustered(rng, 500, 128, 8, 0.5)
+    ix = OracleIndex(128, 8, 1, 8, 45).build(K, K)
+    q = (K[17] + 0.3 * rng.standard_normal((2, 128))).astype(np.float32)
+    codes, _ = ix.query(q)
+    order, _ = _expected_order(ix.dump(0), codes[0])
+    cum = np.cumsum(ix.dump(0)["cnt"][order])
+    for k in (0, 3, 10, 25):
+        _, _, tr = ix.select(q, 64, n_cand=int(cum[k]))
+        assert tr["cands"] == int(cum[k])
+        _, _, tr = ix.select(q, 64, n_cand=int(cum[k]) + 1)
+        assert tr["cands"] == int(cum[k + 1])
+
+
+# --------------------------------------------------------------------------
+# Exact top-k (Table 1 "TOP-k": the k keys with the largest inner product with
+# the query), the reference of the recall report.
+# --------------------------------------------------------------------------
+def test_exact_topk_is_fp64_argsort_with_ties(oracle_mod):
+    from oracle.oracle import OracleIndex
+    rng = np.random.default_rng(46)
+    base = _clustered(rng, 150, 128, 6)
+    K = np.concatenate([base, base[:50]])  # tokens t and 150 + t tie exactly for t < 50
+    ix = OracleIndex(128, 8, 1, 16, 46).build(K, K)
+    for G in (1, 4):
+        q = (base[3] + 0.3 * rng.standard_normal((G, 128))).astype(np.float32)
+        acc = q[0].copy()
+        for h in range(1, G):
+            acc = (acc + q[h]).astype(np.float32)
+        s = K.astype(np.float64) @ acc.astype(np.float64)
+        ref = np.lexsort((np.arange(len(s)), -s))  # score desc, then token asc
+        for k in (1, 7, 64, 200):
+            got = ix.exact_topk(q, k)
+            assert np.array_equal(got, ref[:k]), (G, k)
+        # a tied pair ranks the lower token first
+        top = ix.exact_topk(q, 200)
+        pos = {int(t): i for i, t in enumerate(top)}
+        for t in range(50):
+            assert pos[t] < pos[150 + t]
+    # scores that fp32 cannot separate: q . k1 = 1 and q . k2 = 1 + 2^-30 are
+    # distinct in fp64, so token 1 ranks before token 0
+    K2 = np.zeros((3, 128), np.float32)
+    K2[0, 0] = 1.0
+    K2[1, 0], K2[1, 1] = 1.0, 1.0
+    K2[2, 0] = -1.0
+    q2 = np.zeros((1, 128), np.float32)
+    q2[0, 0], q2[0, 1] = 1.0, 2.0 ** -30
+    ix2 = OracleIndex(128, 8, 1, 16, 47).build(K2, K2)
+    assert ix2.exact_topk(q2, 3).tolist() == [1, 0, 2]
