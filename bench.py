@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-step select+attn latency (µs/layer) & achieved HBM GB/s vs peak, 1 GB300"
 UNIT = "us/layer"
 WORKLOAD = "llama8b_36k"
+FUSED_KERNEL, FUSED_SRC = "select_kernel<fused>", "ice_select.cu"
 FLUSH_BYTES = 256 << 20
 INSERT_WORKLOAD = "mistral7b_gen8k"
 
@@ -235,7 +236,7 @@ def us_per_layer(ms_step, w, world):
     return ms_step * 1e3 / (w.n_layers * w.batch * world)
 
 
-def per_layer_serial(ice, w, keys, values, q, flush, timed, args):
+def per_layer_serial(ice, w, keys, values, q, per_step, args, step_bytes, peak):
     """One launch per layer, in sequence, as a decode loop issues them: an index per
     layer (its KV heads), and the step = n_layers fused calls after an L2 flush."""
     import torch
@@ -249,22 +250,23 @@ def per_layer_serial(ice, w, keys, values, q, flush, timed, args):
         outs.append(torch.empty_like(qs[-1]))
         del kl, vl
 
-    def step():
-        flush.zero_()
+    def step(mark):
         for ixl, ql, ol in zip(idx, qs, outs):
             ixl.select_attn(ql, w.budget, ol)
 
-    n = max(20, args.steps // 30)
-    timed(step, 3)
-    t_f = timed(lambda: flush.zero_(), n)
-    t_s = timed(step, n)
+    n = max(20, args.steps)
+    per_step(step, 3)
+    ms = statistics.median(x[0] for x in per_step(step, n))
     for ixl in idx:
         ixl.check()
         ixl.destroy()
-    us = (t_s - t_f) / n * 1e3 / (w.n_layers * w.batch)
+    us = ms * 1e3 / (w.n_layers * w.batch)
+    gbs = step_bytes / (ms * 1e-3) / 1e9
     return {"value": round(us, 3), "unit": UNIT, "launches_per_step": w.n_layers,
+            "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "samples": n,
             "note": (f"each layer's {w.batch * w.n_kv_heads} units in their own launch, the "
-                     f"{w.n_layers} launches in sequence after an L2 flush")}
+                     f"{w.n_layers} launches in sequence after an L2 flush; median of per-step "
+                     "event pairs; frac = the step's canonical bytes / time / measured peak")}
 
 
 def host_kv_run(ice, w, keys, values, q, flush, timed, args, st):
@@ -625,19 +627,62 @@ def run_ice(args):
     def flush_only():
         flush.zero_()
 
-    def flush_select():
-        flush.zero_()
-        ix.select(q, w.budget, page_ids, n_pages)
-
-    def flush_step():
-        flush.zero_()
-        ix.select(q, w.budget, page_ids, n_pages)
-        ix.sparse_attn(q, page_ids, n_pages, out)
-
     def flush_fused():
         flush.zero_()
         ix.select_attn(q, w.budget, out, page_ids, n_pages)
 
+    def per_step(fn, k, flush_first=True, marks=2):
+        """Device time of each of k steps: the L2 flush (outside the events), then
+        CUDA events on the launching stream around the step's launches. fn(mark)
+        runs the step and calls mark() between its parts (marks - 2 times)."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(k)]
+        torch.cuda.synchronize()
+        for i in range(k):
+            if flush_first:
+                flush.zero_()
+            it = iter(ev[i])
+            next(it).record(stream)
+            fn(lambda: next(it).record(stream))
+            next(it).record(stream)
+        torch.cuda.synchronize()
+        return [[e[j].elapsed_time(e[j + 1]) for j in range(marks - 1)] for e in ev]
+
+    def fused_step(mark):
+        ix.select_attn(q, w.budget, out, page_ids, n_pages)
+
+    def separate_step(mark):
+        ix.select(q, w.budget, page_ids, n_pages)
+        mark()
+        ix.sparse_attn(q, page_ids, n_pages, out)
+
+    warm_n = max(3, args.warmup)
+    per_step(fused_step, warm_n)
+    per_step(separate_step, warm_n, marks=3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    # the timed region: exactly args.steps fused steps (one launch each), every
+    # step after an L2 flush and bracketed by its own pair of events
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        fused_ms = [x[0] for x in per_step(fused_step, args.steps)]
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    n_steps = args.steps
+
+    def pct(xs, f):
+        xs = sorted(xs)
+        return xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))]
+
+    ms_fused = statistics.median(fused_ms)
+    fused_p10, fused_p90 = pct(fused_ms, 0.1), pct(fused_ms, 0.9)
+    # the two separate calls, the same number of steps, each call between events
+    sep = per_step(separate_step, args.steps, marks=3)
+    ms_sel = statistics.median([x[0] for x in sep])
+    ms_att = statistics.median([x[1] for x in sep])
+    ms_sep = statistics.median([x[0] + x[1] for x in sep])
+    # cross-check: back-to-back loops by subtraction, [flush + step] - [flush]
     def timed(fn, k):
         """Device time of k back-to-back calls (the host runs ahead of the GPU)."""
         e0 = torch.cuda.Event(enable_timing=True)
@@ -650,33 +695,12 @@ def run_ice(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
-    for fn in (flush_only, flush_select, flush_step, flush_fused):
-        timed(fn, max(3, args.warmup))
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    # the three loops alternate so that clock drift affects them alike
-    t_f = t_fs = t_fsa = t_fx = 0.0
-    reps = 3
-    k_rep = max(1, args.steps // reps)
-    with ClockSampler(local) as clk:
-        wall0 = time.perf_counter()
-        for _ in range(reps):
-            t_f += timed(flush_only, k_rep)
-            t_fs += timed(flush_select, k_rep)
-            t_fsa += timed(flush_step, k_rep)
-            t_fx += timed(flush_fused, k_rep)
-        wall = time.perf_counter() - wall0
-    if world > 1:
-        dist.barrier()
-    n_steps = reps * k_rep
-    ms_sel = (t_fs - t_f) / n_steps
-    ms_att = (t_fsa - t_fs) / n_steps
-    ms_sep = (t_fsa - t_f) / n_steps
-    ms_fused = (t_fx - t_f) / n_steps  # the fused call: one launch per step
-    ms_sel, ms_att, ms_sep, ms_fused = reduce_max([ms_sel, ms_att, ms_sep, ms_fused], dev, world)
-    fused_faster = ms_fused <= ms_sep
-    ms_step = min(ms_fused, ms_sep)
+    n_x = max(50, args.steps)
+    ms_loop = (timed(flush_fused, n_x) - timed(flush_only, n_x)) / n_x
+    (ms_sel, ms_att, ms_sep, ms_fused, fused_p10, fused_p90,
+     ms_loop) = reduce_max([ms_sel, ms_att, ms_sep, ms_fused, fused_p10, fused_p90, ms_loop], dev,
+                           world)
+    ms_step = ms_fused  # the reported path is always the fused call (one launch per step)
     ix.check()
 
     # end to end through the public API with host buffers, every step: q in page-locked
@@ -685,7 +709,7 @@ def run_ice(args):
     q_host = q.cpu().pin_memory()
     out_host = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     q_in = torch.empty_like(q)
-    n_e2e = max(10, args.steps // 4)
+    n_e2e = max(20, args.steps)
 
     def e2e_loop(step):
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
@@ -698,7 +722,7 @@ def run_ice(args):
             step()
             ev2[k][1].record(stream)
         torch.cuda.synchronize()
-        return reduce_max([sum(e[0].elapsed_time(e[1]) for e in ev2) / n_e2e], dev, world)[0]
+        return reduce_max([statistics.median(e[0].elapsed_time(e[1]) for e in ev2)], dev, world)[0]
 
     def step_in_place():
         ix.select_attn(q_host, w.budget, out_host, page_ids, n_pages)
@@ -719,14 +743,9 @@ def run_ice(args):
     peak, peak_kind = _peaks()
     sel_gbs = sel_bytes / (ms_sel * 1e-3) / 1e9
     att_gbs = attn_bytes / (ms_att * 1e-3) / 1e9
-    # the reported path is the faster of the fused call and the two separate calls;
-    # the roofline kernel is the fused kernel, or else the longer of the two
-    if fused_faster:
-        dom, dom_bytes, dom_ms, src = "select_kernel<fused>", step_bytes, ms_fused, "ice_select.cu"
-    elif ms_sel >= ms_att:
-        dom, dom_bytes, dom_ms, src = "select_kernel", sel_bytes, ms_sel, "ice_select.cu"
-    else:
-        dom, dom_bytes, dom_ms, src = "attn_kernel", attn_bytes, ms_att, "ice_attn.cu"
+    # the reported path is always the fused call; it is one kernel, so the roofline
+    # kernel is that kernel and its time is the step's
+    dom, dom_bytes, dom_ms, src = FUSED_KERNEL, step_bytes, ms_fused, FUSED_SRC
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
     # every rank runs its own replica of the workload: the job processes
     # world x n_layers layers per step
@@ -739,9 +758,11 @@ def run_ice(args):
         "step_bytes": int(step_bytes),
         "step_gbs": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
         "step_frac_of_peak": round(step_bytes / (ms_step * 1e-3) / 1e9 / peak, 4),
-        "path": ("ice_select_attn (select and paged attention fused, one launch per step)"
-                 if fused_faster else "ice_select + ice_sparse_attn (two launches per step)"),
-        "kernels": {"select_kernel<fused>": {"us": round(ms_fused * 1e3, 3),
+        "path": "ice_select_attn (select and paged attention fused, one launch per step)",
+        "step_us": {"median": round(ms_fused * 1e3, 3), "p10": round(fused_p10 * 1e3, 3),
+                    "p90": round(fused_p90 * 1e3, 3), "samples": n_steps,
+                    "loop_crosscheck": round(ms_loop * 1e3, 3), "loop_steps": n_x},
+        "kernels": {FUSED_KERNEL: {"us": round(ms_fused * 1e3, 3),
                                              "bytes": int(step_bytes),
                                              "gbs": round(step_bytes / (ms_fused * 1e-3) / 1e9, 1)},
                     "separate_calls": {"us": round(ms_sep * 1e3, 3),
@@ -761,21 +782,26 @@ def run_ice(args):
                 "with_copies": {"value": round(us_per_layer(ms_e2e_copies, w, world), 4),
                                 "unit": UNIT, "how": "cudaMemcpyAsync of q in and out back "
                                 "around ice_select_attn on device buffers"}},
-        "gpu_launches": 4 * n_steps,
-        "timing": ("device time of back-to-back loops (host runs ahead), each step after an L2 "
-                   "flush: step = [flush+select_attn] - [flush]; separate calls: select = "
-                   "[flush+select] - [flush], attn = [flush+select+attn] - [flush+select]"),
+        "gpu_launches": n_steps,
+        "timing": ("median over the timed steps of each step's own CUDA-event pair on the "
+                   "launching stream; every step follows an L2 flush (256 MiB write) outside its "
+                   "events; p10/p90 over the same steps; loop_crosscheck = ([flush + step] - "
+                   "[flush]) over back-to-back loops of loop_steps steps; separate calls timed "
+                   "per call with events over the same number of steps"),
         "build_ms": round(build_ms, 1),
         "wall_s_timed_region": round(wall, 3),
         "clocks": clk.summary(),
     }
-    # warm L2 (no flush): the same fused step repeated on resident data
-    n_w = max(100, args.steps // 3)
-    t_w = reduce_max([timed(lambda: ix.select_attn(q, w.budget, out, page_ids, n_pages), n_w)], dev, world)[0]
-    line["warm"] = {"value": round(us_per_layer(t_w / n_w, w, world), 4),
-                    "unit": UNIT, "note": "no L2 flush between steps"}
+    # warm L2 (no flush): the same fused step, each step between its own events
+    n_w = max(50, args.steps)
+    t_w = statistics.median(x[0] for x in per_step(fused_step, n_w, flush_first=False))
+    t_w = reduce_max([t_w], dev, world)[0]
+    line["warm"] = {"value": round(us_per_layer(t_w, w, world), 4), "unit": UNIT,
+                    "samples": n_w,
+                    "note": "no L2 flush between steps; median of per-step event pairs"}
     if not args.no_extras and world == 1:  # single-replica extras (not part of scaling runs)
-        line["per_layer_serial"] = per_layer_serial(ice, w, keys, values, q, flush, timed, args)
+        line["per_layer_serial"] = per_layer_serial(ice, w, keys, values, q, per_step, args,
+                                                    step_bytes, peak)
         line["insert"] = insert_run(ice, synth, dev, flush, timed, args)
         line["host_kv"] = host_kv_run(ice, w, keys, values, q, flush, timed, args, st)
         line["reuse"] = reuse_run(ice, synth, ix, w, centers, flush, timed, args)
@@ -814,7 +840,7 @@ def run_ice(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ice", "reference"], default="ice")
     ap.add_argument("--workload", default=WORKLOAD)

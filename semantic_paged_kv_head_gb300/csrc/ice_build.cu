@@ -55,16 +55,6 @@ __global__ void __launch_bounds__(256) norms_kernel(const T* __restrict__ keys, 
     }
 }
 
-// Smallest e with 4^e >= maxn (e >= -60); 0 when maxn == 0.
-__device__ __forceinline__ int scale_exponent_dev(float maxn) {
-    if (!(maxn > 0.0f)) return 0;
-    int x;
-    float f = frexpf(maxn, &x);  // maxn = f * 2^x, f in [0.5, 1)
-    int need = (f == 0.5f) ? x - 1 : x;  // 2e >= need
-    int e = need >= 0 ? (need + 1) / 2 : -((-need) / 2);
-    return e < -60 ? -60 : e;
-}
-
 __global__ void exponent_kernel(const unsigned int* __restrict__ umax, int* __restrict__ e_unit,
                                 int U) {
     int u = blockIdx.x * blockDim.x + threadIdx.x;

@@ -158,6 +158,18 @@ __device__ __forceinline__ float thread_dot_fixed_self(const float* x) {
     return acc[0];
 }
 
+// Frozen scale exponent of a unit: the smallest e with 4^e >= maxn (the largest
+// squared key norm), kept at e >= -60 so that 2^-2e stays a finite float; 0
+// when maxn == 0.
+__device__ __forceinline__ int scale_exponent_dev(float maxn) {
+    if (!(maxn > 0.0f)) return 0;
+    int x;
+    float f = frexpf(maxn, &x);  // maxn = f * 2^x, f in [0.5, 1)
+    int need = (f == 0.5f) ? x - 1 : x;  // 2e >= need
+    int e = need >= 0 ? (need + 1) / 2 : -((-need) / 2);
+    return e < -60 ? -60 : e;
+}
+
 // code = clamp(floor((p + 1) * 128), 0, 255) evaluated in fp32.
 __device__ __forceinline__ int quantise_code(float p) {
     float y = __fmul_rn(__fadd_rn(p, 1.0f), 128.0f);

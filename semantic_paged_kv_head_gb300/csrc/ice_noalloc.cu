@@ -15,6 +15,8 @@
 // uses the same arrays, so two calls that run on the GPU at the same time (for
 // example on two streams) race and both give wrong results; calls on one
 // stream are ordered and safe.
+#include <mutex>
+
 #include "ice_internal.cuh"
 
 namespace ice {
@@ -80,17 +82,7 @@ __global__ void __launch_bounds__(256) na_norms_kernel(const T* __restrict__ key
 __global__ void na_exponent_kernel(const unsigned int* __restrict__ umax, int* __restrict__ e_out,
                                    int U) {
     const int u = blockIdx.x * blockDim.x + threadIdx.x;
-    if (u >= U) return;
-    const float maxn = __uint_as_float(umax[u]);
-    int e = 0;
-    if (maxn > 0.0f) {
-        int x;
-        const float f = frexpf(maxn, &x);  // maxn = f * 2^x, f in [0.5, 1)
-        const int need = (f == 0.5f) ? x - 1 : x;
-        e = need >= 0 ? (need + 1) / 2 : -((-need) / 2);
-        e = e < -60 ? -60 : e;
-    }
-    e_out[u] = e;
+    if (u < U) e_out[u] = scale_exponent_dev(__uint_as_float(umax[u]));
 }
 
 // One thread per (key, composite): transformed key, 8 projections in the fixed
@@ -136,7 +128,9 @@ __global__ void __launch_bounds__(128) na_codes_kernel(const T* __restrict__ key
     mk[g] = morton8(code);
 }
 
-// Device address of the scratch arrays, looked up once per device.
+// Device address of the scratch arrays, looked up once per device (with that
+// device current) under a lock, so that first calls from several host threads
+// do not race on the table.
 struct NoAllocPtrs {
     float* nrm2;
     unsigned int* umax;
@@ -144,16 +138,22 @@ struct NoAllocPtrs {
     bool ready;
 };
 NoAllocPtrs g_na_ptrs[64];
+std::mutex g_na_lock;
 
-cudaError_t na_setup(int dev) {
+cudaError_t na_setup(int dev, NoAllocPtrs* out) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> guard(g_na_lock);
     NoAllocPtrs& p = g_na_ptrs[dev];
-    if (p.ready) return cudaSuccess;
-    cudaError_t e = cudaGetSymbolAddress((void**)&p.nrm2, g_na_nrm2);
-    if (e == cudaSuccess) e = cudaGetSymbolAddress((void**)&p.umax, g_na_umax);
-    if (e == cudaSuccess) e = cudaGetSymbolAddress((void**)&p.dirs, g_na_dirs);
-    if (e != cudaSuccess) return e;
-    p.ready = true;
+    if (!p.ready) {
+        NoAllocPtrs q{};
+        cudaError_t e = cudaGetSymbolAddress((void**)&q.nrm2, g_na_nrm2);
+        if (e == cudaSuccess) e = cudaGetSymbolAddress((void**)&q.umax, g_na_umax);
+        if (e == cudaSuccess) e = cudaGetSymbolAddress((void**)&q.dirs, g_na_dirs);
+        if (e != cudaSuccess) return e;
+        q.ready = true;
+        p = q;
+    }
+    *out = p;
     return cudaSuccess;
 }
 
@@ -176,8 +176,8 @@ extern "C" int ice_key_codes_noalloc(const ice_params* params, const void* keys,
     if (U > kNoAllocMaxUnits || U * n_tokens > kNoAllocMaxTokens) return ICE_ERR_CAPACITY;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ICE_ERR_CUDA;
-    if (na_setup(dev) != cudaSuccess) return ICE_ERR_CUDA;
-    const NoAllocPtrs& p = g_na_ptrs[dev];
+    NoAllocPtrs p{};
+    if (na_setup(dev, &p) != cudaSuccess) return ICE_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
     const int L = params->n_composite;
     const long long total = U * n_tokens;

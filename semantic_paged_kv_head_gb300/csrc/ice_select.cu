@@ -383,11 +383,11 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
         }
         const bool ok = mbar_wait_bounded(bar, (unsigned)(round & 1));
         if (!ok) {
-            if (tid == 0) {
-                set_status(v.status, ICE_ERR_TIMEOUT);
-                *s_fail = 1;
-            }
-            mbar_wait_bounded(bar, (unsigned)(round & 1));  // copies possibly still in flight
+            // any thread whose wait ran out marks the block; the copies may still
+            // be in flight, so wait for them once more (bounded) before leaving
+            *s_fail = 1;
+            set_status(v.status, ICE_ERR_TIMEOUT);
+            mbar_wait_bounded(bar, (unsigned)(round & 1));
         }
         if (ok) {
             for (int j = warp; j < nrow; j += kSelWarps) {  // warp-uniform
@@ -428,6 +428,9 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
             }
         }
         __syncthreads();  // the round's rows are consumed before the next copies land
+        // after a timeout the barrier's phase may never complete: issue no further
+        // expect_tx or copies on it (block-uniform: s_fail is read after the barrier)
+        if (*s_fail) break;
         p0 = p1;
         ++round;
     }

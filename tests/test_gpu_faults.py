@@ -79,6 +79,39 @@ def test_forced_timeout_reports_and_recovers(ice, small):
     assert torch.equal(out2, ref)
 
 
+def test_forced_timeout_over_several_staging_rounds(ice):
+    """A selection larger than the fused kernel's staging region (64 pages of
+    up to 16 fp32 rows each) is attended in several rounds; a forced timeout in
+    the first round ends the attention there: no further copies are issued on
+    the barrier, the status reports the timeout, the output is zero and the
+    next call on the same index is exact."""
+    from semantic_paged_kv_head_gb300 import synth
+    w = synth.scaled(synth.WORKLOADS["tiny_fp32_4k"], n_tokens=4096, n_centers=16, seed=33,
+                     budget=1024)
+    keys, values, centers = synth.make_kv(w)
+    q = synth.make_queries(w, centers).cuda()
+    gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                             n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed)
+    ref, ids_ref, npg_ref = gix.select_attn(q, w.budget)
+    torch.cuda.synchronize()
+    assert gix.get_error() == 0
+    d = gix.dump(0)
+    rows = sum(int(d["comp"][0]["list_cnt"][p]) for p in ids_ref[0, :int(npg_ref[0])].tolist())
+    assert rows * 2 * 128 * 4 > 100 * 1024  # more K and V rows than one staging round holds
+    gix.debug_set_flags(ice.DEBUG_STALL_ATTN)
+    out, ids, npg = gix.select_attn(q, w.budget)
+    torch.cuda.synchronize()
+    assert gix.get_error() == ice.ICE_ERR_TIMEOUT
+    assert torch.equal(ids, ids_ref) and torch.equal(npg, npg_ref)
+    assert float(out.float().abs().max()) == 0.0
+    gix.debug_set_flags(0)
+    out2, _, _ = gix.select_attn(q, w.budget)
+    torch.cuda.synchronize()
+    assert gix.get_error() == 0
+    assert torch.equal(out2, ref)
+    gix.destroy()
+
+
 def test_insert_capacity_is_reported(ice):
     from semantic_paged_kv_head_gb300 import synth
     w = synth.scaled(synth.WORKLOADS["mistral7b_gen8k"], n_kv_heads=1, n_tokens=40, n_insert=3,
