@@ -278,6 +278,28 @@ typedef struct ice_info {
 int ice_get_info(const ice_index* ix, ice_info* info);
 
 /*
+ * ice_set_cluster_size - how many thread blocks share one unit in the selection
+ * of ice_select and ice_select_attn (a tuning knob; results do not depend on it).
+ * The selection of a unit is a chain of dependent phases (IceCache page, Figure 2
+ * steps 2-3); with few units per launch (one layer of a decode step) one block
+ * per unit leaves most SMs idle. A thread-block cluster of k blocks splits the
+ * leaf scan, the rescoring and the attended pages of a unit, and merges the
+ * priority histograms, the page keys and the softmax partials over distributed
+ * shared memory.
+ *   k = 0: automatic (16, 8, 4 or 2 blocks per unit for launches of up to 9, 19,
+ *          38 or 152 units; one block per unit above that, and a cluster
+ *          whenever one block cannot hold the unit's tables);
+ *   k = 1: one block per unit;
+ *   k = 2, 4, 8, 16: that many blocks per unit (k >= n_composite).
+ * The cluster path takes budget/page_size <= 32 pages; ice_select_attn_reuse,
+ * ice_decode_step and ice_select_heads always use one block per unit. A call
+ * whose forced k cannot be launched (tables too large, or clusters of that
+ * size not resident on this GPU) returns ICE_ERR_UNSUPPORTED or ICE_ERR_CUDA.
+ * Returns ICE_ERR_INVALID_ARG for any other k.
+ */
+int ice_set_cluster_size(ice_index* ix, int32_t k);
+
+/*
  * Debug views (tests only). ice_debug_dump copies the index of one unit to
  * host memory and waits for the copy. Layout of host_buf, little endian:
  *   int64 header[16]: L, P, list_capacity C, n_tokens n, e, n_leaf[0..3],

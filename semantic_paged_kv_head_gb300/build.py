@@ -19,8 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libice.so")
 OBJDIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["ice_api.cu", "ice_build.cu", "ice_select.cu", "ice_attn.cu", "ice_insert.cu",
-           "ice_noalloc.cu", "ice_reuse.cu", "ice_union.cu"]
+SOURCES = ["ice_api.cu", "ice_build.cu", "ice_select.cu", "ice_select_cluster.cu", "ice_attn.cu",
+           "ice_insert.cu", "ice_noalloc.cu", "ice_reuse.cu", "ice_union.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + INCLUDE, "-I" + CSRC]

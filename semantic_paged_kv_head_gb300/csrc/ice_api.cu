@@ -311,7 +311,8 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         }
         v.page_k = pk;
         v.page_v = pv;
-        if (select_prepare() != cudaSuccess || insert_prepare(P, params->dtype) != cudaSuccess) {
+        if (select_prepare() != cudaSuccess || select_cluster_prepare() != cudaSuccess ||
+            insert_prepare(P, params->dtype) != cudaSuccess) {
             scratch_free(s, st);
             cudaGetLastError();
             free_all(ix);
@@ -353,8 +354,11 @@ int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
     return ICE_OK;
 }
 
+// cluster_ok: the call may run on the cluster selection kernel (plain select
+// and select + attention), which holds larger per-unit tables than one block.
 static int select_args(const ice_index* ix, const void* q, int32_t token_budget,
-                       const int32_t* page_ids, const int32_t* n_pages, const void* out) {
+                       const int32_t* page_ids, const int32_t* n_pages, const void* out,
+                       bool cluster_ok = false) {
     if (!ix || !q || !page_ids || !n_pages || !aligned16(q)) return ICE_ERR_INVALID_ARG;
     if (out && !aligned16(out)) return ICE_ERR_INVALID_ARG;
     const int P = ix->p.page_size;
@@ -363,16 +367,28 @@ static int select_args(const ice_index* ix, const void* q, int32_t token_budget,
     if (n_sel > 512) return ICE_ERR_UNSUPPORTED;
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
     if (n_cand > (1 << 16)) return ICE_ERR_UNSUPPORTED;
-    if (select_smem_bytes(ix->C, ix->p.n_composite, P, n_cand, n_sel, ix->G, out != nullptr) >
-        kSelSmemMax)
-        return ICE_ERR_UNSUPPORTED;
+    const bool one_fits =
+        select_smem_bytes(ix->C, ix->p.n_composite, P, n_cand, n_sel, ix->G, out != nullptr) <= kSelSmemMax;
+    if (cluster_ok) {
+        const int forced = ix->v.cluster_k;
+        if (forced >= 2)
+            return select_cluster_bytes(ix->v, forced, n_sel, n_cand, out != nullptr) >= 0
+                       ? ICE_OK
+                       : ICE_ERR_UNSUPPORTED;
+        if (forced == 1) return one_fits ? ICE_OK : ICE_ERR_UNSUPPORTED;
+        if (one_fits) return ICE_OK;
+        const int K = std::max(2, select_cluster_auto(ix->U, ix->p.n_composite));
+        return select_cluster_bytes(ix->v, K, n_sel, n_cand, out != nullptr) >= 0 ? ICE_OK
+                                                                                  : ICE_ERR_UNSUPPORTED;
+    }
+    if (!one_fits) return ICE_ERR_UNSUPPORTED;
     return ICE_OK;
 }
 
 static int select_common(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
                          int32_t* n_pages, int32_t* stats, void* out, void* stream,
                          const int32_t* reselect = nullptr) {
-    const int a = select_args(ix, q, token_budget, page_ids, n_pages, out);
+    const int a = select_args(ix, q, token_budget, page_ids, n_pages, out, reselect == nullptr);
     if (a != ICE_OK) return a;
     ICE_KERNEL_ADDR(q);
     ICE_KERNEL_ADDR(page_ids);
@@ -554,6 +570,13 @@ void ice_destroy(ice_index* ix) {
 int ice_debug_set_flags(ice_index* ix, int32_t flags) {
     if (!ix || (flags & ~ICE_DEBUG_STALL_ATTN)) return ICE_ERR_INVALID_ARG;
     ix->v.debug = flags;
+    return ICE_OK;
+}
+
+int ice_set_cluster_size(ice_index* ix, int32_t k) {
+    if (!ix || !(k == 0 || k == 1 || k == 2 || k == 4 || k == 8 || k == 16)) return ICE_ERR_INVALID_ARG;
+    if (k >= 2 && k < ix->p.n_composite) return ICE_ERR_INVALID_ARG;
+    ix->v.cluster_k = k;
     return ICE_OK;
 }
 

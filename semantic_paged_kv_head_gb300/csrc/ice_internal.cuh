@@ -74,6 +74,7 @@ struct IndexView {
     int* status;
     int* n_tok;  // [U] tokens in each unit (build + inserts), advanced by the insert kernel
     int debug;  // ICE_DEBUG_* flags (tests only), 0 in normal use
+    int cluster_k;  // blocks per unit of the selection: 0 automatic, 1, 2, 4, 8 or 16
 
     __host__ __device__ long long ul(int u, int l) const { return (long long)u * L + l; }
     __host__ __device__ long long leaf_base(int u, int l) const { return ul(u, l) * C; }
@@ -303,6 +304,18 @@ void scratch_free(BuildScratch& s, cudaStream_t st);
 int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, bool fused);
 bool select_insert_fits(long long C, int L, int P, int n_cand, int n_sel, int es);
 cudaError_t select_prepare();
+// The selection spread over a thread-block cluster of K blocks per unit
+// (ice_select_cluster.cu): the cluster size chosen for U units, the dynamic
+// shared memory of a launch (-1 if the cluster path cannot take it: K not a
+// power of two in [max(2, L), 16], n_sel > 32, or the tables too large), the
+// per-device setup, and the launch (*launched false if clusters of that size
+// cannot be resident; nothing is launched then).
+int select_cluster_auto(int U, int L);
+int select_cluster_bytes(const IndexView& v, int K, int n_sel, int n_cand, bool fused);
+cudaError_t select_cluster_prepare();
+cudaError_t launch_select_cluster(const IndexView& v, int K, const void* q, int n_sel, int n_cand,
+                                  int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                                  cudaStream_t s, bool* launched);
 
 // ---- launchers (implemented in the .cu files) --------------------------------------
 cudaError_t launch_insert(const IndexView& v, const void* k, const void* val, cudaStream_t s);

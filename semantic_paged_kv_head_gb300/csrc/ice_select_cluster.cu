@@ -1,0 +1,1207 @@
+// Decode-time page selection and attention of one unit spread over a cluster
+// of K thread blocks ("IceCache", Figure 2 steps 2-3; the blog's mechanism
+// section: P-DCI, the prioritised DCI search, picks the pages for the current
+// query, and attention runs over every token of those pages).
+//
+// The selection of a unit is a chain of dependent phases. One block per unit
+// leaves most of the GPU idle when a decode step launches few units (one layer
+// at a time), and its chain sets the step time. Here the K blocks of a cluster
+// share a unit, and the phases that touch many bytes are split between them:
+//  * composites: blocks [0, K/L) serve composite 0, the others composite 1;
+//  * leaf scan: the Kc = K/L blocks of a composite scan contiguous ranges of its
+//    leaves (64-leaf chunks), so that position order is block order;
+//  * threshold: the blocks' priority histograms are added over distributed
+//    shared memory (DSMEM), and every block of the composite derives the same
+//    pi* and need;
+//  * ties at pi*: each block publishes the tokens of its own ties; a block takes
+//    its ties in position order while the ties of the blocks before it plus its
+//    own taken so far stay below the need (the flat (priority, position) order);
+//  * duplicates: composite-0 blocks set the pages they took in a bitmap of
+//    block 0; a composite-1 candidate whose page is set there is dropped;
+//  * rescoring: every block rescores its own candidates (fixed-order fp32 dot)
+//    and keeps the minimum (score desc, token asc) key of every page it saw;
+//  * ranking: each block publishes its n_sel best pages to block 0. A page in
+//    the global top n_sel reaches there with its true minimum, because the block
+//    that holds that minimum has fewer than n_sel pages above it; every other
+//    page arrives with a key no smaller than its true minimum. So the n_sel
+//    smallest of the published keys, taken per page, are the selection. Every
+//    block computes it from block 0's lists;
+//  * attention: block r attends selected pages r, r + K, ... (fp32 online
+//    softmax over pages staged with bulk copies), and the blocks' partial
+//    (max, sum, accumulator) triples are merged in block order over DSMEM, each
+//    block writing a slice of the output.
+// Every block of a cluster passes the same sequence of cluster barriers, and
+// no block leaves while another may still read its shared memory.
+#include <cooperative_groups.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "ice_internal.cuh"
+#include "ice_select_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace ice {
+
+constexpr int kCT = 256;           // threads per block
+constexpr int kCW = kCT / 32;      // warps per block
+constexpr int kCSubH = 8;          // sub-histograms (lane groups)
+constexpr int kCHistRow = 257;     // words per sub-histogram row
+constexpr int kCRing = 3;          // scan chunks in flight per warp
+constexpr int kCSlotB = 640;       // one chunk: 64 corners (8 B) + 64 (t | count << 7) (2 B)
+constexpr int kCRingB = kCW * kCRing * kCSlotB;
+constexpr int kCTop = 32;          // largest n_sel of the cluster path (warp top-32 ranking)
+constexpr int kCluSmemMax = 220 * 1024;
+
+struct CluSmem {
+    int sel, scnt, toff, pub, pubx, bm0, lhist, cpart, qf;  // live through the kernel
+    int A;                                                  // ring / candidates / ranking / staging
+    int skey, sval, hpage, hkey, hcnt, top;                 // local candidates and page table
+    int g_page, g_key, g_cnt, g_ckey, g_cidx, g_top;        // global ranking
+    int B;                                                  // scan tables; rescoring staging
+    int prio, cnt, tieb, hist, ghist, chosen, cmeta, coff;
+    int end;
+};
+
+__host__ __device__ inline CluSmem clu_layout(long long C, int rcap, int n_cand, int cand_cap,
+                                              int hcap2, int n_sel, int K, int G, int min_total) {
+    CluSmem s;
+    int o = 0;
+    s.sel = o; o = align16(o + kCTop * 4);
+    s.scnt = o; o = align16(o + kCTop * 4);
+    s.toff = o; o = align16(o + (kCTop + 1) * 4);
+    s.pub = o; o = align16(o + K * n_sel * 16);
+    s.pubx = o; o = align16(o + K * 4 * 4);
+    s.bm0 = o; o = align16(o + (int)((C + 31) / 32) * 4);
+    s.lhist = o; o = align16(o + 256 * 4);
+    s.cpart = o; o = align16(o + (G * (kD + 2) + 4) * 4);
+    s.qf = o; o = align16(o + G * kD * 4);
+    s.A = o;
+    int a = o;
+    s.skey = a; a = align16(a + cand_cap * 8);
+    s.sval = a; a = align16(a + cand_cap * 4);
+    s.hpage = a; a = align16(a + cand_cap * 4);
+    s.hkey = a; a = align16(a + cand_cap * 8);
+    s.hcnt = a; a = align16(a + cand_cap * 4);
+    s.top = a; a = align16(a + kCW * 32 * 12);
+    int g = o;
+    s.g_page = g; g = align16(g + hcap2 * 4);
+    s.g_key = g; g = align16(g + hcap2 * 8);
+    s.g_cnt = g; g = align16(g + hcap2 * 4);
+    s.g_ckey = g; g = align16(g + hcap2 * 8);
+    s.g_cidx = g; g = align16(g + hcap2 * 4);
+    s.g_top = g; g = align16(g + kCW * 32 * 12);
+    int b = o + kCRingB;
+    b = a > b ? a : b;
+    b = g > b ? g : b;
+    s.B = b;
+    o = b;
+    s.prio = o; o = align16(o + rcap);
+    s.cnt = o; o = align16(o + rcap);
+    s.tieb = o; o = align16(o + (rcap / 32) * 4);
+    s.hist = o; o = align16(o + kCSubH * kCHistRow * 4);
+    s.ghist = o; o = align16(o + 256 * 4);
+    s.chosen = o; o = align16(o + n_cand * 4);
+    s.cmeta = o; o = align16(o + n_cand * 4);
+    s.coff = o; o = align16(o + (n_cand + 1) * 4);
+    s.end = o > min_total ? o : min_total;
+    return s;
+}
+
+// The n smallest (key, index) pairs of keys[0..cnt) in ascending order, into
+// warp 0's lanes (tk, tv valid in warp 0 after the call; n <= 32). topk/topv:
+// [kCW][32] scratch. Block-wide: every thread calls it.
+__device__ __forceinline__ void block_top32(const unsigned long long* keys, const int* idx, int cnt,
+                                            unsigned long long* topk, int* topv,
+                                            unsigned long long& tk, int& tv) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nb = (cnt + 31) / 32;
+    tk = ~0ull;
+    tv = -1;
+    for (int bt = warp; bt < nb; bt += kCW) {  // warp-uniform
+        const int j = bt * 32 + lane;
+        unsigned long long k = j < cnt ? keys[j] : ~0ull;
+        int vv = j < cnt ? idx[j] : -1;
+        warp_sort32(k, vv, lane);
+        warp_merge32(tk, tv, k, vv, lane);
+    }
+    const int nw = min(kCW, max(nb, 1));
+    if (warp < nw) {
+        topk[warp * 32 + lane] = tk;
+        topv[warp * 32 + lane] = tv;
+    }
+    __syncthreads();
+    for (int st = 1; st < nw; st <<= 1) {
+        if ((warp & (2 * st - 1)) == 0 && warp + st < nw) {
+            unsigned long long a = topk[warp * 32 + lane];
+            int av = topv[warp * 32 + lane];
+            warp_merge32(a, av, topk[(warp + st) * 32 + lane], topv[(warp + st) * 32 + lane], lane);
+            topk[warp * 32 + lane] = a;
+            topv[warp * 32 + lane] = av;
+        }
+        __syncthreads();
+    }
+    tk = topk[lane];
+    tv = topv[lane];
+}
+
+// Partial attention of the G query heads over this block's share of the
+// selected pages (s_sel[r], s_sel[r + K], ...): the pages' K and V rows are
+// staged with one bulk copy per page and tensor onto an mbarrier, in rounds
+// that fit the staging region; warp w takes tokens w, w + kCW, ... of a round
+// (lane = (head, group of 4G dimensions)); the warps' (max, sum, accumulator)
+// triples are merged in warp order into cpart[h][kD + 2].
+template <typename T, int G>
+__device__ __forceinline__ void attend_partial(const IndexView& v, int u, const float* s_q,
+                                               const int* s_sel, const int* s_scnt, int taken,
+                                               int r, int K, int* s_toff, unsigned char* stage,
+                                               int stage_bytes, unsigned bar, int* s_fail,
+                                               float* cpart) {
+    constexpr int LPH = 32 / G;
+    constexpr int DPL = kD / LPH;
+    constexpr int ROWB = kD * (int)sizeof(T);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = v.P;
+    const long long C = v.C;
+    const int h = lane / LPH, g = lane % LPH;
+    const int npg = taken > r ? (taken - r + K - 1) / K : 0;
+    if (warp == 0) {
+        int carry = 0;
+        for (int i0 = 0; i0 < npg; i0 += 32) {
+            const int i = i0 + lane;
+            int c = 0;
+            if (i < npg) {
+                const int pg = s_sel[r + K * i];
+                c = (pg >= 0 && pg < C) ? s_scnt[r + K * i] : 0;
+                c = c < 0 ? 0 : (c > P ? P : c);
+            }
+            int inc = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (i < npg) s_toff[i] = carry + inc - c;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_toff[npg] = carry;
+    }
+    float qa[DPL];
+    {
+        const float sc = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) qa[k] = s_q[h * kD + g * DPL + k] * sc;
+    }
+    __syncthreads();
+    const int rows_cap = stage_bytes / (2 * ROWB);
+    const T* sk = reinterpret_cast<const T*>(stage);
+    const T* sv = reinterpret_cast<const T*>(stage + (size_t)rows_cap * ROWB);
+    float m = -INFINITY, lsum = 0.0f, acc[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.0f;
+    int p0 = 0, round = 0;
+    while (p0 < npg) {  // block-uniform rounds
+        int p1 = p0 + 1;
+        while (p1 < npg && s_toff[p1 + 1] - s_toff[p0] <= rows_cap) ++p1;
+        const int t0 = s_toff[p0], nrow = s_toff[p1] - t0;
+        if (warp == 0) {
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                // ICE_DEBUG_STALL_ATTN: expect 16 bytes that no copy delivers (tests of
+                // the bounded wait)
+                const unsigned extra = (v.debug & ICE_DEBUG_STALL_ATTN) ? 16u : 0u;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                             "r"((unsigned)(2 * nrow * ROWB) + extra)
+                             : "memory");
+            }
+            __syncwarp();
+            for (int i = p0 + lane; i < p1; i += 32) {
+                const int c = s_toff[i + 1] - s_toff[i];
+                if (c > 0) {
+                    const long long row0 = v.page_row(u, s_sel[r + K * i], 0);
+                    const unsigned off = (unsigned)(s_toff[i] - t0) * ROWB;
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            smem_u32(sk) + off),
+                        "l"(reinterpret_cast<const char*>(v.page_k) + row0 * ROWB), "r"((unsigned)c * ROWB),
+                        "r"(bar)
+                        : "memory");
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            smem_u32(sv) + off),
+                        "l"(reinterpret_cast<const char*>(v.page_v) + row0 * ROWB), "r"((unsigned)c * ROWB),
+                        "r"(bar)
+                        : "memory");
+                }
+            }
+        }
+        const bool ok = mbar_wait_bounded(bar, (unsigned)(round & 1));
+        if (!ok) {
+            *s_fail = 1;
+            set_status(v.status, ICE_ERR_TIMEOUT);
+            mbar_wait_bounded(bar, (unsigned)(round & 1));  // copies possibly still in flight
+        }
+        if (ok) {
+            for (int j = warp; j < nrow; j += kCW) {  // warp-uniform
+                float kx[DPL];
+#pragma unroll
+                for (int k = 0; k < DPL; k += 4) {
+                    float x[4];
+                    load4(sk + (size_t)j * kD + g * DPL + k, x);
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) kx[k + z] = x[z];
+                }
+                float2 s2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int k = 0; k < DPL; k += 2)
+                    s2 = __ffma2_rn(make_float2(qa[k], qa[k + 1]), make_float2(kx[k], kx[k + 1]), s2);
+                float s = s2.x + s2.y;
+#pragma unroll
+                for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                const float mn = fmaxf(m, s);
+                const float corr = exp2f(m - mn);
+                const float p = exp2f(s - mn);
+                lsum = lsum * corr + p;
+                const float2 c2 = make_float2(corr, corr), p2 = make_float2(p, p);
+#pragma unroll
+                for (int k = 0; k < DPL; k += 4) {
+                    float x[4];
+                    load4(sv + (size_t)j * kD + g * DPL + k, x);
+#pragma unroll
+                    for (int z = 0; z < 4; z += 2) {
+                        const float2 a = __ffma2_rn(p2, make_float2(x[z], x[z + 1]),
+                                                    __fmul2_rn(make_float2(acc[k + z], acc[k + z + 1]), c2));
+                        acc[k + z] = a.x;
+                        acc[k + z + 1] = a.y;
+                    }
+                }
+                m = mn;
+            }
+        }
+        __syncthreads();  // the round's rows are consumed before the next copies land
+        if (*s_fail) break;  // no further copies on a barrier whose phase may never complete
+        p0 = p1;
+        ++round;
+    }
+    float* part = reinterpret_cast<float*>(stage);  // [warp][head][kD + 2]
+    {
+        float* pw = part + (warp * G + h) * (kD + 2);
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) pw[g * DPL + k] = acc[k];
+        if (g == 0) {
+            pw[kD] = m;
+            pw[kD + 1] = lsum;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < G * kD; e += kCT) {
+        const int hh = e / kD, dcol = e % kD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) M = fmaxf(M, part[(w * G + hh) * (kD + 2) + kD]);
+        float Lt = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) {
+                const float* pw = part + (w * G + hh) * (kD + 2);
+                if (pw[kD] == -INFINITY) continue;
+                const float cf = exp2f(pw[kD] - M);
+                Lt = fmaf(pw[kD + 1], cf, Lt);
+                O = fmaf(pw[dcol], cf, O);
+            }
+        }
+        cpart[hh * (kD + 2) + dcol] = O;
+        if (dcol == 0) {
+            cpart[hh * (kD + 2) + kD] = M;
+            cpart[hh * (kD + 2) + kD + 1] = Lt;
+        }
+    }
+    if (tid == 0) reinterpret_cast<int*>(cpart)[G * (kD + 2)] = *s_fail;
+}
+
+template <typename T, int G, bool FUSED>
+__global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
+    IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int cand_cap, int hcap2, int rcap,
+    int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
+    int32_t* __restrict__ stats, T* __restrict__ attn_out) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(16) float2 s_qp[kD / 2];  // (q_sel[e], q_sel[e + 64]), e < 64
+    __shared__ int s_qcode[kM];
+    __shared__ __align__(16) __half2 s_width[97 * 4];
+    __shared__ int s_pstar, s_need, s_nch, s_tot, s_tt, s_ncand, s_nraw, s_npg, s_cmp, s_fail, s_gn;
+    __shared__ __align__(8) unsigned long long s_bar;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int K = (int)cluster.num_blocks();
+    const int r = (int)cluster.block_rank();
+    const int u = blockIdx.x / K;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int L = v.L, P = v.P;
+    const long long C = v.C;
+    const int Kc = K / L, l = r / Kc, rc = r % Kc;
+    const CluSmem lay = clu_layout(C, rcap, n_cand, cand_cap, hcap2, n_sel, K, G, 0);
+    int* s_sel = reinterpret_cast<int*>(smem + lay.sel);
+    int* s_scnt = reinterpret_cast<int*>(smem + lay.scnt);
+    int* s_toff = reinterpret_cast<int*>(smem + lay.toff);
+    uint4* pub = reinterpret_cast<uint4*>(smem + lay.pub);  // [K][n_sel] (key lo, key hi, page, cnt)
+    int* pubx = reinterpret_cast<int*>(smem + lay.pubx);    // [K][4] (entries, ncand, nraw, -)
+    unsigned* bm0 = reinterpret_cast<unsigned*>(smem + lay.bm0);
+    int* lhist = reinterpret_cast<int*>(smem + lay.lhist);
+    float* cpart = reinterpret_cast<float*>(smem + lay.cpart);
+    float* qf = reinterpret_cast<float*>(smem + lay.qf);
+    unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.skey);
+    int* sval = reinterpret_cast<int*>(smem + lay.sval);
+    int* hpage = reinterpret_cast<int*>(smem + lay.hpage);
+    unsigned long long* hkey = reinterpret_cast<unsigned long long*>(smem + lay.hkey);
+    int* hcnt = reinterpret_cast<int*>(smem + lay.hcnt);
+    unsigned long long* topk = reinterpret_cast<unsigned long long*>(smem + lay.top);
+    int* topv = reinterpret_cast<int*>(smem + lay.top + kCW * 32 * 8);
+    unsigned char* prio = smem + lay.prio;
+    unsigned char* cnts = smem + lay.cnt;
+    unsigned* tieb = reinterpret_cast<unsigned*>(smem + lay.tieb);
+    int* hist = reinterpret_cast<int*>(smem + lay.hist);
+    int* ghist = reinterpret_cast<int*>(smem + lay.ghist);
+    int* chosen = reinterpret_cast<int*>(smem + lay.chosen);
+    unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);
+    int* coff = reinterpret_cast<int*>(smem + lay.coff);
+    const int nwords0 = (int)((C + 31) / 32);
+
+    // ---- 1. leaf count, query heads and directions requested together ------------------
+    int Nl = v.n_leaf[v.ul(u, l)];
+    int Nall = 0;
+    if (r == 0)
+        for (int ll = 0; ll < L; ++ll) Nall += max(0, min(v.n_leaf[v.ul(u, ll)], (int)C));
+    float qh[G][4];
+    const T* qu = q + (long long)u * G * kD;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) load4(qu + (long long)hh * kD + 4 * lane, qh[hh]);
+    float wdir[4] = {0.f, 0.f, 0.f, 0.f};
+    float wlast = 0.f;
+    if (warp < kM) {
+        const float* ud = v.dirs + (long long)(l * kM + warp) * kDirStride;
+        load4(ud + 4 * lane, wdir);
+        wlast = ud[kD];
+    }
+    if (tid < 97) {
+        __half2 w[4];
+        cell_widths(tid, w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s_width[tid * 4 + k] = w[k];
+    }
+    for (int i = tid; i < kCSubH * kCHistRow; i += kCT) hist[i] = 0;
+    for (int i = tid; i < rcap / 32; i += kCT) tieb[i] = 0u;
+    if (r == 0 && L > 1)
+        for (int i = tid; i < nwords0; i += kCT) bm0[i] = 0u;
+    if (tid == 0) {
+        s_nch = 0;
+        s_tt = 0;
+        s_ncand = 0;
+        s_nraw = 0;
+        s_npg = 0;
+        s_fail = 0;
+        if (FUSED) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+    }
+    Nl = Nl < 0 ? 0 : (Nl > C ? (int)C : Nl);
+    // this block's leaves: 64-leaf chunks [c0, c1) of the composite, in position order
+    const int chunks = (Nl + 63) >> 6;
+    const int c0 = rc * chunks / Kc, c1 = (rc + 1) * chunks / Kc;
+    const int nck = c1 - c0;
+    const int lo_leaf = 64 * c0;
+    const int nloc = max(0, min(Nl, 64 * c1) - lo_leaf);
+    const unsigned long long* slo = v.leaf_lo + v.leaf_base(u, l) + lo_leaf;
+    const unsigned short* stc = v.leaf_tc + v.leaf_base(u, l) + lo_leaf;
+    const unsigned ring = smem_u32(smem + lay.A + warp * (kCRing * kCSlotB));
+    auto ring_issue = [&](int k, int slot) {
+        const unsigned d = ring + slot * kCSlotB;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + lane * 16),
+                     "l"(slo + 64 * k + 2 * lane)
+                     : "memory");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d + 512 + lane * 4),
+                     "l"(stc + 64 * k + 2 * lane)
+                     : "memory");
+    };
+#pragma unroll
+    for (int sidx = 0; sidx < kCRing; ++sidx) {
+        const int k = warp + sidx * kCW;
+        if (k < nck) ring_issue(k, sidx);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    // query prep: q_sel = sum of the heads in head order, q~ = q_sel / |q_sel|,
+    // codes of this block's composite (warp j: direction j)
+    {
+        float qs[4] = {qh[0][0], qh[0][1], qh[0][2], qh[0][3]};
+#pragma unroll
+        for (int hh = 1; hh < G; ++hh)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) qs[k] = __fadd_rn(qs[k], qh[hh][k]);
+        const float nq = warp_dot_fixed(qs, qs);
+        float qt[4] = {0.f, 0.f, 0.f, 0.f};
+        if (nq > 0.0f) {
+            const float sn = __fsqrt_rn(nq);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) qt[k] = __fdiv_rn(qs[k], sn);
+        }
+        if (warp < kM) {
+            const float p = __fmaf_rn(wlast, 0.0f, warp_dot_fixed(wdir, qt));
+            if (lane == 0) s_qcode[warp] = quantise_code(p);
+        }
+        if (warp == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = 4 * lane + k;
+                if (e < kD / 2) s_qp[e].x = qs[k];
+                else s_qp[e - kD / 2].y = qs[k];
+            }
+            if (FUSED) {
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) qf[hh * kD + 4 * lane + k] = qh[hh][k];
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- 2. priorities, counts and sub-histograms of this block's leaves ----------------
+    {
+        __half2 qc[4];
+        {
+            unsigned lo4 = 0, hi4 = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                lo4 |= (unsigned)s_qcode[j] << (8 * j);
+                hi4 |= (unsigned)s_qcode[4 + j] << (8 * j);
+            }
+            qc[0] = bytes_to_h2(lo4, 0x4140u);
+            qc[1] = bytes_to_h2(lo4, 0x4342u);
+            qc[2] = bytes_to_h2(hi4, 0x4140u);
+            qc[3] = bytes_to_h2(hi4, 0x4342u);
+        }
+        int* hl = hist + (lane & (kCSubH - 1)) * kCHistRow;
+        const unsigned pr_base = smem_u32(prio);
+        const unsigned cn_base = smem_u32(cnts);
+        int slot = 0;
+        for (int k = warp; k < nck; k += kCW) {  // warp-uniform
+            asm volatile("cp.async.wait_group %0;" ::"n"(kCRing - 1) : "memory");
+            const unsigned d = ring + slot * kCSlotB;
+            uint4 lo2;
+            unsigned tc2;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(lo2.x), "=r"(lo2.y), "=r"(lo2.z), "=r"(lo2.w)
+                         : "r"(d + lane * 16)
+                         : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tc2) : "r"(d + 512 + lane * 4) : "memory");
+            const int i0 = 64 * k + 2 * lane;
+            const unsigned tca = tc2 & 0xFFFFu, tcb = tc2 >> 16;
+            const int p0 = leaf_priority(lo2.x, lo2.y, tc_t(tca), qc, s_width);
+            const int p1 = leaf_priority(lo2.z, lo2.w, tc_t(tcb), qc, s_width);
+            const int cA = tc_cnt(tca), cB = tc_cnt(tcb);
+            if (i0 < nloc) {
+                st_shared_u16(pr_base + i0, p0 | (p1 << 8));
+                st_shared_u16(cn_base + i0, cA | (cB << 8));
+                atomicAdd(&hl[p0], cA);
+                if (i0 + 1 < nloc) atomicAdd(&hl[p1], cB);
+            }
+            const int kn = k + kCRing * kCW;
+            if (kn < nck) ring_issue(kn, slot);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            slot = slot + 1 == kCRing ? 0 : slot + 1;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+    __syncthreads();
+
+    // ---- 3a. the composite's histogram (over DSMEM when it is split) and pi* --------------
+    {
+        int hsum = 0;
+#pragma unroll
+        for (int sh = 0; sh < kCSubH; ++sh) hsum += hist[sh * kCHistRow + tid];
+        if (Kc > 1) {
+            lhist[tid] = hsum;
+            cluster.sync();
+            int gs = 0;
+            for (int rr = 0; rr < Kc; ++rr) gs += cluster.map_shared_rank(lhist, l * Kc + rr)[tid];
+            ghist[tid] = gs;
+        } else {
+            ghist[tid] = hsum;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int loc[8], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            loc[k] = ghist[lane * 8 + k];
+            sum += loc[k];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int excl = incl - sum;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= n_cand);
+        if (hit == 0u) {
+            if (lane == 0) {
+                s_pstar = 256;  // fewer than n_cand tokens in the composite: take every leaf
+                s_need = 0;
+            }
+        } else if (lane == __ffs(hit) - 1) {
+            int run = excl, k = 0;
+            while (run + loc[k] < n_cand) {
+                run += loc[k];
+                ++k;
+            }
+            s_pstar = lane * 8 + k;
+            s_need = n_cand - run;
+        }
+    }
+    __syncthreads();
+
+    // ---- 3b. leaves below pi* are taken; leaves at pi* are marked, their tokens summed ----
+    for (int i = tid; i < cand_cap; i += kCT) {  // the page table takes over the scan ring
+        hpage[i] = -1;
+        hkey[i] = ~0ull;
+    }
+    const uint4* lrec = v.leaf_rec + v.leaf_base(u, l) + lo_leaf;
+    {
+        const int ps = s_pstar;
+        const unsigned* p32 = reinterpret_cast<const unsigned*>(prio);
+        const unsigned* c32 = reinterpret_cast<const unsigned*>(cnts);
+        const int nw = (nloc + 3) >> 2;
+        int ttok = 0;
+        for (int w4 = tid; w4 < nw; w4 += kCT) {
+            const unsigned word = p32[w4];
+            const unsigned cword = c32[w4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int i = 4 * w4 + b;
+                if (i >= nloc) break;
+                const int pr = (int)((word >> (8 * b)) & 0xFFu);
+                if (pr < ps) {
+                    const int slot = atomicAdd(&s_nch, 1);
+                    if (slot < n_cand) {
+                        chosen[slot] = i;
+                        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                         smem_u32(cmeta + slot)),
+                                     "l"(&lrec[i].z)
+                                     : "memory");
+                    }
+                } else if (pr == ps) {
+                    atomicOr(&tieb[i >> 5], 1u << (i & 31));
+                    ttok += (int)((cword >> (8 * b)) & 0xFFu);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) ttok += __shfl_xor_sync(0xffffffffu, ttok, o);
+        if (lane == 0 && ttok) atomicAdd(&s_tt, ttok);
+    }
+    __syncthreads();
+    // ties of the blocks before this one (position order) count against the need
+    int need = s_need;
+    if (Kc > 1) {
+        cluster.sync();
+        int before = 0;
+        for (int rr = 0; rr < rc; ++rr) before += *cluster.map_shared_rank(&s_tt, l * Kc + rr);
+        need = max(0, need - before);
+    }
+    // ---- 3c. this block's ties in position order while the tokens taken before them < need
+    // ---- 3d. slot offsets of the taken leaves (counts from the scan's bytes)
+    if (warp == 0) {
+        const int nwords = (nloc + 31) >> 5;
+        const int nbelow = min(s_nch, n_cand);
+        int run = 0, ntaken = 0;
+        for (int w0 = 0; w0 < nwords && run < need; w0 += 32) {
+            const int wi = w0 + lane;
+            const unsigned bits = wi < nwords ? tieb[wi] : 0u;
+            uint4 ca = make_uint4(0u, 0u, 0u, 0u), cb = ca;
+            if (bits) {
+                ca = *reinterpret_cast<const uint4*>(cnts + wi * 32);
+                cb = *reinterpret_cast<const uint4*>(cnts + wi * 32 + 16);
+            }
+            const unsigned cw[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+            unsigned tsum = 0u;
+#pragma unroll
+            for (int qd = 0; qd < 8; ++qd)
+                tsum = __dp4a(cw[qd] & nibble_bytes((bits >> (4 * qd)) & 0xFu), 0x01010101u, tsum);
+            const int tot = (int)tsum;
+            int inc = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            int acc = run + inc - tot, mine = 0;
+            unsigned take = 0u;
+            if (acc + tot <= need) {
+                take = bits;
+                mine = __popc(bits);
+            } else {
+                for (unsigned bb = bits; bb && acc < need; bb &= bb - 1u) {
+                    const int bit = __ffs(bb) - 1;
+                    take |= 1u << bit;
+                    acc += (int)((byte_word(cw, bit >> 2) >> (8 * (bit & 3))) & 0xFFu);
+                    ++mine;
+                }
+            }
+            int tinc = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, tinc, o);
+                if (lane >= o) tinc += y;
+            }
+            int slot = nbelow + ntaken + tinc - mine;
+            for (unsigned bb = take; bb; bb &= bb - 1u, ++slot)
+                if (slot < n_cand) {
+                    const int i = wi * 32 + __ffs(bb) - 1;
+                    chosen[slot] = i;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(cmeta + slot)),
+                                 "l"(&lrec[i].z)
+                                 : "memory");
+                }
+            ntaken += __shfl_sync(0xffffffffu, tinc, 31);
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        __syncwarp();
+        const int nch = min(nbelow + ntaken, n_cand);
+        int carry = 0;
+        for (int k0 = 0; k0 < nch; k0 += 32) {
+            const int k = k0 + lane;
+            const int c = k < nch ? (int)cnts[chosen[k]] : 0;
+            int inc = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (k < nch) coff[k] = carry + inc - c;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) {
+            coff[nch] = carry;
+            s_tot = carry;
+            s_nch = nbelow + ntaken;
+        }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // the taken leaves' records
+    __syncthreads();
+    const int nch = min(s_nch, n_cand);
+    // composite-0 pages taken whole, in block 0's bitmap
+    if (L > 1) {
+        if (l == 0) {
+            unsigned* bm0r = cluster.map_shared_rank(bm0, 0);
+            for (int k = tid; k < nch; k += kCT) {
+                const int id = (int)(cmeta[k] >> 8);
+                if (id < C) atomicOr(&bm0r[id >> 5], 1u << (id & 31));
+            }
+        }
+        cluster.sync();
+    }
+
+    // ---- 4. candidate expansion: every (leaf, slot) of this block at once -----------------
+    {
+        const int total = s_tot;
+        if (tid == 0) s_nraw = total;
+        const unsigned* bm0r = L > 1 ? cluster.map_shared_rank(bm0, 0) : nullptr;
+        for (int j0 = warp * 32; j0 < total; j0 += kCT) {
+            const int j = j0 + lane;
+            bool keep = false;
+            int tok = 0, loc = 0;
+            if (j < total) {
+                int lo = 0, hi = nch;  // last k with coff[k] <= j
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (coff[mid] <= j) lo = mid; else hi = mid;
+                }
+                const int slot = j - coff[lo];
+                const int id = (int)(cmeta[lo] >> 8);
+                if (id < C && slot < P) {
+                    tok = v.slot_tok[v.slot_base(u, l) + (long long)id * P + slot];
+                    if (l == 0) {
+                        loc = id * P + slot;
+                        keep = true;
+                    } else {
+                        loc = v.slot_loc1[v.loc1_base(u) + (long long)id * P + slot];
+                        const int pg = loc >= 0 ? loc / P : 0;
+                        keep = tok >= 0 && loc >= 0 && pg < C && !((bm0r[pg >> 5] >> (pg & 31)) & 1u);
+                    }
+                }
+            }
+            const unsigned km = __ballot_sync(0xffffffffu, keep);
+            int pos0 = 0;
+            if (lane == 0 && km) pos0 = atomicAdd(&s_ncand, __popc(km));
+            pos0 = __shfl_sync(0xffffffffu, pos0, 0);
+            if (keep) {
+                const int pos = pos0 + __popc(km & ((1u << lane) - 1u));
+                if (pos < cand_cap) {
+                    skey[pos] = (unsigned long long)(unsigned)tok;
+                    sval[pos] = loc;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int ncand = min(s_ncand, cand_cap);
+
+    // ---- 5. exact rescoring of this block's candidates; per-page minimum key --------------
+    {
+        constexpr int EPC = 16 / (int)sizeof(T);
+        constexpr int CPR = kD / EPC;
+        constexpr int ROWB = kD * (int)sizeof(T);
+        unsigned char* stg = smem + lay.B;
+        const int half = min((smem_total - lay.B) / (2 * ROWB), kCT / 2);
+        const int nchunk = (ncand + half - 1) / half;
+        const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
+        const int hmask = cand_cap - 1;
+        auto issue = [&](int ch) {
+            if (ch < nchunk) {
+                const int rb = ch * half, nr = min(half, ncand - rb);
+                unsigned char* buf = stg + (ch & 1) * half * ROWB;
+                for (int k = tid; k < nr * CPR; k += kCT) {
+                    const int rr = k / CPR, c = k % CPR;
+                    const int pos = c ^ ((rr & (CPR / 2 - 1)) << 1);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                     smem_u32(buf + rr * ROWB + 16 * pos)),
+                                 "l"(pk + (long long)sval[rb + rr] * ROWB + 16 * c)
+                                 : "memory");
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        issue(0);
+        issue(1);
+        for (int ch = 0; ch < nchunk; ++ch) {  // block-uniform
+            const int rb0 = ch * half, nr = min(half, ncand - rb0);
+            const unsigned char* stgc = stg + (ch & 1) * half * ROWB;
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            __syncthreads();
+            const int rr = tid >> 1, t = tid & 1;
+            const bool ok = rr < nr;
+            const int sw = (rr & (CPR / 2 - 1)) << 1;
+            int pg = -1;
+            unsigned long long key = ~0ull;
+            float s4[2] = {0.0f, 0.0f};
+            if (ok) {
+                const unsigned char* rowp = stgc + rr * ROWB;
+                float s16[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int ln = ((j >> 1) << 2) | (t << 1) | (j & 1);
+                    const int e0 = 4 * ln, e1 = 4 * (ln + 16);
+                    const int cc0 = e0 / EPC, cc1 = e1 / EPC;
+                    float x0[EPC], x1[EPC];
+                    load_chunk<T>(rowp + 16 * (cc0 ^ sw), x0);
+                    load_chunk<T>(rowp + 16 * (cc1 ^ sw), x1);
+                    const int o0 = e0 % EPC, o1 = e1 % EPC;
+                    float2 ab = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        ab = __ffma2_rn(s_qp[e0 + i], make_float2(x0[o0 + i], x1[o1 + i]), ab);
+                    s16[j] = __fadd_rn(ab.x, ab.y);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) s16[j] = __fadd_rn(s16[j], s16[j + 4]);
+                s4[0] = __fadd_rn(s16[0], s16[2]);
+                s4[1] = __fadd_rn(s16[1], s16[3]);
+            }
+            {
+                const float p0 = __shfl_xor_sync(0xffffffffu, s4[0], 1);
+                const float p1 = __shfl_xor_sync(0xffffffffu, s4[1], 1);
+                const float a0 = t ? p0 : s4[0], a2 = t ? s4[0] : p0;
+                const float a1 = t ? p1 : s4[1], a3 = t ? s4[1] : p1;
+                const float sc = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
+                if (ok) {
+                    pg = sval[rb0 + rr] / P;
+                    key = ((unsigned long long)score_key_desc(sc) << 32) | (unsigned)skey[rb0 + rr];
+                }
+            }
+#pragma unroll
+            for (int o = 2; o < 32; o <<= 1) {
+                const int opg = __shfl_up_sync(0xffffffffu, pg, o);
+                const unsigned long long okey = __shfl_up_sync(0xffffffffu, key, o);
+                if (lane >= o && opg == pg && okey < key) key = okey;
+            }
+            const int next_pg = __shfl_down_sync(0xffffffffu, pg, 2);
+            bool fresh = false;
+            if (ok && t == 0 && (lane >= 30 || next_pg != pg)) {
+                unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
+                for (int probe = 0; probe < cand_cap; ++probe) {
+                    const int old = atomicCAS(&hpage[hh], -1, pg);
+                    if (old == -1 || old == pg) {
+                        fresh = old == -1;
+                        if (fresh)  // the page's token count travels with it to the attention
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(hcnt + hh)),
+                                         "l"(v.list_cnt + v.leaf_base(u, 0) + pg)
+                                         : "memory");
+                        atomicMin(&hkey[hh], key);
+                        break;
+                    }
+                    hh = (hh + 1) & (unsigned)hmask;
+                }
+            }
+            {
+                const unsigned nf = __ballot_sync(0xffffffffu, fresh);
+                if (lane == 0 && nf) atomicAdd(&s_npg, __popc(nf));
+            }
+            __syncthreads();
+            issue(ch + 2);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+    __syncthreads();
+
+    // ---- 6. this block's n_sel best pages, published to block 0 ---------------------------
+    if (tid == 0) s_cmp = 0;
+    __syncthreads();
+    for (int h0 = warp * 32; h0 < cand_cap; h0 += kCT) {  // warp-uniform
+        const int hh = h0 + lane;
+        const int pg = hh < cand_cap ? hpage[hh] : -1;
+        const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
+        int base = 0;
+        if (lane == 0 && km) base = atomicAdd(&s_cmp, __popc(km));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (pg >= 0) {
+            const int pos = base + __popc(km & ((1u << lane) - 1u));
+            skey[pos] = hkey[hh];
+            sval[pos] = hh;
+        }
+    }
+    __syncthreads();
+    {
+        const int npl = s_cmp;
+        unsigned long long tk;
+        int tv;
+        block_top32(skey, sval, npl, topk, topv, tk, tv);
+        const int ntop = min(n_sel, npl);
+        if (warp == 0) {
+            uint4* pub0 = cluster.map_shared_rank(pub, 0);
+            if (lane < ntop)
+                pub0[r * n_sel + lane] = make_uint4((unsigned)tk, (unsigned)(tk >> 32),
+                                                    (unsigned)hpage[tv], (unsigned)hcnt[tv]);
+            if (lane == 0) {
+                int* px = cluster.map_shared_rank(pubx, 0);
+                px[r * 4 + 0] = ntop;
+                px[r * 4 + 1] = ncand;
+                px[r * 4 + 2] = s_nraw;
+            }
+        }
+    }
+    cluster.sync();
+
+    // ---- 7. the selection: the n_sel smallest published keys, one per page -----------------
+    {
+        int* g_page = reinterpret_cast<int*>(smem + lay.g_page);
+        unsigned long long* g_key = reinterpret_cast<unsigned long long*>(smem + lay.g_key);
+        int* g_cnt = reinterpret_cast<int*>(smem + lay.g_cnt);
+        unsigned long long* g_ckey = reinterpret_cast<unsigned long long*>(smem + lay.g_ckey);
+        int* g_cidx = reinterpret_cast<int*>(smem + lay.g_cidx);
+        unsigned long long* gtk = reinterpret_cast<unsigned long long*>(smem + lay.g_top);
+        int* gtv = reinterpret_cast<int*>(smem + lay.g_top + kCW * 32 * 8);
+        for (int i = tid; i < hcap2; i += kCT) {
+            g_page[i] = -1;
+            g_key[i] = ~0ull;
+        }
+        if (tid == 0) s_gn = 0;
+        __syncthreads();
+        const uint4* pub0 = cluster.map_shared_rank(pub, 0);
+        const int* px = cluster.map_shared_rank(pubx, 0);
+        const int gmask = hcap2 - 1;
+        for (int e = tid; e < K * n_sel; e += kCT) {
+            const int rr = e / n_sel, i = e % n_sel;
+            if (i < px[rr * 4]) {
+                const uint4 x = pub0[rr * n_sel + i];
+                const unsigned long long key = ((unsigned long long)x.y << 32) | x.x;
+                const int pg = (int)x.z;
+                unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
+                for (int probe = 0; probe < hcap2; ++probe) {
+                    const int old = atomicCAS(&g_page[hh], -1, pg);
+                    if (old == -1 || old == pg) {
+                        if (old == -1) g_cnt[hh] = (int)x.w;
+                        atomicMin(&g_key[hh], key);
+                        break;
+                    }
+                    hh = (hh + 1) & (unsigned)gmask;
+                }
+            }
+        }
+        __syncthreads();
+        for (int h0 = warp * 32; h0 < hcap2; h0 += kCT) {
+            const int hh = h0 + lane;
+            const int pg = hh < hcap2 ? g_page[hh] : -1;
+            const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
+            int base = 0;
+            if (lane == 0 && km) base = atomicAdd(&s_gn, __popc(km));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (pg >= 0) {
+                const int pos = base + __popc(km & ((1u << lane) - 1u));
+                g_ckey[pos] = g_key[hh];
+                g_cidx[pos] = hh;
+            }
+        }
+        __syncthreads();
+        const int gn = s_gn;
+        unsigned long long tk;
+        int tv;
+        block_top32(g_ckey, g_cidx, gn, gtk, gtv, tk, tv);
+        const int taken = min(n_sel, gn);
+        if (warp == 0 && lane < n_sel) {
+            const int pg = lane < taken ? g_page[tv] : -1;
+            const int c = lane < taken ? g_cnt[tv] : 0;
+            s_sel[lane] = pg;
+            s_scnt[lane] = c;
+            if (r == 0) page_ids[(long long)u * n_sel + lane] = pg;
+        }
+        if (r == 0 && warp == 0) {
+            int tok_sel = lane < taken ? g_cnt[tv] : 0;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
+            int nc = 0, nr = 0;
+            if (lane < K) {
+                nc = px[lane * 4 + 1];
+                nr = px[lane * 4 + 2];
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                nc += __shfl_xor_sync(0xffffffffu, nc, o);
+                nr += __shfl_xor_sync(0xffffffffu, nr, o);
+            }
+            if (lane == 0) {
+                n_pages_out[u] = taken;
+                if (stats) {
+                    stats[4 * u + 0] = Nall;
+                    stats[4 * u + 1] = nc;
+                    stats[4 * u + 2] = tok_sel;
+                    stats[4 * u + 3] = nr;
+                }
+            }
+        }
+        if (tid == 0) s_gn = taken;
+        if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
+    }
+    __syncthreads();
+
+    // ---- 8. attention over this block's pages; partials merged over the cluster ------------
+    if constexpr (FUSED) {
+        const int taken = s_gn;
+        attend_partial<T, G>(v, u, qf, s_sel, s_scnt, taken, r, K, s_toff, smem + lay.A,
+                             smem_total - lay.A, smem_u32(&s_bar), &s_fail, cpart);
+        cluster.sync();
+        const int E = G * kD;
+        const int e0 = r * E / K, e1 = (r + 1) * E / K;
+        T* ou = attn_out + (long long)u * G * kD;
+        for (int e = e0 + tid; e < e1; e += kCT) {
+            const int hh = e / kD, dcol = e % kD;
+            float M = -INFINITY;
+            int fail = 0;
+            for (int rr = 0; rr < K; ++rr) {
+                const float* cp = cluster.map_shared_rank(cpart, rr);
+                M = fmaxf(M, cp[hh * (kD + 2) + kD]);
+                fail |= reinterpret_cast<const int*>(cp)[G * (kD + 2)];
+            }
+            float Lt = 0.0f, O = 0.0f;
+            if (M != -INFINITY && !fail) {
+                for (int rr = 0; rr < K; ++rr) {
+                    const float* cp = cluster.map_shared_rank(cpart, rr);
+                    const float mr = cp[hh * (kD + 2) + kD];
+                    if (mr == -INFINITY) continue;
+                    const float cf = exp2f(mr - M);
+                    Lt = fmaf(cp[hh * (kD + 2) + kD + 1], cf, Lt);
+                    O = fmaf(cp[hh * (kD + 2) + dcol], cf, O);
+                }
+            }
+            ou[e] = from_f<T>(Lt > 0.0f ? O / Lt : 0.0f);
+        }
+    }
+    cluster.sync();  // no block leaves while another still reads its shared memory
+}
+
+// ---- host side -------------------------------------------------------------------------
+
+namespace {
+
+struct CluPlan {
+    int K = 1, cand_cap = 0, hcap2 = 0, rcap = 0, bytes = 0;
+};
+
+int pow2_at_least(int x) {
+    int c = 1;
+    while (c < x) c <<= 1;
+    return c;
+}
+
+CluPlan clu_plan(const IndexView& v, int K, int n_sel, int n_cand, bool fused, int target_bytes) {
+    CluPlan p;
+    p.K = K;
+    const int L = v.L, P = v.P;
+    const int Kc = K / L;
+    p.cand_cap = pow2_at_least(n_cand + P - 1);
+    p.hcap2 = pow2_at_least(2 * K * n_sel + 1);
+    const long long ch = (v.C + 63) / 64;
+    p.rcap = (int)(64 * ((ch + Kc - 1) / Kc));
+    const int es = v.dtype == ICE_BF16 ? 2 : 4;
+    const CluSmem lay = clu_layout(v.C, p.rcap, n_cand, p.cand_cap, p.hcap2, n_sel, K, v.G, 0);
+    int need = lay.end;
+    // the rescoring stages at least two rows, the attention at least one page's
+    // K and V rows and then the warps' partials
+    need = std::max(need, lay.B + 2 * 2 * kD * es);
+    if (fused) {
+        need = std::max(need, lay.A + 2 * P * kD * es);
+        need = std::max(need, lay.A + kCW * v.G * (kD + 2) * 4);
+    }
+    p.bytes = std::max(need, target_bytes);
+    if (need > kCluSmemMax) p.bytes = need;  // refused by the caller
+    else p.bytes = std::min(p.bytes, kCluSmemMax);
+    return p;
+}
+
+template <typename T, int G, bool F>
+cudaError_t clu_launch(const IndexView& v, const CluPlan& p, const void* q, int n_sel, int n_cand,
+                       int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                       cudaStream_t s) {
+    auto kern = select_cluster_kernel<T, G, F>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(v.U * p.K));
+    cfg.blockDim = dim3(kCT);
+    cfg.dynamicSmemBytes = (size_t)p.bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)p.K;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, v, (const T*)q, n_sel, n_cand, p.cand_cap, p.hcap2, p.rcap,
+                              p.bytes, page_ids, n_pages, stats, (T*)out);
+}
+
+template <typename T, int G, bool F>
+cudaError_t clu_prepare_one() {
+    auto kern = select_cluster_kernel<T, G, F>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCluSmemMax);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+// Whether clusters of p.K blocks with p.bytes of shared memory can be resident
+// at all (cached per configuration).
+template <typename T, int G, bool F>
+bool clu_fits(const IndexView& v, const CluPlan& p) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int>, bool> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(p.K, p.bytes);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(v.U * p.K));
+    cfg.blockDim = dim3(kCT);
+    cfg.dynamicSmemBytes = (size_t)p.bytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)p.K;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, select_cluster_kernel<T, G, F>, &cfg);
+    if (e != cudaSuccess) cudaGetLastError();
+    const bool ok = e == cudaSuccess && n > 0;
+    cache[key] = ok;
+    return ok;
+}
+
+template <typename T, bool F>
+cudaError_t clu_dispatch_g(const IndexView& v, const CluPlan& p, const void* q, int n_sel,
+                           int n_cand, int32_t* page_ids, int32_t* n_pages, int32_t* stats,
+                           void* out, cudaStream_t s, bool check_only, bool* fits) {
+    switch (v.G) {
+#define ICE_CLU_G(GG)                                                                              \
+    case GG:                                                                                       \
+        if (check_only) {                                                                          \
+            *fits = clu_fits<T, GG, F>(v, p);                                                      \
+            return cudaSuccess;                                                                    \
+        }                                                                                          \
+        return clu_launch<T, GG, F>(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+        ICE_CLU_G(1) ICE_CLU_G(2) ICE_CLU_G(4) ICE_CLU_G(8)
+#undef ICE_CLU_G
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t clu_dispatch(const IndexView& v, const CluPlan& p, const void* q, int n_sel, int n_cand,
+                         int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                         cudaStream_t s, bool check_only, bool* fits) {
+    const bool fused = out != nullptr;
+    if (v.dtype == ICE_BF16)
+        return fused ? clu_dispatch_g<__nv_bfloat16, true>(v, p, q, n_sel, n_cand, page_ids, n_pages,
+                                                            stats, out, s, check_only, fits)
+                     : clu_dispatch_g<__nv_bfloat16, false>(v, p, q, n_sel, n_cand, page_ids, n_pages,
+                                                             stats, out, s, check_only, fits);
+    return fused ? clu_dispatch_g<float, true>(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out,
+                                               s, check_only, fits)
+                 : clu_dispatch_g<float, false>(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out,
+                                                s, check_only, fits);
+}
+
+}  // namespace
+
+cudaError_t select_cluster_prepare() {
+    cudaError_t e = cudaSuccess;
+#define ICE_CLU_PREP(T, G)                                        \
+    if (e == cudaSuccess) e = clu_prepare_one<T, G, true>();      \
+    if (e == cudaSuccess) e = clu_prepare_one<T, G, false>();
+    ICE_CLU_PREP(__nv_bfloat16, 1) ICE_CLU_PREP(__nv_bfloat16, 2) ICE_CLU_PREP(__nv_bfloat16, 4)
+    ICE_CLU_PREP(__nv_bfloat16, 8) ICE_CLU_PREP(float, 1) ICE_CLU_PREP(float, 2)
+    ICE_CLU_PREP(float, 4) ICE_CLU_PREP(float, 8)
+#undef ICE_CLU_PREP
+    return e;
+}
+
+// Shared memory a block is given beyond its tables (room to stage candidate rows
+// and pages): two blocks per SM for launches of up to two blocks per SM, four
+// blocks per SM above that.
+int clu_target_bytes(int blocks) { return blocks <= 304 ? 100 * 1024 : 54 * 1024; }
+
+// Cluster size for U units: enough blocks to cover the SMs about twice, at
+// most 16 blocks per unit; 1 (the one-block kernel) for large launches.
+int select_cluster_auto(int U, int L) {
+    int K = 1;
+    if (U <= 9) K = 16;
+    else if (U <= 19) K = 8;
+    else if (U <= 38) K = 4;
+    else if (U <= 152) K = 2;
+    if (K < L) K = 1;
+    return K;
+}
+
+int select_cluster_bytes(const IndexView& v, int K, int n_sel, int n_cand, bool fused) {
+    if (K < 2 || K > 16 || (K & (K - 1)) || K < v.L || n_sel > kCTop) return -1;
+    const CluPlan p = clu_plan(v, K, n_sel, n_cand, fused, clu_target_bytes(v.U * K));
+    return p.bytes > kCluSmemMax ? -1 : p.bytes;
+}
+
+cudaError_t launch_select_cluster(const IndexView& v, int K, const void* q, int n_sel, int n_cand,
+                                  int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
+                                  cudaStream_t s, bool* launched) {
+    *launched = false;
+    const bool fused = out != nullptr;
+    if (select_cluster_bytes(v, K, n_sel, n_cand, fused) < 0) return cudaSuccess;
+    const CluPlan p = clu_plan(v, K, n_sel, n_cand, fused, clu_target_bytes(v.U * K));
+    bool fits = false;
+    cudaError_t e = clu_dispatch(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out, s, true, &fits);
+    if (e != cudaSuccess || !fits) return e;
+    e = clu_dispatch(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out, s, false, &fits);
+    if (e == cudaSuccess) *launched = true;
+    return e;
+}
+
+}  // namespace ice

@@ -38,7 +38,7 @@ ICE_BF16 = 1
 EXPORTS = ["ice_build", "ice_insert", "ice_select", "ice_select_attn", "ice_sparse_attn", "ice_get_error",
            "ice_destroy", "ice_status_string", "ice_get_info", "ice_debug_dump", "ice_debug_page",
            "ice_key_codes_noalloc", "ice_select_attn_reuse", "ice_reuse_reset",
-           "ice_debug_set_flags", "ice_select_heads", "ice_decode_step"]
+           "ice_debug_set_flags", "ice_select_heads", "ice_decode_step", "ice_set_cluster_size"]
 
 
 class ice_params(ctypes.Structure):
@@ -112,6 +112,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ice_select_heads.restype = ctypes.c_int
     lib.ice_debug_set_flags.argtypes = [vp, i32]
     lib.ice_debug_set_flags.restype = ctypes.c_int
+    lib.ice_set_cluster_size.argtypes = [vp, i32]
+    lib.ice_set_cluster_size.restype = ctypes.c_int
     return lib
 
 
@@ -254,6 +256,11 @@ class IceIndex:
         """ice_debug_set_flags (tests only): DEBUG_STALL_ATTN forces the fused call's
         bounded wait to run out."""
         _check(_lib.ice_debug_set_flags(self._h, int(flags)), "ice_debug_set_flags")
+
+    def set_cluster_size(self, k: int):
+        """ice_set_cluster_size: blocks per unit of the selection (0 automatic, 1, 2,
+        4, 8 or 16)."""
+        _check(_lib.ice_set_cluster_size(self._h, int(k)), "ice_set_cluster_size")
 
     def decode_step(self, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, token_budget: int,
                     page_ids: torch.Tensor, n_pages: torch.Tensor, out: torch.Tensor, stream=None):
