@@ -19,10 +19,18 @@ def ice():
 
 
 def _dump_equal(a, b):
+    """The meaningful parts of two dumps are equal: the first n_leaf leaf records,
+    the first next_id lists, and in each list the slots below its count (the
+    rest of the capacity is never written and holds whatever the allocation did)."""
     assert a["n"] == b["n"] and a["n_leaf"] == b["n_leaf"] and a["next_id"] == b["next_id"]
-    for ca, cb in zip(a["comp"], b["comp"]):
-        for key in ("pm", "pt", "t", "lo", "id", "cnt", "list_cnt", "slot_tok", "slot_key"):
-            assert np.array_equal(ca[key], cb[key]), key
+    for l, (ca, cb) in enumerate(zip(a["comp"], b["comp"])):
+        N, NL = a["n_leaf"][l], a["next_id"][l]
+        for key in ("pm", "pt", "t", "lo", "id", "cnt"):
+            assert np.array_equal(ca[key][:N], cb[key][:N]), key
+        assert np.array_equal(ca["list_cnt"][:NL], cb["list_cnt"][:NL])
+        used = np.arange(a["P"])[None, :] < ca["list_cnt"][:NL, None]
+        for key in ("slot_tok", "slot_key"):
+            assert np.array_equal(ca[key][:NL][used], cb[key][:NL][used]), key
     assert np.array_equal(a["tok_loc"], b["tok_loc"])
 
 
@@ -112,7 +120,10 @@ def test_fused_decode_step_equals_separate_calls(ice, dtype):
             orcs[u].insert(k.view(-1, w.d)[u], v.view(-1, w.d)[u])
         torch.cuda.synchronize()
         assert torch.equal(ids_f, ids_s) and torch.equal(npg_f, npg_s), t
-        assert torch.equal(out_f, out_s), t
+        # the separate call may attend with a cluster of blocks per unit, which
+        # merges the softmax partials in another order
+        d = float((out_f.float() - out_s.float()).abs().max())
+        assert d <= (4e-2 if dtype == torch.bfloat16 else 2e-5), (t, d)
         if t % 30 == 29:
             for u in range(U):
                 compare_index(fused.dump(u), orcs[u], f"step {t} unit {u}")
