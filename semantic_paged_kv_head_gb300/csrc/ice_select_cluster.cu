@@ -50,69 +50,92 @@ constexpr int kCW = kCT / 32;      // warps per block
 constexpr int kCSubH = 8;          // sub-histograms (lane groups)
 constexpr int kCHistRow = 257;     // words per sub-histogram row
 constexpr int kCRing = 3;          // scan chunks in flight per warp
-constexpr int kCSlotB = 640;       // one chunk: 64 corners (8 B) + 64 (t | count << 7) (2 B)
+constexpr int kCSlotB = 1024;      // one chunk: 64 leaf records of 16 B
 constexpr int kCRingB = kCW * kCRing * kCSlotB;
 constexpr int kCTop = 32;          // largest n_sel of the cluster path (warp top-32 ranking)
 constexpr int kCluSmemMax = 220 * 1024;
 
 struct CluSmem {
-    int sel, scnt, toff, pub, pubx, bm0, lhist, cpart, qf;  // live through the kernel
-    int A;                                                  // ring / candidates / ranking / staging
-    int skey, sval, hpage, hkey, hcnt, top;                 // local candidates and page table
-    int g_page, g_key, g_cnt, g_ckey, g_cidx, g_top;        // global ranking
-    int B;                                                  // scan tables; rescoring staging
-    int prio, cnt, tieb, hist, ghist, chosen, cmeta, coff;
+    // live through the kernel; the hub fields are written by every block into
+    // block 0 and read there
+    int sel, scnt, toff, lhist, hubx, hub_leaf, hub_pe, hub_part, qf, bm0;
+    int X;  // phase region: scan tables, then candidates, then ranking, then attention staging
+    int ring, prio, cnt, lid, tieb, hist, ghist, gpre, chosen, cmeta;  // scan
+    int tl, toffc, skey, sval, hpage, hkey, hcnt, top, stage;     // candidates (stage: rows)
+    int g_page, g_key, g_cnt, gk, gp, gc, gtop;                   // ranking
     int end;
 };
 
-__host__ __device__ inline CluSmem clu_layout(long long C, int rcap, int n_cand, int cand_cap,
-                                              int hcap2, int n_sel, int K, int G, int min_total) {
+struct CluDims {
+    int rcap;       // leaves of a block's scan range (multiple of 64)
+    int n_cand;     // candidates per composite
+    int s_tot;      // candidate slots of a unit, all composites: L (n_cand + P - 1)
+    int share_cap;  // candidate slots of one block: ceil(s_tot / K)
+    int hcap_l;     // a block's page table (power of two > share_cap)
+    int gcap;       // the ranking's page table (power of two > 2 K n_sel)
+};
+
+__host__ __device__ inline CluSmem clu_layout(long long C, const CluDims& d, int L, int n_sel,
+                                              int K, int G, bool fused, int min_total) {
     CluSmem s;
     int o = 0;
     s.sel = o; o = align16(o + kCTop * 4);
     s.scnt = o; o = align16(o + kCTop * 4);
     s.toff = o; o = align16(o + (kCTop + 1) * 4);
-    s.pub = o; o = align16(o + K * n_sel * 16);
-    s.pubx = o; o = align16(o + K * 4 * 4);
-    s.bm0 = o; o = align16(o + (int)((C + 31) / 32) * 4);
     s.lhist = o; o = align16(o + 256 * 4);
-    s.cpart = o; o = align16(o + (G * (kD + 2) + 4) * 4);
-    s.qf = o; o = align16(o + G * kD * 4);
-    s.A = o;
-    int a = o;
-    s.skey = a; a = align16(a + cand_cap * 8);
-    s.sval = a; a = align16(a + cand_cap * 4);
-    s.hpage = a; a = align16(a + cand_cap * 4);
-    s.hkey = a; a = align16(a + cand_cap * 8);
-    s.hcnt = a; a = align16(a + cand_cap * 4);
-    s.top = a; a = align16(a + kCW * 32 * 12);
-    int g = o;
-    s.g_page = g; g = align16(g + hcap2 * 4);
-    s.g_key = g; g = align16(g + hcap2 * 8);
-    s.g_cnt = g; g = align16(g + hcap2 * 4);
-    s.g_ckey = g; g = align16(g + hcap2 * 8);
-    s.g_cidx = g; g = align16(g + hcap2 * 4);
-    s.g_top = g; g = align16(g + kCW * 32 * 12);
-    int b = o + kCRingB;
-    b = a > b ? a : b;
-    b = g > b ? g : b;
-    s.B = b;
-    o = b;
-    s.prio = o; o = align16(o + rcap);
-    s.cnt = o; o = align16(o + rcap);
-    s.tieb = o; o = align16(o + (rcap / 32) * 4);
-    s.hist = o; o = align16(o + kCSubH * kCHistRow * 4);
-    s.ghist = o; o = align16(o + 256 * 4);
-    s.chosen = o; o = align16(o + n_cand * 4);
-    s.cmeta = o; o = align16(o + n_cand * 4);
-    s.coff = o; o = align16(o + (n_cand + 1) * 4);
-    s.end = o > min_total ? o : min_total;
+    s.hubx = o; o = align16(o + 32 * 4);
+    s.hub_leaf = o; o = align16(o + L * d.n_cand * 4);
+    s.hub_pe = o; o = align16(o + K * n_sel * 16);
+    s.hub_part = o; o = align16(o + (fused ? K * (G * (kD + 2) + 4) * 4 : 0));
+    s.qf = o; o = align16(o + (fused ? G * kD * 4 : 0));
+    s.bm0 = o; o = align16(o + (L > 1 ? (int)((C + 31) / 32) * 4 : 0));
+    s.X = o;
+    int a = o;  // scan
+    s.ring = a; a = align16(a + kCRingB);
+    s.prio = a; a = align16(a + d.rcap);
+    s.cnt = a; a = align16(a + d.rcap);
+    s.lid = a; a = align16(a + d.rcap * 4);
+    s.tieb = a; a = align16(a + (d.rcap / 32) * 4);
+    s.hist = a; a = align16(a + kCSubH * kCHistRow * 4);
+    s.ghist = a; a = align16(a + 256 * 4);
+    s.gpre = a; a = align16(a + 256 * 4);
+    s.chosen = a; a = align16(a + d.n_cand * 4);
+    s.cmeta = a; a = align16(a + d.n_cand * 4);
+    int b = o;  // candidates
+    s.tl = b; b = align16(b + L * d.n_cand * 4);
+    s.toffc = b; b = align16(b + (L * d.n_cand + 1) * 4);
+    s.skey = b; b = align16(b + d.share_cap * 8);
+    s.sval = b; b = align16(b + d.share_cap * 4);
+    s.hpage = b; b = align16(b + d.hcap_l * 4);
+    s.hkey = b; b = align16(b + d.hcap_l * 8);
+    s.hcnt = b; b = align16(b + d.hcap_l * 4);
+    s.top = b; b = align16(b + kCW * 32 * 12);
+    s.stage = b;
+    int g = o;  // ranking
+    s.g_page = g; g = align16(g + d.gcap * 4);
+    s.g_key = g; g = align16(g + d.gcap * 8);
+    s.g_cnt = g; g = align16(g + d.gcap * 4);
+    s.gk = g; g = align16(g + K * n_sel * 8);
+    s.gp = g; g = align16(g + K * n_sel * 4);
+    s.gc = g; g = align16(g + K * n_sel * 4);
+    s.gtop = g; g = align16(g + 16 * 4 + K * n_sel * 8);
+    int e = a > b ? a : b;
+    e = g > e ? g : e;
+    s.end = e > min_total ? e : min_total;
     return s;
 }
 
-// The n smallest (key, index) pairs of keys[0..cnt) in ascending order, into
-// warp 0's lanes (tk, tv valid in warp 0 after the call; n <= 32). topk/topv:
-// [kCW][32] scratch. Block-wide: every thread calls it.
+__device__ __forceinline__ void clu_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void clu_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The 32 smallest (key, index) pairs of keys[0..cnt), ascending, in lane order of
+// every warp's (tk, tv) on return (empty places: key ~0, index -1): each warp
+// sorts batches of 32 and keeps a running top 32, then the warps' lists are
+// merged pairwise. topk/topv: [kCW][32] scratch. Every thread of the block calls it.
 __device__ __forceinline__ void block_top32(const unsigned long long* keys, const int* idx, int cnt,
                                             unsigned long long* topk, int* topv,
                                             unsigned long long& tk, int& tv) {
@@ -152,13 +175,14 @@ __device__ __forceinline__ void block_top32(const unsigned long long* keys, cons
 // staged with one bulk copy per page and tensor onto an mbarrier, in rounds
 // that fit the staging region; warp w takes tokens w, w + kCW, ... of a round
 // (lane = (head, group of 4G dimensions)); the warps' (max, sum, accumulator)
-// triples are merged in warp order into cpart[h][kD + 2].
+// triples are merged in warp order and stored to dst[h][kD + 2] (block 0's
+// shared memory), with this block's timeout flag after them.
 template <typename T, int G>
 __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const float* s_q,
                                                const int* s_sel, const int* s_scnt, int taken,
                                                int r, int K, int* s_toff, unsigned char* stage,
                                                int stage_bytes, unsigned bar, int* s_fail,
-                                               float* cpart) {
+                                               float* dst) {
     constexpr int LPH = 32 / G;
     constexpr int DPL = kD / LPH;
     constexpr int ROWB = kD * (int)sizeof(T);
@@ -312,25 +336,25 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
                 O = fmaf(pw[dcol], cf, O);
             }
         }
-        cpart[hh * (kD + 2) + dcol] = O;
+        dst[hh * (kD + 2) + dcol] = O;
         if (dcol == 0) {
-            cpart[hh * (kD + 2) + kD] = M;
-            cpart[hh * (kD + 2) + kD + 1] = Lt;
+            dst[hh * (kD + 2) + kD] = M;
+            dst[hh * (kD + 2) + kD + 1] = Lt;
         }
     }
-    if (tid == 0) reinterpret_cast<int*>(cpart)[G * (kD + 2)] = *s_fail;
+    if (tid == 0) reinterpret_cast<int*>(dst)[G * (kD + 2)] = *s_fail;
 }
 
 template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
-    IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int cand_cap, int hcap2, int rcap,
-    int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
+    IndexView v, const T* __restrict__ q, int n_sel, CluDims dm, int smem_total,
+    int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
     int32_t* __restrict__ stats, T* __restrict__ attn_out) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float2 s_qp[kD / 2];  // (q_sel[e], q_sel[e + 64]), e < 64
     __shared__ int s_qcode[kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
-    __shared__ int s_pstar, s_need, s_nch, s_tot, s_tt, s_ncand, s_nraw, s_npg, s_cmp, s_fail, s_gn;
+    __shared__ int s_pstar, s_need, s_nch, s_base, s_ncand, s_cmp, s_fail, s_gn, s_nl[kMaxL];
     __shared__ __align__(8) unsigned long long s_bar;
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -341,32 +365,21 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     const int L = v.L, P = v.P;
     const long long C = v.C;
     const int Kc = K / L, l = r / Kc, rc = r % Kc;
-    const CluSmem lay = clu_layout(C, rcap, n_cand, cand_cap, hcap2, n_sel, K, G, 0);
+    const int n_cand = dm.n_cand;
+    const CluSmem lay = clu_layout(C, dm, L, n_sel, K, G, FUSED, 0);
     int* s_sel = reinterpret_cast<int*>(smem + lay.sel);
     int* s_scnt = reinterpret_cast<int*>(smem + lay.scnt);
     int* s_toff = reinterpret_cast<int*>(smem + lay.toff);
-    uint4* pub = reinterpret_cast<uint4*>(smem + lay.pub);  // [K][n_sel] (key lo, key hi, page, cnt)
-    int* pubx = reinterpret_cast<int*>(smem + lay.pubx);    // [K][4] (entries, ncand, nraw, -)
-    unsigned* bm0 = reinterpret_cast<unsigned*>(smem + lay.bm0);
     int* lhist = reinterpret_cast<int*>(smem + lay.lhist);
-    float* cpart = reinterpret_cast<float*>(smem + lay.cpart);
+    // [0..L) taken leaves per composite, 3 candidates, 4 expanded slots, 8 + r pages of block r
+    int* hubx = reinterpret_cast<int*>(smem + lay.hubx);
+    unsigned* hub_leaf = reinterpret_cast<unsigned*>(smem + lay.hub_leaf);  // [L][n_cand] id << 8 | count
+    uint4* hub_pe = reinterpret_cast<uint4*>(smem + lay.hub_pe);  // [K][n_sel] (key lo, key hi, page, count)
+    float* hub_part = reinterpret_cast<float*>(smem + lay.hub_part);  // [K][G (kD + 2) + 4]
     float* qf = reinterpret_cast<float*>(smem + lay.qf);
-    unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.skey);
-    int* sval = reinterpret_cast<int*>(smem + lay.sval);
-    int* hpage = reinterpret_cast<int*>(smem + lay.hpage);
-    unsigned long long* hkey = reinterpret_cast<unsigned long long*>(smem + lay.hkey);
-    int* hcnt = reinterpret_cast<int*>(smem + lay.hcnt);
-    unsigned long long* topk = reinterpret_cast<unsigned long long*>(smem + lay.top);
-    int* topv = reinterpret_cast<int*>(smem + lay.top + kCW * 32 * 8);
-    unsigned char* prio = smem + lay.prio;
-    unsigned char* cnts = smem + lay.cnt;
-    unsigned* tieb = reinterpret_cast<unsigned*>(smem + lay.tieb);
-    int* hist = reinterpret_cast<int*>(smem + lay.hist);
-    int* ghist = reinterpret_cast<int*>(smem + lay.ghist);
-    int* chosen = reinterpret_cast<int*>(smem + lay.chosen);
-    unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);
-    int* coff = reinterpret_cast<int*>(smem + lay.coff);
+    unsigned* bm0 = reinterpret_cast<unsigned*>(smem + lay.bm0);
     const int nwords0 = (int)((C + 31) / 32);
+    int* hubx0 = cluster.map_shared_rank(hubx, 0);
 
     // ---- 1. leaf count, query heads and directions requested together ------------------
     int Nl = v.n_leaf[v.ul(u, l)];
@@ -384,6 +397,8 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         load4(ud + 4 * lane, wdir);
         wlast = ud[kD];
     }
+    int* hist = reinterpret_cast<int*>(smem + lay.hist);
+    unsigned* tieb = reinterpret_cast<unsigned*>(smem + lay.tieb);
     if (tid < 97) {
         __half2 w[4];
         cell_widths(tid, w);
@@ -391,21 +406,23 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         for (int k = 0; k < 4; ++k) s_width[tid * 4 + k] = w[k];
     }
     for (int i = tid; i < kCSubH * kCHistRow; i += kCT) hist[i] = 0;
-    for (int i = tid; i < rcap / 32; i += kCT) tieb[i] = 0u;
-    if (r == 0 && L > 1)
+    for (int i = tid; i < dm.rcap / 32; i += kCT) tieb[i] = 0u;
+    if (L > 1)
         for (int i = tid; i < nwords0; i += kCT) bm0[i] = 0u;
+    if (r == 0 && tid < 32) hubx[tid] = 0;
     if (tid == 0) {
         s_nch = 0;
-        s_tt = 0;
         s_ncand = 0;
-        s_nraw = 0;
-        s_npg = 0;
         s_fail = 0;
         if (FUSED) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
     }
+    // a block of a composite that is not split starts the cluster barrier now: its
+    // histogram is the composite's, and the barrier only has to order block 0's
+    // cleared counters before the first remote update
+    if (Kc == 1) clu_arrive();
     Nl = Nl < 0 ? 0 : (Nl > C ? (int)C : Nl);
     // this block's leaves: 64-leaf chunks [c0, c1) of the composite, in position order
     const int chunks = (Nl + 63) >> 6;
@@ -413,16 +430,16 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     const int nck = c1 - c0;
     const int lo_leaf = 64 * c0;
     const int nloc = max(0, min(Nl, 64 * c1) - lo_leaf);
-    const unsigned long long* slo = v.leaf_lo + v.leaf_base(u, l) + lo_leaf;
-    const unsigned short* stc = v.leaf_tc + v.leaf_base(u, l) + lo_leaf;
-    const unsigned ring = smem_u32(smem + lay.A + warp * (kCRing * kCSlotB));
+    // the scan reads whole leaf records (lower corner, list id | count, prefix length),
+    // so the ids of the taken leaves are at hand without a second round trip
+    const uint4* lrec = v.leaf_rec + v.leaf_base(u, l) + lo_leaf;
+    const unsigned ring = smem_u32(smem + lay.ring + warp * (kCRing * kCSlotB));
     auto ring_issue = [&](int k, int slot) {
-        const unsigned d = ring + slot * kCSlotB;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + lane * 16),
-                     "l"(slo + 64 * k + 2 * lane)
+        const unsigned d = ring + slot * kCSlotB + lane * 32;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(lrec + 64 * k + 2 * lane)
                      : "memory");
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d + 512 + lane * 4),
-                     "l"(stc + 64 * k + 2 * lane)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16),
+                     "l"(lrec + 64 * k + 2 * lane + 1)
                      : "memory");
     };
 #pragma unroll
@@ -468,6 +485,9 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     __syncthreads();
 
     // ---- 2. priorities, counts and sub-histograms of this block's leaves ----------------
+    unsigned char* prio = smem + lay.prio;
+    unsigned char* cnts = smem + lay.cnt;
+    unsigned* lid = reinterpret_cast<unsigned*>(smem + lay.lid);  // list id << 8 | count
     {
         __half2 qc[4];
         {
@@ -488,22 +508,24 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         int slot = 0;
         for (int k = warp; k < nck; k += kCW) {  // warp-uniform
             asm volatile("cp.async.wait_group %0;" ::"n"(kCRing - 1) : "memory");
-            const unsigned d = ring + slot * kCSlotB;
-            uint4 lo2;
-            unsigned tc2;
+            const unsigned d = ring + slot * kCSlotB + lane * 32;
+            uint4 ra, rb;
             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(lo2.x), "=r"(lo2.y), "=r"(lo2.z), "=r"(lo2.w)
-                         : "r"(d + lane * 16)
+                         : "=r"(ra.x), "=r"(ra.y), "=r"(ra.z), "=r"(ra.w)
+                         : "r"(d)
                          : "memory");
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tc2) : "r"(d + 512 + lane * 4) : "memory");
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(rb.x), "=r"(rb.y), "=r"(rb.z), "=r"(rb.w)
+                         : "r"(d + 16)
+                         : "memory");
             const int i0 = 64 * k + 2 * lane;
-            const unsigned tca = tc2 & 0xFFFFu, tcb = tc2 >> 16;
-            const int p0 = leaf_priority(lo2.x, lo2.y, tc_t(tca), qc, s_width);
-            const int p1 = leaf_priority(lo2.z, lo2.w, tc_t(tcb), qc, s_width);
-            const int cA = tc_cnt(tca), cB = tc_cnt(tcb);
+            const int p0 = leaf_priority(ra.x, ra.y, (int)min(ra.w, 127u), qc, s_width);
+            const int p1 = leaf_priority(rb.x, rb.y, (int)min(rb.w, 127u), qc, s_width);
+            const int cA = (int)(ra.z & 0xFFu), cB = (int)(rb.z & 0xFFu);
             if (i0 < nloc) {
                 st_shared_u16(pr_base + i0, p0 | (p1 << 8));
                 st_shared_u16(cn_base + i0, cA | (cB << 8));
+                *reinterpret_cast<uint2*>(lid + i0) = make_uint2(ra.z, rb.z);
                 atomicAdd(&hl[p0], cA);
                 if (i0 + 1 < nloc) atomicAdd(&hl[p1], cB);
             }
@@ -516,19 +538,33 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     }
     __syncthreads();
 
-    // ---- 3a. the composite's histogram (over DSMEM when it is split) and pi* --------------
+    // ---- 3. the composite's histogram (pulled over DSMEM when it is split), pi*, and the
+    //         tokens at pi* in the composite's blocks before this one -------------------------
+    int* ghist = reinterpret_cast<int*>(smem + lay.ghist);
+    int* gpre = reinterpret_cast<int*>(smem + lay.gpre);
     {
         int hsum = 0;
 #pragma unroll
         for (int sh = 0; sh < kCSubH; ++sh) hsum += hist[sh * kCHistRow + tid];
         if (Kc > 1) {
             lhist[tid] = hsum;
-            cluster.sync();
-            int gs = 0;
-            for (int rr = 0; rr < Kc; ++rr) gs += cluster.map_shared_rank(lhist, l * Kc + rr)[tid];
-            ghist[tid] = gs;
+            clu_arrive();
+            clu_wait();
+            int x[16];  // Kc <= 16 blocks per composite
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+                x[rr] = rr < Kc ? cluster.map_shared_rank(lhist, l * Kc + rr)[tid] : 0;
+            int tot = 0, pre = 0;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                tot += x[rr];
+                pre += rr < rc ? x[rr] : 0;
+            }
+            ghist[tid] = tot;
+            gpre[tid] = pre;
         } else {
             ghist[tid] = hsum;
+            gpre[tid] = 0;
         }
     }
     __syncthreads();
@@ -558,27 +594,23 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 run += loc[k];
                 ++k;
             }
-            s_pstar = lane * 8 + k;
-            s_need = n_cand - run;
+            const int ps = lane * 8 + k;
+            s_pstar = ps;
+            // the ties of the blocks before this one come first in position order
+            s_need = max(0, n_cand - run - gpre[ps]);
         }
     }
     __syncthreads();
 
-    // ---- 3b. leaves below pi* are taken; leaves at pi* are marked, their tokens summed ----
-    for (int i = tid; i < cand_cap; i += kCT) {  // the page table takes over the scan ring
-        hpage[i] = -1;
-        hkey[i] = ~0ull;
-    }
-    const uint4* lrec = v.leaf_rec + v.leaf_base(u, l) + lo_leaf;
+    // ---- 4. leaves below pi* are taken; leaves at pi* are marked in a bitmap ---------------
+    int* chosen = reinterpret_cast<int*>(smem + lay.chosen);
+    unsigned* cmeta = reinterpret_cast<unsigned*>(smem + lay.cmeta);
     {
         const int ps = s_pstar;
         const unsigned* p32 = reinterpret_cast<const unsigned*>(prio);
-        const unsigned* c32 = reinterpret_cast<const unsigned*>(cnts);
         const int nw = (nloc + 3) >> 2;
-        int ttok = 0;
         for (int w4 = tid; w4 < nw; w4 += kCT) {
             const unsigned word = p32[w4];
-            const unsigned cword = c32[w4];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int i = 4 * w4 + b;
@@ -588,33 +620,18 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                     const int slot = atomicAdd(&s_nch, 1);
                     if (slot < n_cand) {
                         chosen[slot] = i;
-                        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                                         smem_u32(cmeta + slot)),
-                                     "l"(&lrec[i].z)
-                                     : "memory");
+                        cmeta[slot] = lid[i];
                     }
                 } else if (pr == ps) {
                     atomicOr(&tieb[i >> 5], 1u << (i & 31));
-                    ttok += (int)((cword >> (8 * b)) & 0xFFu);
                 }
             }
         }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) ttok += __shfl_xor_sync(0xffffffffu, ttok, o);
-        if (lane == 0 && ttok) atomicAdd(&s_tt, ttok);
     }
     __syncthreads();
-    // ties of the blocks before this one (position order) count against the need
-    int need = s_need;
-    if (Kc > 1) {
-        cluster.sync();
-        int before = 0;
-        for (int rr = 0; rr < rc; ++rr) before += *cluster.map_shared_rank(&s_tt, l * Kc + rr);
-        need = max(0, need - before);
-    }
-    // ---- 3c. this block's ties in position order while the tokens taken before them < need
-    // ---- 3d. slot offsets of the taken leaves (counts from the scan's bytes)
+    // this block's ties in position order while the tokens taken before them < need
     if (warp == 0) {
+        const int need = s_need;
         const int nwords = (nloc + 31) >> 5;
         const int nbelow = min(s_nch, n_cand);
         int run = 0, ntaken = 0;
@@ -662,104 +679,126 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 if (slot < n_cand) {
                     const int i = wi * 32 + __ffs(bb) - 1;
                     chosen[slot] = i;
-                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(cmeta + slot)),
-                                 "l"(&lrec[i].z)
-                                 : "memory");
+                    cmeta[slot] = lid[i];
                 }
             ntaken += __shfl_sync(0xffffffffu, tinc, 31);
             run += __shfl_sync(0xffffffffu, inc, 31);
         }
-        __syncwarp();
-        const int nch = min(nbelow + ntaken, n_cand);
+        if (lane == 0) s_nch = min(nbelow + ntaken, n_cand);
+    }
+    if (Kc == 1) clu_wait();  // block 0's counters are cleared (the barrier started at the top)
+    __syncthreads();
+    // the taken leaves (list id | count) go to block 0's table of the composite
+    const int nch = s_nch;
+    if (tid == 0) s_base = nch > 0 ? atomicAdd(&hubx0[l], nch) : 0;
+    __syncthreads();
+    {
+        unsigned* hl0 = cluster.map_shared_rank(hub_leaf, 0) + l * n_cand;
+        const int base = s_base;
+        for (int k = tid; k < nch; k += kCT)
+            if (base + k < n_cand) hl0[base + k] = cmeta[k];
+    }
+    clu_arrive();
+    clu_wait();
+
+    // ---- 5. every block expands an equal share of the unit's candidate slots --------------
+    unsigned* tl = reinterpret_cast<unsigned*>(smem + lay.tl);
+    int* toffc = reinterpret_cast<int*>(smem + lay.toffc);
+    unsigned long long* skey = reinterpret_cast<unsigned long long*>(smem + lay.skey);
+    int* sval = reinterpret_cast<int*>(smem + lay.sval);
+    if (tid < L) s_nl[tid] = min(hubx0[tid], n_cand);
+    __syncthreads();
+    const int nl0 = s_nl[0], nt = nl0 + (L > 1 ? s_nl[1] : 0);
+    {
+        const unsigned* hl0 = cluster.map_shared_rank(hub_leaf, 0);
+        for (int k = tid; k < nt; k += kCT) {
+            const unsigned e = k < nl0 ? hl0[k] : hl0[n_cand + (k - nl0)];
+            tl[k] = e;
+            if (L > 1 && k < nl0) {
+                const int id = (int)(e >> 8);
+                if (id < C) atomicOr(&bm0[id >> 5], 1u << (id & 31));
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {  // slot offsets of the taken leaves
         int carry = 0;
-        for (int k0 = 0; k0 < nch; k0 += 32) {
+        for (int k0 = 0; k0 < nt; k0 += 32) {
             const int k = k0 + lane;
-            const int c = k < nch ? (int)cnts[chosen[k]] : 0;
+            const int c = k < nt ? (int)(tl[k] & 0xFFu) : 0;
             int inc = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, inc, o);
                 if (lane >= o) inc += y;
             }
-            if (k < nch) coff[k] = carry + inc - c;
+            if (k < nt) toffc[k] = carry + inc - c;
             carry += __shfl_sync(0xffffffffu, inc, 31);
         }
-        if (lane == 0) {
-            coff[nch] = carry;
-            s_tot = carry;
-            s_nch = nbelow + ntaken;
-        }
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");  // the taken leaves' records
-    __syncthreads();
-    const int nch = min(s_nch, n_cand);
-    // composite-0 pages taken whole, in block 0's bitmap
-    if (L > 1) {
-        if (l == 0) {
-            unsigned* bm0r = cluster.map_shared_rank(bm0, 0);
-            for (int k = tid; k < nch; k += kCT) {
-                const int id = (int)(cmeta[k] >> 8);
-                if (id < C) atomicOr(&bm0r[id >> 5], 1u << (id & 31));
-            }
-        }
-        cluster.sync();
-    }
-
-    // ---- 4. candidate expansion: every (leaf, slot) of this block at once -----------------
-    {
-        const int total = s_tot;
-        if (tid == 0) s_nraw = total;
-        const unsigned* bm0r = L > 1 ? cluster.map_shared_rank(bm0, 0) : nullptr;
-        for (int j0 = warp * 32; j0 < total; j0 += kCT) {
-            const int j = j0 + lane;
-            bool keep = false;
-            int tok = 0, loc = 0;
-            if (j < total) {
-                int lo = 0, hi = nch;  // last k with coff[k] <= j
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (coff[mid] <= j) lo = mid; else hi = mid;
-                }
-                const int slot = j - coff[lo];
-                const int id = (int)(cmeta[lo] >> 8);
-                if (id < C && slot < P) {
-                    tok = v.slot_tok[v.slot_base(u, l) + (long long)id * P + slot];
-                    if (l == 0) {
-                        loc = id * P + slot;
-                        keep = true;
-                    } else {
-                        loc = v.slot_loc1[v.loc1_base(u) + (long long)id * P + slot];
-                        const int pg = loc >= 0 ? loc / P : 0;
-                        keep = tok >= 0 && loc >= 0 && pg < C && !((bm0r[pg >> 5] >> (pg & 31)) & 1u);
-                    }
-                }
-            }
-            const unsigned km = __ballot_sync(0xffffffffu, keep);
-            int pos0 = 0;
-            if (lane == 0 && km) pos0 = atomicAdd(&s_ncand, __popc(km));
-            pos0 = __shfl_sync(0xffffffffu, pos0, 0);
-            if (keep) {
-                const int pos = pos0 + __popc(km & ((1u << lane) - 1u));
-                if (pos < cand_cap) {
-                    skey[pos] = (unsigned long long)(unsigned)tok;
-                    sval[pos] = loc;
-                }
-            }
-        }
+        if (lane == 0) toffc[nt] = carry;
     }
     __syncthreads();
-    const int ncand = min(s_ncand, cand_cap);
+    const int total = toffc[nt];
+    const int j0 = (int)((long long)r * total / K), j1 = (int)((long long)(r + 1) * total / K);
+    for (int jb = j0 + warp * 32; jb < j1; jb += kCT) {
+        const int j = jb + lane;
+        bool keep = false;
+        int tok = 0, loc = 0;
+        if (j < j1) {
+            int lo = 0, hi = nt;  // last k with toffc[k] <= j
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (toffc[mid] <= j) lo = mid; else hi = mid;
+            }
+            const int slot = j - toffc[lo];
+            const int cl = lo < nl0 ? 0 : 1;
+            const int id = (int)(tl[lo] >> 8);
+            if (id < C && slot < P) {
+                tok = v.slot_tok[v.slot_base(u, cl) + (long long)id * P + slot];
+                if (cl == 0) {
+                    loc = id * P + slot;
+                    keep = true;
+                } else {
+                    // a composite-1 token whose page composite 0 took whole is a duplicate
+                    loc = v.slot_loc1[v.loc1_base(u) + (long long)id * P + slot];
+                    const int pg = loc >= 0 ? loc / P : 0;
+                    keep = tok >= 0 && loc >= 0 && pg < C && !((bm0[pg >> 5] >> (pg & 31)) & 1u);
+                }
+            }
+        }
+        const unsigned km = __ballot_sync(0xffffffffu, keep);
+        int pos0 = 0;
+        if (lane == 0 && km) pos0 = atomicAdd(&s_ncand, __popc(km));
+        pos0 = __shfl_sync(0xffffffffu, pos0, 0);
+        if (keep) {
+            const int pos = pos0 + __popc(km & ((1u << lane) - 1u));
+            if (pos < dm.share_cap) {
+                skey[pos] = (unsigned long long)(unsigned)tok;
+                sval[pos] = loc;
+            }
+        }
+    }
+    // page table of this block's candidates
+    int* hpage = reinterpret_cast<int*>(smem + lay.hpage);
+    unsigned long long* hkey = reinterpret_cast<unsigned long long*>(smem + lay.hkey);
+    int* hcnt = reinterpret_cast<int*>(smem + lay.hcnt);
+    for (int i = tid; i < dm.hcap_l; i += kCT) {
+        hpage[i] = -1;
+        hkey[i] = ~0ull;
+    }
+    __syncthreads();
+    const int ncand = min(s_ncand, dm.share_cap);
 
-    // ---- 5. exact rescoring of this block's candidates; per-page minimum key --------------
+    // ---- 6. exact rescoring of this block's candidates; per-page minimum key ---------------
     {
         constexpr int EPC = 16 / (int)sizeof(T);
         constexpr int CPR = kD / EPC;
         constexpr int ROWB = kD * (int)sizeof(T);
-        unsigned char* stg = smem + lay.B;
-        const int half = min((smem_total - lay.B) / (2 * ROWB), kCT / 2);
+        unsigned char* stg = smem + lay.stage;
+        const int half = min((smem_total - lay.stage) / (2 * ROWB), kCT / 2);
         const int nchunk = (ncand + half - 1) / half;
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
-        const int hmask = cand_cap - 1;
+        const int hmask = dm.hcap_l - 1;
         auto issue = [&](int ch) {
             if (ch < nchunk) {
                 const int rb = ch * half, nr = min(half, ncand - rb);
@@ -829,14 +868,12 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 if (lane >= o && opg == pg && okey < key) key = okey;
             }
             const int next_pg = __shfl_down_sync(0xffffffffu, pg, 2);
-            bool fresh = false;
             if (ok && t == 0 && (lane >= 30 || next_pg != pg)) {
                 unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
-                for (int probe = 0; probe < cand_cap; ++probe) {
+                for (int probe = 0; probe < dm.hcap_l; ++probe) {
                     const int old = atomicCAS(&hpage[hh], -1, pg);
                     if (old == -1 || old == pg) {
-                        fresh = old == -1;
-                        if (fresh)  // the page's token count travels with it to the attention
+                        if (old == -1)  // the page's token count travels with it to the attention
                             asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(hcnt + hh)),
                                          "l"(v.list_cnt + v.leaf_base(u, 0) + pg)
                                          : "memory");
@@ -846,180 +883,203 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                     hh = (hh + 1) & (unsigned)hmask;
                 }
             }
-            {
-                const unsigned nf = __ballot_sync(0xffffffffu, fresh);
-                if (lane == 0 && nf) atomicAdd(&s_npg, __popc(nf));
-            }
             __syncthreads();
             issue(ch + 2);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
     }
-    __syncthreads();
-
-    // ---- 6. this block's n_sel best pages, published to block 0 ---------------------------
     if (tid == 0) s_cmp = 0;
     __syncthreads();
-    for (int h0 = warp * 32; h0 < cand_cap; h0 += kCT) {  // warp-uniform
-        const int hh = h0 + lane;
-        const int pg = hh < cand_cap ? hpage[hh] : -1;
-        const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
-        int base = 0;
-        if (lane == 0 && km) base = atomicAdd(&s_cmp, __popc(km));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (pg >= 0) {
-            const int pos = base + __popc(km & ((1u << lane) - 1u));
-            skey[pos] = hkey[hh];
-            sval[pos] = hh;
-        }
-    }
-    __syncthreads();
+    // this block's n_sel best pages (minimum key, count) go to block 0's table: a page
+    // of the unit's selection is among the best pages of the block that holds its
+    // minimum (fewer than n_sel of that block's pages rank before it there)
     {
-        const int npl = s_cmp;
-        unsigned long long tk;
-        int tv;
-        block_top32(skey, sval, npl, topk, topv, tk, tv);
-        const int ntop = min(n_sel, npl);
-        if (warp == 0) {
-            uint4* pub0 = cluster.map_shared_rank(pub, 0);
-            if (lane < ntop)
-                pub0[r * n_sel + lane] = make_uint4((unsigned)tk, (unsigned)(tk >> 32),
-                                                    (unsigned)hpage[tv], (unsigned)hcnt[tv]);
-            if (lane == 0) {
-                int* px = cluster.map_shared_rank(pubx, 0);
-                px[r * 4 + 0] = ntop;
-                px[r * 4 + 1] = ncand;
-                px[r * 4 + 2] = s_nraw;
-            }
-        }
-    }
-    cluster.sync();
-
-    // ---- 7. the selection: the n_sel smallest published keys, one per page -----------------
-    {
-        int* g_page = reinterpret_cast<int*>(smem + lay.g_page);
-        unsigned long long* g_key = reinterpret_cast<unsigned long long*>(smem + lay.g_key);
-        int* g_cnt = reinterpret_cast<int*>(smem + lay.g_cnt);
-        unsigned long long* g_ckey = reinterpret_cast<unsigned long long*>(smem + lay.g_ckey);
-        int* g_cidx = reinterpret_cast<int*>(smem + lay.g_cidx);
-        unsigned long long* gtk = reinterpret_cast<unsigned long long*>(smem + lay.g_top);
-        int* gtv = reinterpret_cast<int*>(smem + lay.g_top + kCW * 32 * 8);
-        for (int i = tid; i < hcap2; i += kCT) {
-            g_page[i] = -1;
-            g_key[i] = ~0ull;
-        }
-        if (tid == 0) s_gn = 0;
-        __syncthreads();
-        const uint4* pub0 = cluster.map_shared_rank(pub, 0);
-        const int* px = cluster.map_shared_rank(pubx, 0);
-        const int gmask = hcap2 - 1;
-        for (int e = tid; e < K * n_sel; e += kCT) {
-            const int rr = e / n_sel, i = e % n_sel;
-            if (i < px[rr * 4]) {
-                const uint4 x = pub0[rr * n_sel + i];
-                const unsigned long long key = ((unsigned long long)x.y << 32) | x.x;
-                const int pg = (int)x.z;
-                unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
-                for (int probe = 0; probe < hcap2; ++probe) {
-                    const int old = atomicCAS(&g_page[hh], -1, pg);
-                    if (old == -1 || old == pg) {
-                        if (old == -1) g_cnt[hh] = (int)x.w;
-                        atomicMin(&g_key[hh], key);
-                        break;
-                    }
-                    hh = (hh + 1) & (unsigned)gmask;
-                }
-            }
-        }
-        __syncthreads();
-        for (int h0 = warp * 32; h0 < hcap2; h0 += kCT) {
+        unsigned long long* ck = skey;  // compacted in place of the candidates
+        int* cpg = sval;
+        for (int h0 = warp * 32; h0 < dm.hcap_l; h0 += kCT) {  // warp-uniform
             const int hh = h0 + lane;
-            const int pg = hh < hcap2 ? g_page[hh] : -1;
+            const int pg = hh < dm.hcap_l ? hpage[hh] : -1;
             const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
             int base = 0;
-            if (lane == 0 && km) base = atomicAdd(&s_gn, __popc(km));
+            if (lane == 0 && km) base = atomicAdd(&s_cmp, __popc(km));
             base = __shfl_sync(0xffffffffu, base, 0);
             if (pg >= 0) {
                 const int pos = base + __popc(km & ((1u << lane) - 1u));
-                g_ckey[pos] = g_key[hh];
-                g_cidx[pos] = hh;
+                ck[pos] = hkey[hh];
+                cpg[pos] = hh;
             }
         }
         __syncthreads();
-        const int gn = s_gn;
+        const int npl = s_cmp;
+        if (tid == 0) {
+            hubx0[8 + r] = min(npl, n_sel);
+            atomicAdd(&hubx0[3], ncand);
+            atomicAdd(&hubx0[4], j1 - j0);
+        }
         unsigned long long tk;
         int tv;
-        block_top32(g_ckey, g_cidx, gn, gtk, gtv, tk, tv);
-        const int taken = min(n_sel, gn);
-        if (warp == 0 && lane < n_sel) {
-            const int pg = lane < taken ? g_page[tv] : -1;
-            const int c = lane < taken ? g_cnt[tv] : 0;
-            s_sel[lane] = pg;
-            s_scnt[lane] = c;
-            if (r == 0) page_ids[(long long)u * n_sel + lane] = pg;
+        block_top32(ck, cpg, npl, reinterpret_cast<unsigned long long*>(smem + lay.top),
+                    reinterpret_cast<int*>(smem + lay.top + kCW * 32 * 8), tk, tv);
+        if (warp == 0 && lane < min(npl, n_sel)) {
+            uint4* pe0 = cluster.map_shared_rank(hub_pe, 0) + r * n_sel;
+            pe0[lane] = make_uint4((unsigned)tk, (unsigned)(tk >> 32), (unsigned)hpage[tv],
+                                   (unsigned)hcnt[tv]);
         }
+    }
+    clu_arrive();
+    clu_wait();
+
+    // ---- 7. the selection: per page the minimum key over the blocks, the n_sel smallest ---
+    // Each block's list is sorted and holds distinct pages; a page can be in several
+    // lists. An entry is a winner if its key is its page's minimum over the lists;
+    // the rank of a winner is the number of entries with a smaller key (binary
+    // searches in the sorted lists) less the losers with a smaller key.
+    int taken = 0;
+    {
+        int* g_page = reinterpret_cast<int*>(smem + lay.g_page);
+        unsigned long long* g_key = reinterpret_cast<unsigned long long*>(smem + lay.g_key);
+        unsigned long long* ek = reinterpret_cast<unsigned long long*>(smem + lay.gk);  // [K][n_sel]
+        int* ep = reinterpret_cast<int*>(smem + lay.gp);
+        int* ec = reinterpret_cast<int*>(smem + lay.gc);
+        int* en = reinterpret_cast<int*>(smem + lay.gtop);  // [K] list lengths
+        unsigned long long* lose = reinterpret_cast<unsigned long long*>(smem + lay.gtop + 16 * 4);
+        for (int i2 = tid; i2 < dm.gcap; i2 += kCT) {
+            g_page[i2] = -1;
+            g_key[i2] = ~0ull;
+        }
+        if (tid < K) en[tid] = min(hubx0[8 + tid], n_sel);
+        if (tid == 0) {
+            s_gn = 0;
+            s_cmp = 0;
+        }
+        __syncthreads();
+        const uint4* pe0 = cluster.map_shared_rank(hub_pe, 0);
+        const int gmask = dm.gcap - 1;
+        auto slot_of = [&](int pg) {  // the page's slot in the table (present or empty)
+            unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
+            for (int probe = 0; probe < dm.gcap; ++probe) {
+                const int cur = g_page[hh];
+                if (cur == pg || cur == -1) break;
+                hh = (hh + 1) & (unsigned)gmask;
+            }
+            return hh;
+        };
+        for (int e = tid; e < K * n_sel; e += kCT) {
+            const int rr = e / n_sel;
+            if (e - rr * n_sel >= en[rr]) {
+                ek[e] = ~0ull;  // padding sorts last
+                continue;
+            }
+            const uint4 x = pe0[e];
+            const unsigned long long key = ((unsigned long long)x.y << 32) | x.x;
+            const int pg = (int)x.z;
+            ek[e] = key;
+            ep[e] = pg;
+            ec[e] = (int)x.w;
+            unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
+            for (int probe = 0; probe < dm.gcap; ++probe) {
+                const int old = atomicCAS(&g_page[hh], -1, pg);
+                if (old == -1 || old == pg) {
+                    atomicMin(&g_key[hh], key);
+                    break;
+                }
+                hh = (hh + 1) & (unsigned)gmask;
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < K * n_sel; e += kCT) {
+            const int rr = e / n_sel;
+            if (e - rr * n_sel >= en[rr]) continue;
+            if (g_key[slot_of(ep[e])] != ek[e]) lose[atomicAdd(&s_cmp, 1)] = ek[e];
+            else atomicAdd(&s_gn, 1);
+        }
+        __syncthreads();
+        const int nlose = s_cmp;
+        taken = min(n_sel, s_gn);
+        for (int e = tid; e < K * n_sel; e += kCT) {
+            const int rr = e / n_sel, i2 = e - rr * n_sel;
+            if (i2 >= en[rr]) continue;
+            const unsigned long long key = ek[e];
+            if (g_key[slot_of(ep[e])] != key) continue;
+            int rank = i2;
+            for (int o = 0; o < K; ++o) {
+                if (o == rr) continue;
+                const unsigned long long* lk = ek + o * n_sel;
+                int lo = 0, hi = en[o];  // entries of list o below key
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (lk[mid] < key) lo = mid + 1; else hi = mid;
+                }
+                rank += lo;
+            }
+            for (int k = 0; k < nlose; ++k) rank -= lose[k] < key;
+            if (rank < n_sel) {
+                s_sel[rank] = ep[e];
+                s_scnt[rank] = ec[e];
+            }
+        }
+        if (tid >= taken && tid < n_sel) {
+            s_sel[tid] = -1;
+            s_scnt[tid] = 0;
+        }
+        __syncthreads();
         if (r == 0 && warp == 0) {
-            int tok_sel = lane < taken ? g_cnt[tv] : 0;
+            if (lane < n_sel) page_ids[(long long)u * n_sel + lane] = s_sel[lane];
+            int tok_sel = lane < taken ? s_scnt[lane] : 0;
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
-            int nc = 0, nr = 0;
-            if (lane < K) {
-                nc = px[lane * 4 + 1];
-                nr = px[lane * 4 + 2];
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                nc += __shfl_xor_sync(0xffffffffu, nc, o);
-                nr += __shfl_xor_sync(0xffffffffu, nr, o);
-            }
             if (lane == 0) {
                 n_pages_out[u] = taken;
                 if (stats) {
                     stats[4 * u + 0] = Nall;
-                    stats[4 * u + 1] = nc;
+                    stats[4 * u + 1] = hubx[3];
                     stats[4 * u + 2] = tok_sel;
-                    stats[4 * u + 3] = nr;
+                    stats[4 * u + 3] = hubx[4];
                 }
             }
         }
-        if (tid == 0) s_gn = taken;
         if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
     }
     __syncthreads();
 
-    // ---- 8. attention over this block's pages; partials merged over the cluster ------------
+    // ---- 8. attention over this block's pages; the partials are merged in block 0 -----------
     if constexpr (FUSED) {
-        const int taken = s_gn;
-        attend_partial<T, G>(v, u, qf, s_sel, s_scnt, taken, r, K, s_toff, smem + lay.A,
-                             smem_total - lay.A, smem_u32(&s_bar), &s_fail, cpart);
-        cluster.sync();
-        const int E = G * kD;
-        const int e0 = r * E / K, e1 = (r + 1) * E / K;
-        T* ou = attn_out + (long long)u * G * kD;
-        for (int e = e0 + tid; e < e1; e += kCT) {
-            const int hh = e / kD, dcol = e % kD;
-            float M = -INFINITY;
-            int fail = 0;
-            for (int rr = 0; rr < K; ++rr) {
-                const float* cp = cluster.map_shared_rank(cpart, rr);
-                M = fmaxf(M, cp[hh * (kD + 2) + kD]);
-                fail |= reinterpret_cast<const int*>(cp)[G * (kD + 2)];
-            }
-            float Lt = 0.0f, O = 0.0f;
-            if (M != -INFINITY && !fail) {
+        const int PW = G * (kD + 2) + 4;
+        attend_partial<T, G>(v, u, qf, s_sel, s_scnt, taken, r, K, s_toff, smem + lay.X,
+                             smem_total - lay.X, smem_u32(&s_bar), &s_fail,
+                             cluster.map_shared_rank(hub_part, 0) + r * PW);
+        clu_arrive();
+        clu_wait();
+        if (r == 0) {
+            T* ou = attn_out + (long long)u * G * kD;
+            for (int e = tid; e < G * kD; e += kCT) {
+                const int hh = e / kD, dcol = e % kD;
+                float M = -INFINITY;
+                int fail = 0;
                 for (int rr = 0; rr < K; ++rr) {
-                    const float* cp = cluster.map_shared_rank(cpart, rr);
-                    const float mr = cp[hh * (kD + 2) + kD];
-                    if (mr == -INFINITY) continue;
-                    const float cf = exp2f(mr - M);
-                    Lt = fmaf(cp[hh * (kD + 2) + kD + 1], cf, Lt);
-                    O = fmaf(cp[hh * (kD + 2) + dcol], cf, O);
+                    const float* cp = hub_part + rr * PW;
+                    M = fmaxf(M, cp[hh * (kD + 2) + kD]);
+                    fail |= reinterpret_cast<const int*>(cp)[G * (kD + 2)];
                 }
+                float Lt = 0.0f, O = 0.0f;
+                if (M != -INFINITY && !fail) {
+                    for (int rr = 0; rr < K; ++rr) {
+                        const float* cp = hub_part + rr * PW;
+                        const float mr = cp[hh * (kD + 2) + kD];
+                        if (mr == -INFINITY) continue;
+                        const float cf = exp2f(mr - M);
+                        Lt = fmaf(cp[hh * (kD + 2) + kD + 1], cf, Lt);
+                        O = fmaf(cp[hh * (kD + 2) + dcol], cf, O);
+                    }
+                }
+                ou[e] = from_f<T>(Lt > 0.0f ? O / Lt : 0.0f);
             }
-            ou[e] = from_f<T>(Lt > 0.0f ? O / Lt : 0.0f);
         }
+    } else {
+        // block 0 keeps its tables until every block has read them
+        clu_arrive();
+        clu_wait();
     }
-    cluster.sync();  // no block leaves while another still reads its shared memory
 }
 
 // ---- host side -------------------------------------------------------------------------
@@ -1027,7 +1087,8 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
 namespace {
 
 struct CluPlan {
-    int K = 1, cand_cap = 0, hcap2 = 0, rcap = 0, bytes = 0;
+    int K = 1, bytes = 0;
+    CluDims d{};
 };
 
 int pow2_at_least(int x) {
@@ -1041,28 +1102,29 @@ CluPlan clu_plan(const IndexView& v, int K, int n_sel, int n_cand, bool fused, i
     p.K = K;
     const int L = v.L, P = v.P;
     const int Kc = K / L;
-    p.cand_cap = pow2_at_least(n_cand + P - 1);
-    p.hcap2 = pow2_at_least(2 * K * n_sel + 1);
     const long long ch = (v.C + 63) / 64;
-    p.rcap = (int)(64 * ((ch + Kc - 1) / Kc));
+    p.d.rcap = (int)(64 * ((ch + Kc - 1) / Kc));
+    p.d.n_cand = n_cand;
+    p.d.s_tot = L * (n_cand + P - 1);
+    p.d.share_cap = (p.d.s_tot + K - 1) / K;
+    p.d.hcap_l = pow2_at_least(p.d.share_cap + 1);
+    p.d.gcap = pow2_at_least(2 * K * n_sel + 1);
     const int es = v.dtype == ICE_BF16 ? 2 : 4;
-    const CluSmem lay = clu_layout(v.C, p.rcap, n_cand, p.cand_cap, p.hcap2, n_sel, K, v.G, 0);
+    const CluSmem lay = clu_layout(v.C, p.d, L, n_sel, K, v.G, fused, 0);
     int need = lay.end;
-    // the rescoring stages at least two rows, the attention at least one page's
-    // K and V rows and then the warps' partials
-    need = std::max(need, lay.B + 2 * 2 * kD * es);
+    // the rescoring stages at least two rows a half, the attention at least one
+    // page's K and V rows and then the warps' partials
+    need = std::max(need, lay.stage + 2 * 2 * kD * es);
     if (fused) {
-        need = std::max(need, lay.A + 2 * P * kD * es);
-        need = std::max(need, lay.A + kCW * v.G * (kD + 2) * 4);
+        need = std::max(need, lay.X + 2 * P * kD * es);
+        need = std::max(need, lay.X + kCW * v.G * (kD + 2) * 4);
     }
-    p.bytes = std::max(need, target_bytes);
-    if (need > kCluSmemMax) p.bytes = need;  // refused by the caller
-    else p.bytes = std::min(p.bytes, kCluSmemMax);
+    p.bytes = need > kCluSmemMax ? need : std::min(std::max(need, target_bytes), kCluSmemMax);
     return p;
 }
 
 template <typename T, int G, bool F>
-cudaError_t clu_launch(const IndexView& v, const CluPlan& p, const void* q, int n_sel, int n_cand,
+cudaError_t clu_launch(const IndexView& v, const CluPlan& p, const void* q, int n_sel,
                        int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
                        cudaStream_t s) {
     auto kern = select_cluster_kernel<T, G, F>;
@@ -1078,8 +1140,8 @@ cudaError_t clu_launch(const IndexView& v, const CluPlan& p, const void* q, int 
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, v, (const T*)q, n_sel, n_cand, p.cand_cap, p.hcap2, p.rcap,
-                              p.bytes, page_ids, n_pages, stats, (T*)out);
+    return cudaLaunchKernelEx(&cfg, kern, v, (const T*)q, n_sel, p.d, p.bytes, page_ids, n_pages,
+                              stats, (T*)out);
 }
 
 template <typename T, int G, bool F>
@@ -1130,7 +1192,7 @@ cudaError_t clu_dispatch_g(const IndexView& v, const CluPlan& p, const void* q, 
             *fits = clu_fits<T, GG, F>(v, p);                                                      \
             return cudaSuccess;                                                                    \
         }                                                                                          \
-        return clu_launch<T, GG, F>(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out, s);
+        return clu_launch<T, GG, F>(v, p, q, n_sel, page_ids, n_pages, stats, out, s);
         ICE_CLU_G(1) ICE_CLU_G(2) ICE_CLU_G(4) ICE_CLU_G(8)
 #undef ICE_CLU_G
         default: return cudaErrorInvalidValue;

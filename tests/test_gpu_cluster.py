@@ -86,7 +86,7 @@ def test_unit_beyond_one_block_tables(ice):
     with pytest.raises(ice.IceError) as ei:
         gix.select_attn(q.cuda(), w.budget)
     assert ei.value.code == ice.ICE_ERR_UNSUPPORTED
-    for K in (0, 2, 16):
+    for K in (0, 8, 16):
         gix.set_cluster_size(K)
         _check_all(ice, gix, w, keys, values, q, f"K={K}")
     gix.destroy()
