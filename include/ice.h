@@ -286,9 +286,9 @@ int ice_get_info(const ice_index* ix, ice_info* info);
  * leaf scan, the rescoring and the attended pages of a unit, and merges the
  * priority histograms, the page keys and the softmax partials over distributed
  * shared memory.
- *   k = 0: automatic (16, 8, 4 or 2 blocks per unit for launches of up to 9, 19,
- *          38 or 152 units; one block per unit above that, and a cluster
- *          whenever one block cannot hold the unit's tables);
+ *   k = 0: automatic (8, 4 or 2 blocks per unit for launches of up to 19, 38 or
+ *          76 units; one block per unit above that, and a cluster whenever one
+ *          block cannot hold the unit's tables);
  *   k = 1: one block per unit;
  *   k = 2, 4, 8, 16: that many blocks per unit (k >= n_composite).
  * The cluster path takes budget/page_size <= 32 pages; ice_select_attn_reuse,

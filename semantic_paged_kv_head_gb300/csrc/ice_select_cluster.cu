@@ -62,7 +62,7 @@ struct CluSmem {
     int X;  // phase region: scan tables, then candidates, then ranking, then attention staging
     int ring, prio, cnt, lid, tieb, hist, ghist, gpre, chosen, cmeta;  // scan
     int tl, toffc, skey, sval, hpage, hkey, hcnt, top, stage;     // candidates (stage: rows)
-    int g_page, g_key, g_cnt, gk, gp, gc, gtop;                   // ranking
+    int g_page, g_key, g_cnt, gk, gp, gc;                         // ranking
     int end;
 };
 
@@ -118,7 +118,6 @@ __host__ __device__ inline CluSmem clu_layout(long long C, const CluDims& d, int
     s.gk = g; g = align16(g + K * n_sel * 8);
     s.gp = g; g = align16(g + K * n_sel * 4);
     s.gc = g; g = align16(g + K * n_sel * 4);
-    s.gtop = g; g = align16(g + 16 * 4 + K * n_sel * 8);
     int e = a > b ? a : b;
     e = g > e ? g : e;
     s.end = e > min_total ? e : min_total;
@@ -354,7 +353,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     __shared__ __align__(16) float2 s_qp[kD / 2];  // (q_sel[e], q_sel[e + 64]), e < 64
     __shared__ int s_qcode[kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
-    __shared__ int s_pstar, s_need, s_nch, s_base, s_ncand, s_cmp, s_fail, s_gn, s_nl[kMaxL];
+    __shared__ int s_pstar, s_need, s_nch, s_base, s_ncand, s_cmp, s_fail, s_gn, s_taken, s_nl[kMaxL];
     __shared__ __align__(8) unsigned long long s_bar;
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -929,57 +928,33 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     clu_arrive();
     clu_wait();
 
-    // ---- 7. the selection: per page the minimum key over the blocks, the n_sel smallest ---
-    // Each block's list is sorted and holds distinct pages; a page can be in several
-    // lists. An entry is a winner if its key is its page's minimum over the lists;
-    // the rank of a winner is the number of entries with a smaller key (binary
-    // searches in the sorted lists) less the losers with a smaller key.
-    int taken = 0;
-    {
+    // ---- 7. the selection (block 0): per page the minimum key over the blocks' lists, the
+    //         n_sel smallest; sent to every block of the cluster -----------------------------
+    if (r == 0) {
         int* g_page = reinterpret_cast<int*>(smem + lay.g_page);
         unsigned long long* g_key = reinterpret_cast<unsigned long long*>(smem + lay.g_key);
-        unsigned long long* ek = reinterpret_cast<unsigned long long*>(smem + lay.gk);  // [K][n_sel]
-        int* ep = reinterpret_cast<int*>(smem + lay.gp);
-        int* ec = reinterpret_cast<int*>(smem + lay.gc);
-        int* en = reinterpret_cast<int*>(smem + lay.gtop);  // [K] list lengths
-        unsigned long long* lose = reinterpret_cast<unsigned long long*>(smem + lay.gtop + 16 * 4);
+        int* g_cnt = reinterpret_cast<int*>(smem + lay.g_cnt);
+        unsigned long long* gk = reinterpret_cast<unsigned long long*>(smem + lay.gk);
+        int* gp = reinterpret_cast<int*>(smem + lay.gp);
+        int* gc = reinterpret_cast<int*>(smem + lay.gc);
         for (int i2 = tid; i2 < dm.gcap; i2 += kCT) {
             g_page[i2] = -1;
             g_key[i2] = ~0ull;
         }
-        if (tid < K) en[tid] = min(hubx0[8 + tid], n_sel);
-        if (tid == 0) {
-            s_gn = 0;
-            s_cmp = 0;
-        }
+        if (tid == 0) s_gn = 0;
         __syncthreads();
-        const uint4* pe0 = cluster.map_shared_rank(hub_pe, 0);
         const int gmask = dm.gcap - 1;
-        auto slot_of = [&](int pg) {  // the page's slot in the table (present or empty)
-            unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
-            for (int probe = 0; probe < dm.gcap; ++probe) {
-                const int cur = g_page[hh];
-                if (cur == pg || cur == -1) break;
-                hh = (hh + 1) & (unsigned)gmask;
-            }
-            return hh;
-        };
         for (int e = tid; e < K * n_sel; e += kCT) {
             const int rr = e / n_sel;
-            if (e - rr * n_sel >= en[rr]) {
-                ek[e] = ~0ull;  // padding sorts last
-                continue;
-            }
-            const uint4 x = pe0[e];
+            if (e - rr * n_sel >= min(hubx[8 + rr], n_sel)) continue;
+            const uint4 x = hub_pe[e];
             const unsigned long long key = ((unsigned long long)x.y << 32) | x.x;
             const int pg = (int)x.z;
-            ek[e] = key;
-            ep[e] = pg;
-            ec[e] = (int)x.w;
             unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
             for (int probe = 0; probe < dm.gcap; ++probe) {
                 const int old = atomicCAS(&g_page[hh], -1, pg);
                 if (old == -1 || old == pg) {
+                    if (old == -1) g_cnt[hh] = (int)x.w;
                     atomicMin(&g_key[hh], key);
                     break;
                 }
@@ -987,43 +962,41 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
             }
         }
         __syncthreads();
-        for (int e = tid; e < K * n_sel; e += kCT) {
-            const int rr = e / n_sel;
-            if (e - rr * n_sel >= en[rr]) continue;
-            if (g_key[slot_of(ep[e])] != ek[e]) lose[atomicAdd(&s_cmp, 1)] = ek[e];
-            else atomicAdd(&s_gn, 1);
+        for (int h0 = warp * 32; h0 < dm.gcap; h0 += kCT) {  // warp-uniform
+            const int hh = h0 + lane;
+            const int pg = hh < dm.gcap ? g_page[hh] : -1;
+            const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
+            int base = 0;
+            if (lane == 0 && km) base = atomicAdd(&s_gn, __popc(km));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (pg >= 0) {
+                const int pos = base + __popc(km & ((1u << lane) - 1u));
+                gk[pos] = g_key[hh];
+                gp[pos] = pg;
+                gc[pos] = g_cnt[hh];
+            }
         }
         __syncthreads();
-        const int nlose = s_cmp;
-        taken = min(n_sel, s_gn);
-        for (int e = tid; e < K * n_sel; e += kCT) {
-            const int rr = e / n_sel, i2 = e - rr * n_sel;
-            if (i2 >= en[rr]) continue;
-            const unsigned long long key = ek[e];
-            if (g_key[slot_of(ep[e])] != key) continue;
-            int rank = i2;
-            for (int o = 0; o < K; ++o) {
-                if (o == rr) continue;
-                const unsigned long long* lk = ek + o * n_sel;
-                int lo = 0, hi = en[o];  // entries of list o below key
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (lk[mid] < key) lo = mid + 1; else hi = mid;
-                }
-                rank += lo;
-            }
-            for (int k = 0; k < nlose; ++k) rank -= lose[k] < key;
+        const int gn = s_gn;
+        const int taken = min(n_sel, gn);
+        // the rank of a page is the number of pages with a smaller key (keys are unique)
+        for (int i2 = tid; i2 < gn; i2 += kCT) {
+            const unsigned long long key = gk[i2];
+            int rank = 0;
+#pragma unroll 8
+            for (int j2 = 0; j2 < gn; ++j2) rank += gk[j2] < key ? 1 : 0;
             if (rank < n_sel) {
-                s_sel[rank] = ep[e];
-                s_scnt[rank] = ec[e];
+                s_sel[rank] = gp[i2];
+                s_scnt[rank] = gc[i2];
             }
         }
         if (tid >= taken && tid < n_sel) {
             s_sel[tid] = -1;
             s_scnt[tid] = 0;
         }
+        if (tid == 0) s_taken = taken;
         __syncthreads();
-        if (r == 0 && warp == 0) {
+        if (warp == 0) {
             if (lane < n_sel) page_ids[(long long)u * n_sel + lane] = s_sel[lane];
             int tok_sel = lane < taken ? s_scnt[lane] : 0;
 #pragma unroll
@@ -1038,9 +1011,25 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 }
             }
         }
-        if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
+        if (FUSED) {  // the selection to the other blocks
+            for (int e = tid; e < (K - 1) * n_sel; e += kCT) {
+                const int rr = 1 + e / n_sel, i2 = e % n_sel;
+                cluster.map_shared_rank(s_sel, rr)[i2] = s_sel[i2];
+                cluster.map_shared_rank(s_scnt, rr)[i2] = s_scnt[i2];
+            }
+            if (tid > 0 && tid < K) *cluster.map_shared_rank(&s_taken, tid) = taken;
+        }
     }
-    __syncthreads();
+    if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
+    if (!FUSED) {
+        // block 0 keeps its tables until every block has finished
+        clu_arrive();
+        clu_wait();
+        return;
+    }
+    clu_arrive();
+    clu_wait();
+    const int taken = s_taken;
 
     // ---- 8. attention over this block's pages; the partials are merged in block 0 -----------
     if constexpr (FUSED) {
@@ -1075,10 +1064,6 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 ou[e] = from_f<T>(Lt > 0.0f ? O / Lt : 0.0f);
             }
         }
-    } else {
-        // block 0 keeps its tables until every block has read them
-        clu_arrive();
-        clu_wait();
     }
 }
 
@@ -1233,14 +1218,15 @@ cudaError_t select_cluster_prepare() {
 // blocks per SM above that.
 int clu_target_bytes(int blocks) { return blocks <= 304 ? 100 * 1024 : 54 * 1024; }
 
-// Cluster size for U units: enough blocks to cover the SMs about twice, at
-// most 16 blocks per unit; 1 (the one-block kernel) for large launches.
+// Cluster size for U units: 8 blocks per unit up to 19 units (one layer of
+// 8 KV heads: 64 blocks; 16 blocks per unit measured slower there, the block
+// that ranks gathers twice the lists), 4 up to 38, 2 up to 76; the one-block
+// kernel for large launches, whose blocks already fill the SMs.
 int select_cluster_auto(int U, int L) {
     int K = 1;
-    if (U <= 9) K = 16;
-    else if (U <= 19) K = 8;
+    if (U <= 19) K = 8;
     else if (U <= 38) K = 4;
-    else if (U <= 152) K = 2;
+    else if (U <= 76) K = 2;
     if (K < L) K = 1;
     return K;
 }
