@@ -247,7 +247,8 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
         std::vector<int> nleaf((size_t)L * U, 0);
         int cur = 0;
         if (n > 0) {
-            if ((e = scratch_alloc(s, U, L, n, st)) != cudaSuccess) {
+            const bool tc = params->dtype == ICE_BF16 && params->dir_kind == ICE_DIR_RADEMACHER;
+            if ((e = scratch_alloc(s, U, L, n, tc, st)) != cudaSuccess) {
                 scratch_free(s, st);
                 goto fail;
             }
@@ -257,6 +258,15 @@ int ice_build(const ice_params* params, const void* keys, const void* values, in
                 e = cudaMemcpyAsync(nleaf.data(), s.nleaf, sizeof(int) * L * U,
                                     cudaMemcpyDeviceToHost, st);
             if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+            int berr = 0;
+            if (e == cudaSuccess) e = cudaMemcpy(&berr, s.err, sizeof(int), cudaMemcpyDeviceToHost);
+            if (e == cudaSuccess && berr != 0) {  // a bounded wait of the key pass ran out
+                scratch_free(s, st);
+                cudaStreamSynchronize(st);
+                free_all(ix);
+                delete ix;
+                return ICE_ERR_TIMEOUT;
+            }
             if (e != cudaSuccess) {
                 scratch_free(s, st);
                 goto fail;

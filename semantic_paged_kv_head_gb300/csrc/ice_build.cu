@@ -6,9 +6,13 @@
 // Every unit (sequence, layer, KV head) is an independent segment; all units
 // are processed by the same launches.
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
+#include <cuda.h>  // the CUtensorMap type and its enums (the encoder is looked up at run time)
+
 #include "ice_internal.cuh"
+#include "ice_select_common.cuh"
 
 namespace ice {
 
@@ -277,6 +281,317 @@ __global__ void __launch_bounds__(kPmWarps * 32) project_mma_kernel(
             int c[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) c[j] = codes[rr][l * kM + j];
+            const long long o = ((long long)l * U + u) * n + t;
+            mk_out[o] = morton8(c);
+            tok_out[o] = (int)t;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K1d: the key read of the build done once, on the fifth-generation tensor
+// cores, for bf16 keys and +-1/16 directions: a tile of 128 tokens (128 x 128
+// bf16, 32 KB) is staged by the tensor memory accelerator (two boxes of 64
+// dimensions, 128-byte swizzle) and
+//  * one thread issues 8 tcgen05.mma (kind::f16, M = 128, N = 16, K = 16) that
+//    leave P_raw = K U^T (the unscaled projections, fp32) in tensor memory;
+//  * meanwhile every thread forms its token's squared norm with the fixed-order
+//    dot from the same shared-memory tile;
+//  * each warp reads its 32 tokens' 16 projections back with tcgen05.ld and
+//    stores them with the norm (68 bytes per token); the unit's largest norm is
+//    kept with atomicMax.
+// The next tile's copy is in flight while a tile is processed. The unit's
+// exponent is known only after all its tokens are read, so the codes come from
+// a second, light pass (K1e) over these 68 bytes: 2^-e is exact, so the scaled
+// projection equals D(u, k) 2^-e of the fixed-order definition whenever the
+// tensor cores' sum equals the fixed-order sum, and values within kCodeGuard of
+// a code boundary are recomputed there in the fixed order.
+// ---------------------------------------------------------------------------
+constexpr int kTcRows = 128;                 // tokens per tile (the MMA's M)
+constexpr int kTcThreads = 128;              // one thread per token row, 4 warps
+constexpr int kTcTileB = kTcRows * kD * 2;   // 32 KB
+constexpr int kTcHalfB = kTcTileB / 2;       // one 64-dimension box
+constexpr int kTcDirB = 16 * kD * 2;         // 16 directions x 128 bf16
+constexpr int kTcSmem = 1024 + 2 * kTcTileB + kTcDirB;  // + alignment slack
+constexpr int kTcTmemCols = 32;
+
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte
+// swizzle: start address >> 4 (bits 0-13), leading offset 16 B (unused with
+// this swizzle, bits 16-29), stride 1024 B between 8-row groups (bits 32-45),
+// the fixed value 1 at bit 46, swizzle mode 2 (128 B) in bits 61-63.
+__device__ __forceinline__ unsigned long long sdesc_k_sw128(unsigned saddr) {
+    return (unsigned long long)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), both K-major, N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
+constexpr unsigned kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void tc_mbar_init(unsigned bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap, const float* __restrict__ dirs, int L, long long n,
+    int tiles_per_unit, long long tiles_total, float* __restrict__ praw, float* __restrict__ nrm2,
+    unsigned* __restrict__ umax, int* __restrict__ err) {
+    extern __shared__ unsigned char tc_smem[];
+    __shared__ __align__(8) unsigned long long bar_full[2], bar_mma[2];
+    __shared__ unsigned tmem_slot;
+    __shared__ int s_fail;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned raw0 = smem_u32(tc_smem);
+    const unsigned base = (raw0 + 1023u) & ~1023u;  // the swizzle atoms need 1024-byte alignment
+    const unsigned sA0 = base, sA1 = base + kTcTileB, sB = base + 2 * kTcTileB;
+    unsigned char* pB = tc_smem + (sB - raw0);
+    // the directions in bf16 (exact for +-1/16): row j (direction), dimensions
+    // 64h..64h+63 in half h; the 16-byte chunk c of row j sits at chunk c ^ (j mod 8)
+    for (int idx = tid; idx < 16 * 16; idx += kTcThreads) {
+        const int j = idx >> 4, chunk = idx & 15, h = chunk >> 3, c = chunk & 7;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (j < L * kM) {
+            const float* ud = dirs + (long long)j * kDirStride + 64 * h + 8 * c;
+            w.x = (__float_as_uint(ud[0]) >> 16) | (__float_as_uint(ud[1]) & 0xFFFF0000u);
+            w.y = (__float_as_uint(ud[2]) >> 16) | (__float_as_uint(ud[3]) & 0xFFFF0000u);
+            w.z = (__float_as_uint(ud[4]) >> 16) | (__float_as_uint(ud[5]) & 0xFFFF0000u);
+            w.w = (__float_as_uint(ud[6]) >> 16) | (__float_as_uint(ud[7]) & 0xFFFF0000u);
+        }
+        *reinterpret_cast<uint4*>(pB + h * (kTcDirB / 2) + j * 128 + ((c ^ (j & 7)) << 4)) = w;
+    }
+    if (tid == 0) {
+        s_fail = 0;
+        tc_mbar_init(smem_u32(&bar_full[0]));
+        tc_mbar_init(smem_u32(&bar_full[1]));
+        tc_mbar_init(smem_u32(&bar_mma[0]));
+        tc_mbar_init(smem_u32(&bar_mma[1]));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<unsigned long long>(&tmap)) : "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_slot)),
+                     "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // the directions written by ordinary stores are read by the tensor cores
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const unsigned tmem = tmem_slot;
+
+    auto issue = [&](long long tile, int s) {  // thread 0
+        const unsigned bar = smem_u32(&bar_full[s]);
+        const unsigned dst = s ? sA1 : sA0;
+        const long long uu = tile / tiles_per_unit;
+        const int y = (int)(uu * n + (tile % tiles_per_unit) * kTcRows);
+        const unsigned long long tm = reinterpret_cast<unsigned long long>(&tmap);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTcTileB)
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+                dst),
+            "l"(tm), "r"(0), "r"(y), "r"(bar)
+            : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+                dst + kTcHalfB),
+            "l"(tm), "r"(64), "r"(y), "r"(bar)
+            : "memory");
+    };
+
+    long long tile = blockIdx.x;
+    if (tid == 0 && tile < tiles_total) issue(tile, 0);
+    int it = 0;
+    // s_fail: 1 = the tile's copy did not land in time, 2 = its MMAs did not finish
+    for (; tile < tiles_total; tile += gridDim.x, ++it) {  // block-uniform
+        const int s = it & 1;
+        const unsigned ph = (unsigned)((it >> 1) & 1);
+        const unsigned sA = s ? sA1 : sA0;
+        const long long next = tile + gridDim.x;
+        if (tid == 0 && next < tiles_total) issue(next, s ^ 1);
+        if (!mbar_wait_bounded(smem_u32(&bar_full[s]), ph)) s_fail = 1;
+        __syncthreads();
+        if (s_fail) break;
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const unsigned off = (unsigned)((ks >> 2) * kTcHalfB + (ks & 3) * 32);
+                const unsigned boff = (unsigned)((ks >> 2) * (kTcDirB / 2) + (ks & 3) * 32);
+                const unsigned long long ad = sdesc_k_sw128(sA + off);
+                const unsigned long long bd = sdesc_k_sw128(sB + boff);
+                const unsigned acc = ks > 0 ? 1u : 0u;
+                asm volatile(
+                    "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                    " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem + 16u * s),
+                    "l"(ad), "l"(bd), "r"(kTcIdesc), "r"(acc)
+                    : "memory");
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             smem_u32(&bar_mma[s]))
+                         : "memory");
+        }
+        // the token's squared norm in the fixed order, from the swizzled tile: lane
+        // partial l covers dimensions 4l..4l+3, i.e. half l / 16, chunk (l mod 16) / 2
+        float part[32];
+        {
+            const unsigned row = sA + tid * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 x;
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                                 : "r"(row + h * kTcHalfB + ((c ^ (tid & 7)) << 4))
+                                 : "memory");
+                    const float e0 = __uint_as_float(x.x << 16), e1 = __uint_as_float(x.x & 0xFFFF0000u);
+                    const float e2 = __uint_as_float(x.y << 16), e3 = __uint_as_float(x.y & 0xFFFF0000u);
+                    const float e4 = __uint_as_float(x.z << 16), e5 = __uint_as_float(x.z & 0xFFFF0000u);
+                    const float e6 = __uint_as_float(x.w << 16), e7 = __uint_as_float(x.w & 0xFFFF0000u);
+                    float a = 0.0f, b = 0.0f;
+                    a = __fmaf_rn(e0, e0, a);
+                    a = __fmaf_rn(e1, e1, a);
+                    a = __fmaf_rn(e2, e2, a);
+                    a = __fmaf_rn(e3, e3, a);
+                    b = __fmaf_rn(e4, e4, b);
+                    b = __fmaf_rn(e5, e5, b);
+                    b = __fmaf_rn(e6, e6, b);
+                    b = __fmaf_rn(e7, e7, b);
+                    part[16 * h + 2 * c] = a;
+                    part[16 * h + 2 * c + 1] = b;
+                }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+                for (int l = 0; l < o; ++l) part[l] = __fadd_rn(part[l], part[l + o]);
+        }
+        const float nrm = part[0];
+        // the projections of the warp's 32 tokens from tensor memory
+        if (!mbar_wait_bounded(smem_u32(&bar_mma[s]), ph)) s_fail = 2;
+        __syncthreads();
+        if (s_fail) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        unsigned r[16];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+              "=r"(r[14]), "=r"(r[15])
+            : "r"(tmem + ((unsigned)(32 * warp) << 16) + 16u * s)
+            : "memory");
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const long long uu = tile / tiles_per_unit;
+        const long long t = (tile % tiles_per_unit) * kTcRows + tid;
+        const bool valid = t < n;
+        if (valid) {
+            const long long g = uu * n + t;
+            float4* dst = reinterpret_cast<float4*>(praw + g * 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dst[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                     __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+            nrm2[g] = nrm;
+        }
+        float mx = valid ? nrm : 0.0f;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) atomicMax(&umax[uu], __float_as_uint(mx));
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();  // the tile's buffer and tensor-memory columns are free again
+    }
+    if (s_fail) {
+        // a wait ran out: report it, then let the copies and MMAs still in flight
+        // finish (bounded) before the tensor memory is released
+        if (tid == 0) {
+            atomicExch(err, 1);
+            const int s = it & 1;
+            const unsigned ph = (unsigned)((it >> 1) & 1);
+            if (s_fail == 1) mbar_wait_bounded(smem_u32(&bar_full[s]), ph);
+            else mbar_wait_bounded(smem_u32(&bar_mma[s]), ph);
+            if (tile + gridDim.x < tiles_total)  // the next tile's copy, use it + 1 of its buffer
+                mbar_wait_bounded(smem_u32(&bar_full[s ^ 1]), (unsigned)(((it + 1) >> 1) & 1));
+        }
+        __syncthreads();
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
+                     : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// K1e: codes and Morton keys from the stored projections: p = fma(u[d], tail,
+// P_raw 2^-e) with the unit's frozen exponent; a value whose (p + 1) * 128
+// lies within kCodeGuard of an integer is recomputed from the key row with the
+// fixed-order dot (one warp per queued value).
+// ---------------------------------------------------------------------------
+constexpr int kCodeTok = 256;
+
+__global__ void __launch_bounds__(kCodeTok) codes_tc_kernel(
+    const __nv_bfloat16* __restrict__ keys, const float* __restrict__ praw, const float* __restrict__ nrm2,
+    const int* __restrict__ e_unit, const float* __restrict__ dirs, int L, long long n, int tiles_per_unit,
+    unsigned long long* __restrict__ mk_out, int* __restrict__ tok_out, int U) {
+    __shared__ unsigned char codes[kCodeTok][kMaxL * kM];
+    __shared__ float tail_s[kCodeTok];
+    __shared__ unsigned short queue[kCodeTok * kMaxL * kM];
+    __shared__ int qn;
+    const int ndir = L * kM;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int u = blockIdx.x / tiles_per_unit;
+    const long long t0 = (long long)(blockIdx.x % tiles_per_unit) * kCodeTok;
+    const long long t = t0 + tid;
+    const int e = e_unit[u];
+    const float sc = ldexpf(1.0f, -e), sc2 = ldexpf(1.0f, -2 * e);
+    if (tid == 0) qn = 0;
+    __syncthreads();
+    if (t < n) {
+        const long long g = (long long)u * n + t;
+        float rr = __fsub_rn(1.0f, __fmul_rn(nrm2[g], sc2));
+        rr = rr > 0.0f ? rr : 0.0f;
+        const float tail = __fsqrt_rn(rr);
+        tail_s[tid] = tail;
+        const float4* src = reinterpret_cast<const float4*>(praw + g * 16);
+        float raw[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 x = src[k];
+            raw[4 * k] = x.x;
+            raw[4 * k + 1] = x.y;
+            raw[4 * k + 2] = x.z;
+            raw[4 * k + 3] = x.w;
+        }
+#pragma unroll
+        for (int dd = 0; dd < kMaxL * kM; ++dd) {
+            if (dd >= ndir) break;
+            const float p = __fmaf_rn(dirs[(long long)dd * kDirStride + kD], tail, __fmul_rn(raw[dd], sc));
+            const float y = __fmul_rn(__fadd_rn(p, 1.0f), 128.0f);
+            const float fr = y - floorf(y);
+            codes[tid][dd] = (unsigned char)quantise_code(p);
+            if (fr < kCodeGuard || fr > 1.0f - kCodeGuard)
+                queue[atomicAdd(&qn, 1)] = (unsigned short)((tid << 4) | dd);
+        }
+    }
+    __syncthreads();
+    const __nv_bfloat16* ku = keys + (long long)u * n * kD;
+    for (int i = warp; i < qn; i += kCodeTok / 32) {  // warp-uniform
+        const int lt = queue[i] >> 4, dd = queue[i] & 15;
+        const int c = exact_code_warp(ku + (t0 + lt) * kD, sc, dirs + (long long)dd * kDirStride,
+                                      tail_s[lt], lane);
+        if (lane == 0) codes[lt][dd] = (unsigned char)c;
+    }
+    __syncthreads();
+    if (t < n) {
+        for (int l = 0; l < L; ++l) {
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = codes[tid][l * kM + j];
             const long long o = ((long long)l * U + u) * n + t;
             mk_out[o] = morton8(c);
             tok_out[o] = (int)t;
@@ -579,6 +894,43 @@ __global__ void __launch_bounds__(256) pack_kernel(IndexView v, const T* __restr
         if (e_ != cudaSuccess) return e_;   \
     } while (0)
 
+// The driver's tensor-map encoder, looked up once through the runtime (no link
+// against the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn key_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of the keys as a [rows][128] bf16 matrix: boxes of 64 dimensions x
+// 128 rows with the 128-byte swizzle (the layout the MMA descriptors expect);
+// rows past the end read as zeros.
+static bool encode_key_map(CUtensorMap* m, const void* keys, long long rows) {
+    EncodeTiledFn enc = key_map_encoder();
+    if (enc == nullptr || rows < 1 || rows > 0x7FFFFFFFLL) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTcRows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(keys), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Phase 1: keys -> sorted 96-bit keys and leaf numbering in scratch.
 cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long long n,
                          const float* dirs, bool dirs_bf16_exact, int* e_unit, BuildScratch& s,
@@ -586,18 +938,45 @@ cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long 
     const long long total = (long long)U * n;
     const int S = L * U;
     ICE_TRY(cudaMemsetAsync(s.umax, 0, sizeof(unsigned) * U, st));
-    const int nb = (int)((total + 255) / 256);
-    if (dtype == ICE_BF16)
-        norms_kernel<__nv_bfloat16><<<nb, 256, 0, st>>>((const __nv_bfloat16*)keys, total, n,
-                                                         s.nrm2, s.umax);
-    else
-        norms_kernel<float><<<nb, 256, 0, st>>>((const float*)keys, total, n, s.nrm2, s.umax);
+    ICE_TRY(cudaMemsetAsync(s.err, 0, sizeof(int), st));
+    // bf16 keys and +-1/16 directions: one read of the keys on the tensor cores
+    // (K1d), when the tensor-map encoder of the driver is at hand
+    CUtensorMap tmap;
+    const bool tc_path = dtype == ICE_BF16 && dirs_bf16_exact && s.praw != nullptr &&
+                         encode_key_map(&tmap, keys, total);
+    if (tc_path) {
+        static int nsm = 0;
+        if (nsm == 0) {
+            int dev = 0;
+            ICE_TRY(cudaGetDevice(&dev));
+            ICE_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+            ICE_TRY(cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTcSmem));
+        }
+        const int tpu = (int)((n + kTcRows - 1) / kTcRows);
+        const long long tiles = (long long)U * tpu;
+        const int grid = (int)std::min<long long>(tiles, 3LL * nsm);
+        project_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tmap, dirs, L, n, tpu, tiles, s.praw,
+                                                             s.nrm2, s.umax, s.err);
+    } else {
+        const int nb = (int)((total + 255) / 256);
+        if (dtype == ICE_BF16)
+            norms_kernel<__nv_bfloat16><<<nb, 256, 0, st>>>((const __nv_bfloat16*)keys, total, n,
+                                                             s.nrm2, s.umax);
+        else
+            norms_kernel<float><<<nb, 256, 0, st>>>((const float*)keys, total, n, s.nrm2, s.umax);
+    }
     ICE_TRY(cudaGetLastError());
     exponent_kernel<<<(U + 127) / 128, 128, 0, st>>>(s.umax, e_unit, U);
     ICE_TRY(cudaGetLastError());
     const int tpb = kProjThreads / (L * kM);
     const int tiles_u = (int)((n + tpb - 1) / tpb);
-    if (dtype == ICE_BF16 && dirs_bf16_exact) {
+    if (tc_path) {
+        const int tiles_c = (int)((n + kCodeTok - 1) / kCodeTok);
+        codes_tc_kernel<<<U * tiles_c, kCodeTok, 0, st>>>((const __nv_bfloat16*)keys, s.praw, s.nrm2,
+                                                          e_unit, dirs, L, n, tiles_c, s.mk[0],
+                                                          s.tk[0], U);
+    } else if (dtype == ICE_BF16 && dirs_bf16_exact) {
         const int tiles_m = (int)((n + kPmTok - 1) / kPmTok);
         project_mma_kernel<<<U * tiles_m, kPmWarps * 32, 0, st>>>(
             (const __nv_bfloat16*)keys, s.nrm2, e_unit, dirs, L, n, tiles_m, s.mk[0], s.tk[0], U);
@@ -648,11 +1027,14 @@ cudaError_t build_phase2(const IndexView& v, const void* keys, const void* value
     return cudaGetLastError();
 }
 
-cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st) {
+cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, bool with_praw,
+                          cudaStream_t st) {
     const long long SN = (long long)L * U * n;
     const long long tiles = (n + kSortTile - 1) / kSortTile;
     ICE_TRY(cudaMallocAsync((void**)&s.nrm2, sizeof(float) * U * n, st));
     ICE_TRY(cudaMallocAsync((void**)&s.umax, sizeof(unsigned) * U, st));
+    ICE_TRY(cudaMallocAsync((void**)&s.err, sizeof(int), st));
+    if (with_praw) ICE_TRY(cudaMallocAsync((void**)&s.praw, sizeof(float) * 16 * U * n, st));
     for (int b = 0; b < 2; ++b) {
         ICE_TRY(cudaMallocAsync((void**)&s.mk[b], sizeof(unsigned long long) * SN, st));
         ICE_TRY(cudaMallocAsync((void**)&s.tk[b], sizeof(int) * SN, st));
@@ -667,7 +1049,7 @@ cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream
 
 void scratch_free(BuildScratch& s, cudaStream_t st) {
     void* ptrs[] = {s.nrm2, s.umax, s.mk[0], s.mk[1], s.tk[0], s.tk[1], s.hist, s.leaf_of,
-                    s.leaf_start, s.tdepth, s.nleaf};
+                    s.leaf_start, s.tdepth, s.nleaf, s.praw, s.err};
     for (void* p : ptrs)
         if (p) cudaFreeAsync(p, st);
     s = BuildScratch();

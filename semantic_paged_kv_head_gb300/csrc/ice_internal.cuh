@@ -291,6 +291,8 @@ struct BuildScratch {
     int* leaf_start = nullptr;         // [L][U][n] first position of each leaf
     unsigned char* tdepth = nullptr;   // [L][U][n] leaf depth of each sorted position
     int* nleaf = nullptr;              // [L][U] leaves per segment
+    float* praw = nullptr;             // [U][n][16] unscaled projections (tensor-core path)
+    int* err = nullptr;                // set when a bounded wait of the build ran out
 };
 // dirs_bf16_exact: every direction component is exact in bf16 (the +-1/16
 // directions); bf16 keys then take the tensor-core projection.
@@ -299,7 +301,8 @@ cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long 
                          cudaStream_t st, int* final_buf);
 cudaError_t build_phase2(const IndexView& v, const void* keys, const void* values, long long n,
                          BuildScratch& s, int cur, cudaStream_t st);
-cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, cudaStream_t st);
+cudaError_t scratch_alloc(BuildScratch& s, int U, int L, long long n, bool with_praw,
+                          cudaStream_t st);
 void scratch_free(BuildScratch& s, cudaStream_t st);
 int select_smem_bytes(long long C, int L, int P, int n_cand, int n_sel, int G, bool fused);
 bool select_insert_fits(long long C, int L, int P, int n_cand, int n_sel, int es);
