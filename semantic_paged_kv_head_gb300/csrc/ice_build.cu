@@ -312,7 +312,9 @@ constexpr int kTcThreads = 128;              // one thread per token row, 4 warp
 constexpr int kTcTileB = kTcRows * kD * 2;   // 32 KB
 constexpr int kTcHalfB = kTcTileB / 2;       // one 64-dimension box
 constexpr int kTcDirB = 16 * kD * 2;         // 16 directions x 128 bf16
-constexpr int kTcSmem = 1024 + 2 * kTcTileB + kTcDirB;  // + alignment slack
+constexpr int kTcStages = 3;                 // tiles in shared memory (two copies ahead)
+constexpr int kTcSmem = 1024 + kTcStages * kTcTileB + kTcDirB;  // + alignment slack
+constexpr int kTcBlocksPerSm = 2;
 constexpr int kTcTmemCols = 32;
 
 // Shared-memory matrix descriptor of a K-major operand with the 128-byte
@@ -338,13 +340,13 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
     int tiles_per_unit, long long tiles_total, float* __restrict__ praw, float* __restrict__ nrm2,
     unsigned* __restrict__ umax, int* __restrict__ err) {
     extern __shared__ unsigned char tc_smem[];
-    __shared__ __align__(8) unsigned long long bar_full[2], bar_mma[2];
+    __shared__ __align__(8) unsigned long long bar_full[kTcStages], bar_mma;
     __shared__ unsigned tmem_slot;
     __shared__ int s_fail;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned raw0 = smem_u32(tc_smem);
     const unsigned base = (raw0 + 1023u) & ~1023u;  // the swizzle atoms need 1024-byte alignment
-    const unsigned sA0 = base, sA1 = base + kTcTileB, sB = base + 2 * kTcTileB;
+    const unsigned sB = base + kTcStages * kTcTileB;
     unsigned char* pB = tc_smem + (sB - raw0);
     // the directions in bf16 (exact for +-1/16): row j (direction), dimensions
     // 64h..64h+63 in half h; the 16-byte chunk c of row j sits at chunk c ^ (j mod 8)
@@ -362,10 +364,8 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
     }
     if (tid == 0) {
         s_fail = 0;
-        tc_mbar_init(smem_u32(&bar_full[0]));
-        tc_mbar_init(smem_u32(&bar_full[1]));
-        tc_mbar_init(smem_u32(&bar_mma[0]));
-        tc_mbar_init(smem_u32(&bar_mma[1]));
+        for (int k = 0; k < kTcStages; ++k) tc_mbar_init(smem_u32(&bar_full[k]));
+        tc_mbar_init(smem_u32(&bar_mma));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<unsigned long long>(&tmap)) : "memory");
     }
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
 
     auto issue = [&](long long tile, int s) {  // thread 0
         const unsigned bar = smem_u32(&bar_full[s]);
-        const unsigned dst = s ? sA1 : sA0;
+        const unsigned dst = base + s * kTcTileB;
         const long long uu = tile / tiles_per_unit;
         const int y = (int)(uu * n + (tile % tiles_per_unit) * kTcRows);
         const unsigned long long tm = reinterpret_cast<unsigned long long>(&tmap);
@@ -404,15 +404,17 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
     };
 
     long long tile = blockIdx.x;
-    if (tid == 0 && tile < tiles_total) issue(tile, 0);
+    if (tid == 0)
+        for (int k = 0; k + 1 < kTcStages; ++k)
+            if (tile + (long long)k * gridDim.x < tiles_total) issue(tile + (long long)k * gridDim.x, k);
     int it = 0;
     // s_fail: 1 = the tile's copy did not land in time, 2 = its MMAs did not finish
     for (; tile < tiles_total; tile += gridDim.x, ++it) {  // block-uniform
-        const int s = it & 1;
-        const unsigned ph = (unsigned)((it >> 1) & 1);
-        const unsigned sA = s ? sA1 : sA0;
-        const long long next = tile + gridDim.x;
-        if (tid == 0 && next < tiles_total) issue(next, s ^ 1);
+        const int s = it % kTcStages;
+        const unsigned ph = (unsigned)((it / kTcStages) & 1);
+        const unsigned sA = base + s * kTcTileB;
+        const long long ahead = tile + (long long)(kTcStages - 1) * gridDim.x;
+        if (tid == 0 && ahead < tiles_total) issue(ahead, (it + kTcStages - 1) % kTcStages);
         if (!mbar_wait_bounded(smem_u32(&bar_full[s]), ph)) s_fail = 1;
         __syncthreads();
         if (s_fail) break;
@@ -427,12 +429,12 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
                 const unsigned acc = ks > 0 ? 1u : 0u;
                 asm volatile(
                     "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                    " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem + 16u * s),
+                    " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
                     "l"(ad), "l"(bd), "r"(kTcIdesc), "r"(acc)
                     : "memory");
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                             smem_u32(&bar_mma[s]))
+                             smem_u32(&bar_mma))
                          : "memory");
         }
         // the token's squared norm in the fixed order, from the swizzled tile: lane
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
         }
         const float nrm = part[0];
         // the projections of the warp's 32 tokens from tensor memory
-        if (!mbar_wait_bounded(smem_u32(&bar_mma[s]), ph)) s_fail = 2;
+        if (!mbar_wait_bounded(smem_u32(&bar_mma), (unsigned)(it & 1))) s_fail = 2;
         __syncthreads();
         if (s_fail) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
               "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
               "=r"(r[14]), "=r"(r[15])
-            : "r"(tmem + ((unsigned)(32 * warp) << 16) + 16u * s)
+            : "r"(tmem + ((unsigned)(32 * warp) << 16))
             : "memory");
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         const long long uu = tile / tiles_per_unit;
@@ -509,12 +511,14 @@ __global__ void __launch_bounds__(kTcThreads) project_tc_kernel(
         // finish (bounded) before the tensor memory is released
         if (tid == 0) {
             atomicExch(err, 1);
-            const int s = it & 1;
-            const unsigned ph = (unsigned)((it >> 1) & 1);
-            if (s_fail == 1) mbar_wait_bounded(smem_u32(&bar_full[s]), ph);
-            else mbar_wait_bounded(smem_u32(&bar_mma[s]), ph);
-            if (tile + gridDim.x < tiles_total)  // the next tile's copy, use it + 1 of its buffer
-                mbar_wait_bounded(smem_u32(&bar_full[s ^ 1]), (unsigned)(((it + 1) >> 1) & 1));
+            if (s_fail == 1)
+                mbar_wait_bounded(smem_u32(&bar_full[it % kTcStages]), (unsigned)((it / kTcStages) & 1));
+            else
+                mbar_wait_bounded(smem_u32(&bar_mma), (unsigned)(it & 1));
+            for (int k = 1; k < kTcStages; ++k)  // the copies issued ahead
+                if (tile + (long long)k * gridDim.x < tiles_total)
+                    mbar_wait_bounded(smem_u32(&bar_full[(it + k) % kTcStages]),
+                                      (unsigned)(((it + k) / kTcStages) & 1));
         }
         __syncthreads();
     }
@@ -579,12 +583,35 @@ __global__ void __launch_bounds__(kCodeTok) codes_tc_kernel(
         }
     }
     __syncthreads();
+    // the queued values, four per warp at a time: all their rows are requested
+    // before any is reduced (one memory latency per round, not four)
     const __nv_bfloat16* ku = keys + (long long)u * n * kD;
-    for (int i = warp; i < qn; i += kCodeTok / 32) {  // warp-uniform
-        const int lt = queue[i] >> 4, dd = queue[i] & 15;
-        const int c = exact_code_warp(ku + (t0 + lt) * kD, sc, dirs + (long long)dd * kDirStride,
-                                      tail_s[lt], lane);
-        if (lane == 0) codes[lt][dd] = (unsigned char)c;
+    constexpr int kW = kCodeTok / 32, kB = 4;
+    for (int i0 = warp; i0 < qn; i0 += kW * kB) {  // warp-uniform
+        float x[kB][4];
+        float4 w[kB];
+        int lt[kB], dd[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int i = i0 + kW * b;
+            lt[b] = i < qn ? queue[i] >> 4 : 0;
+            dd[b] = i < qn ? queue[i] & 15 : 0;
+            load4_nc(ku + (t0 + lt[b]) * kD + 4 * lane, x[b]);
+            w[b] = __ldg(reinterpret_cast<const float4*>(dirs + (long long)dd[b] * kDirStride + 4 * lane));
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            float acc = 0.0f;  // the fixed-order dot of K1b: lane partial, then the pairwise tree
+            acc = __fmaf_rn(w[b].x, __fmul_rn(x[b][0], sc), acc);
+            acc = __fmaf_rn(w[b].y, __fmul_rn(x[b][1], sc), acc);
+            acc = __fmaf_rn(w[b].z, __fmul_rn(x[b][2], sc), acc);
+            acc = __fmaf_rn(w[b].w, __fmul_rn(x[b][3], sc), acc);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+            if (lane == 0 && i0 + kW * b < qn)
+                codes[lt[b]][dd[b]] = (unsigned char)quantise_code(
+                    __fmaf_rn(dirs[(long long)dd[b] * kDirStride + kD], tail_s[lt[b]], acc));
+        }
     }
     __syncthreads();
     if (t < n) {
@@ -955,7 +982,7 @@ cudaError_t build_phase1(int dtype, const void* keys, int U, int L, int P, long 
         }
         const int tpu = (int)((n + kTcRows - 1) / kTcRows);
         const long long tiles = (long long)U * tpu;
-        const int grid = (int)std::min<long long>(tiles, 3LL * nsm);
+        const int grid = (int)std::min<long long>(tiles, (long long)kTcBlocksPerSm * nsm);
         project_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tmap, dirs, L, n, tpu, tiles, s.praw,
                                                              s.nrm2, s.umax, s.err);
     } else {
