@@ -214,9 +214,11 @@ int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t
 /*
  * ice_decode_step - one decode step of every unit: ice_insert of the new
  * token's k, v, then ice_select_attn for the query q (the new token is a
- * candidate like any other). One kernel launch on `stream` (each block inserts
- * its unit's token, then selects and attends; with a host-resident pool, or
- * when the split's staging does not fit, the separate launches), no host
+ * candidate like any other). For a launch of many units, one kernel launch on
+ * `stream` (each block inserts its unit's token, then selects and attends);
+ * when the selection runs on a cluster of blocks per unit (few units, see
+ * ice_set_cluster_size), with a host-resident pool, or when the split's staging
+ * does not fit, the insert and the selection are separate launches. No host
  * synchronisation and no allocation, so a sequence of steps can be captured
  * once in a CUDA graph and replayed: the insert takes the token index from a
  * per-unit count kept on the device, which every replay advances (a unit at
@@ -291,8 +293,9 @@ int ice_get_info(const ice_index* ix, ice_info* info);
  *          block cannot hold the unit's tables);
  *   k = 1: one block per unit;
  *   k = 2, 4, 8, 16: that many blocks per unit (k >= n_composite).
- * The cluster path takes budget/page_size <= 32 pages; ice_select_attn_reuse,
- * ice_decode_step and ice_select_heads always use one block per unit. A call
+ * The cluster path takes budget/page_size <= 32 pages; ice_decode_step uses it
+ * after a separate insert launch; ice_select_attn_reuse and ice_select_heads
+ * always use one block per unit. A call
  * whose forced k cannot be launched (tables too large, or clusters of that
  * size not resident on this GPU) returns ICE_ERR_UNSUPPORTED or ICE_ERR_CUDA.
  * Returns ICE_ERR_INVALID_ARG for any other k.

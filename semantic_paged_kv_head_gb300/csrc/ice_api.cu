@@ -500,6 +500,18 @@ int ice_decode_step(ice_index* ix, const void* k, const void* v, const void* q,
     const int n_sel = token_budget / P;
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
     const int es = ix->p.dtype == ICE_BF16 ? 2 : 4;
+    // few units: the insert kernel, then the selection over a cluster of blocks per unit
+    // (two launches, both capturable); many units: one launch in which every block
+    // inserts its unit's token and then selects and attends
+    const int Kc = ix->v.cluster_k > 0 ? ix->v.cluster_k : select_cluster_auto(ix->U, ix->p.n_composite);
+    if (ix->p.kv_location == ICE_KV_DEVICE && Kc >= 2 &&
+        select_cluster_bytes(ix->v, Kc, n_sel, n_cand, true) >= 0) {
+        if (launch_insert(ix->v, k, v, (cudaStream_t)stream) != cudaSuccess) return ICE_ERR_CUDA;
+        ix->n_tok += 1;
+        cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, nullptr, out,
+                                      nullptr, (cudaStream_t)stream);
+        return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
+    }
     if (ix->p.kv_location == ICE_KV_DEVICE &&
         select_insert_fits(ix->C, ix->p.n_composite, P, n_cand, n_sel, es)) {
         // one launch: every block inserts its unit's token, then selects and attends

@@ -27,30 +27,39 @@ __device__ __forceinline__ void place_loc1(const IndexView& v, int u, int tok, i
 }
 
 // Shift leaf keys, records and the records' scan copies [from, N) one place to
-// the right (backwards, in chunks of one element per thread of the NT-thread block).
+// the right, backwards, in rounds of 1024 elements (1024 / NT per thread of the
+// NT-thread block): all loads of a round are in flight together, then the
+// stores (the next round reads only indices below the ones this round wrote).
 template <int NT>
 __device__ void shift_right(LeafKey* key, uint4* rec, unsigned long long* lo, unsigned short* tc,
                             int from, int N) {
-    for (int end = N; end > from; end -= NT) {
-        const int start = max(from, end - NT);
-        const int i = start + (int)threadIdx.x;
-        LeafKey k;
-        uint4 r;
-        unsigned long long a = 0;
-        unsigned short c = 0;
-        const bool act = i < end;
-        if (act) {
-            k = key[i];
-            r = rec[i];
-            a = lo[i];
-            c = tc[i];
+    constexpr int kShiftUnr = NT >= 1024 ? 1 : 1024 / NT;
+    for (int end = N; end > from; end -= NT * kShiftUnr) {
+        const int start = max(from, end - NT * kShiftUnr);
+        LeafKey k[kShiftUnr];
+        uint4 r[kShiftUnr];
+        unsigned long long a[kShiftUnr];
+        unsigned short c[kShiftUnr];
+#pragma unroll
+        for (int j = 0; j < kShiftUnr; ++j) {
+            const int i = start + (int)threadIdx.x + j * NT;
+            if (i < end) {
+                k[j] = key[i];
+                r[j] = rec[i];
+                a[j] = lo[i];
+                c[j] = tc[i];
+            }
         }
         __syncthreads();
-        if (act) {
-            key[i + 1] = k;
-            rec[i + 1] = r;
-            lo[i + 1] = a;
-            tc[i + 1] = c;
+#pragma unroll
+        for (int j = 0; j < kShiftUnr; ++j) {
+            const int i = start + (int)threadIdx.x + j * NT;
+            if (i < end) {
+                key[i + 1] = k[j];
+                rec[i + 1] = r[j];
+                lo[i + 1] = a[j];
+                tc[i + 1] = c[j];
+            }
         }
         __syncthreads();
     }
@@ -70,7 +79,7 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
     __shared__ unsigned int e_t[kMaxP + 1];
     __shared__ int e_slot[kMaxP + 1];  // original slot (P = the new token)
     __shared__ int s_sorted[kMaxP + 1];
-    __shared__ int s_lo, s_hi, s_cnt, s_abort;
+    __shared__ int s_cnt, s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = v.P;
@@ -81,6 +90,45 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
         if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
         return;
     }
+
+    // ---- the search for the new key's leaf runs for all composites at once: thread
+    //      group l (NT / L threads) searches composite l. The leaf counts come first;
+    //      the first probes are requested while warp 0 forms the new key's codes.
+    __shared__ int s_N[kMaxL], s_nid[kMaxL], s_lo2[kMaxL], s_hi2[kMaxL], s_a[kMaxL], s_fin[kMaxL];
+    __shared__ LeafKey s_pk[kMaxL];
+    __shared__ uint4 s_pr[kMaxL];
+    const int Lc = v.L;
+    if (tid < Lc) {
+        s_N[tid] = v.n_leaf[v.ul(u, tid)];
+        s_nid[tid] = v.next_id[v.ul(u, tid)];
+        s_lo2[tid] = 0;
+        s_a[tid] = -1;
+        s_fin[tid] = 0;
+        s_pr[tid] = make_uint4(0u, 0u, 0u, 0u);
+        s_pk[tid] = LeafKey{0ull, 0u, 0u};
+    }
+    if (tid == 0) s_abort = 0;
+    __syncthreads();
+    if (tid < Lc) s_hi2[tid] = s_N[tid];
+    const int gsz = NT / Lc, gl = tid / gsz, gi = tid - gl * gsz;
+    const bool in_group = gl < Lc;
+    // probe of this thread in the current round: leaf key and record (the record of
+    // the last probe at or below the key is the leaf's, without another round trip)
+    auto probe = [&](int lo, int hi, int& i, LeafKey& k, uint4& r) {
+        const int span = hi - lo;
+        const int step = span <= gsz ? 1 : (span + gsz - 1) / gsz;
+        i = lo + gi * step;
+        if (in_group && i < hi) {
+            const long long lb = v.leaf_base(u, gl);
+            k = v.leaf_key[lb + i];
+            r = v.leaf_rec[lb + i];
+        }
+        return step;
+    };
+    int pi = 0, pstep = 0;
+    LeafKey pk{0ull, 0u, 0u};
+    uint4 pr = make_uint4(0u, 0u, 0u, 0u);
+    if (in_group) pstep = probe(0, s_N[gl], pi, pk, pr);
 
     // ---- key of the new token: frozen scale, projections, codes (warp 0) ----------
     if (warp == 0) {
@@ -108,8 +156,47 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
             if (lane == 0) s_mk[l] = morton8(c);
         }
     }
-    if (tid == 0) s_abort = 0;
     __syncthreads();
+    // k-ary rounds: a = number of leaves whose prefix <= x, per composite
+    __shared__ int s_cntp[kMaxL];
+    for (int round = 0; round < 64; ++round) {  // block-uniform; ends when every composite is done
+        if (tid < Lc) s_cntp[tid] = 0;
+        __syncthreads();
+        bool le = false;
+        if (in_group && !s_fin[gl] && pi < s_hi2[gl])
+            le = !key_less(s_mk[gl], (unsigned)tok, pk.pm, pk.pt);
+        if (le) atomicAdd(&s_cntp[gl], 1);
+        __syncthreads();
+        if (in_group && !s_fin[gl]) {
+            const int c = s_cntp[gl];
+            const int lo = s_lo2[gl], hi = s_hi2[gl];
+            // the last probe at or below the key publishes its leaf (keys are sorted)
+            if (c > 0 && gi == c - 1) {
+                s_pk[gl] = pk;
+                s_pr[gl] = pr;
+            }
+            if (pstep == 1) {  // every leaf of [lo, hi) was probed: done
+                if (gi == 0) {
+                    s_a[gl] = lo + c;
+                    s_fin[gl] = 1;
+                }
+            } else if (c == 0) {
+                if (gi == 0) {
+                    s_a[gl] = lo;
+                    s_fin[gl] = 1;
+                }
+            } else if (gi == 0) {
+                const int pc = lo + (c - 1) * pstep;
+                s_lo2[gl] = pc + 1;
+                s_hi2[gl] = min(hi, pc + pstep);
+            }
+        }
+        __syncthreads();
+        bool all = true;
+        for (int l = 0; l < Lc; ++l) all = all && s_fin[l];
+        if (all) break;
+        if (in_group && !s_fin[gl]) pstep = probe(s_lo2[gl], s_hi2[gl], pi, pk, pr);
+    }
 
     for (int l = 0; l < v.L; ++l) {
         const unsigned long long xm = s_mk[l];
@@ -122,61 +209,22 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
         int* cntl = v.list_cnt + v.leaf_base(u, l);
         int* stok = v.slot_tok + v.slot_base(u, l);
         unsigned long long* skey = v.slot_key + v.slot_base(u, l);
-        const int N = v.n_leaf[v.ul(u, l)];
-        const int nid = v.next_id[v.ul(u, l)];
-
-        // ---- a = number of leaves whose prefix <= x (k-ary search) --------------------
-        if (tid == 0) {
-            s_lo = 0;
-            s_hi = N;
-        }
-        __syncthreads();
-        int a = -1;
-        while (a < 0) {
-            const int lo = s_lo, hi = s_hi;
-            if (hi - lo <= NT) {
-                const int i = lo + tid;
-                bool le = false;
-                if (i < hi) {
-                    const LeafKey k = lk[i];
-                    le = !key_less(xm, xt, k.pm, k.pt);
-                }
-                a = lo + __syncthreads_count(le);
-                break;
-            }
-            const int step = (hi - lo + NT - 1) / NT;
-            const int i = lo + tid * step;
-            bool le = false;
-            if (i < hi) {
-                const LeafKey k = lk[i];
-                le = !key_less(xm, xt, k.pm, k.pt);
-            }
-            const int c = __syncthreads_count(le);
-            if (c == 0) {
-                a = lo;
-                break;
-            }
-            if (tid == 0) {
-                const int pc = lo + (c - 1) * step;
-                s_lo = pc + 1;
-                s_hi = min(hi, pc + step);
-            }
-            __syncthreads();
-        }
-        const int pos = a - 1;  // last leaf with prefix <= x, or -1
+        const int N = s_N[l];
+        const int nid = s_nid[l];
+        const int pos = s_a[l] - 1;  // last leaf with prefix <= x, or -1
         bool member = false;
         uint4 rc = make_uint4(0u, 0u, 0u, 0u);
         if (pos >= 0) {
-            const LeafKey k = lk[pos];
+            const LeafKey k = s_pk[l];
             unsigned long long pm;
             unsigned int pt;
             prefix96(xm, xt, (int)k.t, pm, pt);
             member = pm == k.pm && pt == k.pt;
-            rc = lr[pos];
+            rc = s_pr[l];
         }
         const int id = rec_id(rc), cnt = rec_cnt(rc);
         const bool split = member && cnt >= P;
-        __syncthreads();  // every thread has read the record before any thread updates it
+        __syncthreads();  // every thread has read the leaf before any thread updates it
         // capacity: a split or a new leaf needs one more leaf record and list id
         if (!(member && !split) && (N + 1 > v.C || nid + 1 > v.C)) {
             if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
