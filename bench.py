@@ -477,6 +477,9 @@ def insert_run(ice, synth, dev, flush, timed, args):
     torch.cuda.synchronize()
     ix.check()
     us_ins = e0.elapsed_time(e1) * 1e3 / w.n_insert
+    after = sa_us(q1)
+    ix.check()
+    leaves1 = [ix.dump(u)["n_leaf"] for u in range(U)]
     # device time of an insert: a CUDA graph of ins_graph inserts, replayed (the eager
     # loop above is bound by the host's call overhead)
     kg, vg = K[0].clone(), V[0].clone()
@@ -486,9 +489,6 @@ def insert_run(ice, synth, dev, flush, timed, args):
             ix.insert(kg, vg)
     t_ig = timed(gi.replay, ins_reps)
     ix.check()
-    after = sa_us(q1)
-    ix.check()
-    leaves1 = [ix.dump(u)["n_leaf"] for u in range(U)]
     n_fin = w.n_tokens + w.n_insert
     # whole decode steps (insert + select + attention): eager calls against the
     # replay of one step captured in a CUDA graph
