@@ -85,6 +85,33 @@ struct IndexView {
     }
 };
 
+// ---- programmatic dependent launch ---------------------------------------------
+// The decode-path kernels are launched with the programmatic stream-serialization
+// attribute, so that a kernel's launch (block scheduling, shared-memory setup)
+// overlaps the previous kernel of the stream. Each kernel waits here, before its
+// first global memory access, until the previous kernel has completed and its
+// writes are visible, and then lets the next kernel of the stream be scheduled.
+// Launched without the attribute, both instructions return at once.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename Kern, typename... Act>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Act&&>(args)...);
+}
+
 // ---- status word -----------------------------------------------------------
 __device__ __forceinline__ void set_status(int* status, int code) {
     atomicCAS(status, 0, code);

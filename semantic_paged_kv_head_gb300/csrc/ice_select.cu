@@ -321,6 +321,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     __shared__ int s_ncand, s_nraw, s_npg, s_ntok, s_fail, s_cmp;
     __shared__ __align__(8) unsigned long long s_bar;
 
+    pdl_wait_then_release();
     // head_div > 1: per-query-head selection, block = (unit, head), row = block
     const int u = blockIdx.x / head_div, row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1036,14 +1037,12 @@ static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel,
     const bool fused = out != nullptr;
     const int bytes = select_smem_bytes(v.C, v.L, v.P, n_cand, n_sel, G, fused);
     if (fused)
-        select_kernel<T, G, true><<<v.U, kSelThreads, bytes, s>>>(
-            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, (T*)out,
-            reselect, 1, (const T*)knew, (const T*)vnew);
-    else
-        select_kernel<T, G, false><<<v.U, kSelThreads, bytes, s>>>(
-            v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats, nullptr,
-            reselect, 1, nullptr, nullptr);
-    return cudaGetLastError();
+        return launch_pdl(select_kernel<T, G, true>, dim3(v.U), dim3(kSelThreads), (size_t)bytes, s, v,
+                          (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats,
+                          (T*)out, reselect, 1, (const T*)knew, (const T*)vnew);
+    return launch_pdl(select_kernel<T, G, false>, dim3(v.U), dim3(kSelThreads), (size_t)bytes, s, v,
+                      (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats,
+                      (T*)nullptr, reselect, 1, (const T*)nullptr, (const T*)nullptr);
 }
 
 template <typename T>

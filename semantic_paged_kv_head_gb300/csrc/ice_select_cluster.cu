@@ -356,6 +356,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     __shared__ int s_pstar, s_need, s_nch, s_base, s_ncand, s_cmp, s_fail, s_gn, s_taken, s_nl[kMaxL];
     __shared__ __align__(8) unsigned long long s_bar;
 
+    pdl_wait_then_release();
     cg::cluster_group cluster = cg::this_cluster();
     const int K = (int)cluster.num_blocks();
     const int r = (int)cluster.block_rank();
@@ -1118,13 +1119,15 @@ cudaError_t clu_launch(const IndexView& v, const CluPlan& p, const void* q, int 
     cfg.blockDim = dim3(kCT);
     cfg.dynamicSmemBytes = (size_t)p.bytes;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned)p.K;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait_then_release
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, v, (const T*)q, n_sel, p.d, p.bytes, page_ids, n_pages,
                               stats, (T*)out);
 }
