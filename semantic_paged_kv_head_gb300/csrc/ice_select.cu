@@ -73,7 +73,7 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
     int o = 0;
     s.sel = o; o = align16(o + n_sel * 4);
     s.toff = o; o = align16(o + (n_sel + 1) * 4);
-    s.qf = o; o = align16(o + kMaxG * kD * 4);
+    s.qf = o; o = align128(o + kMaxG * kD * 4);
     s.keys = o; o = align16(o + sort_cap * 8);
     s.vals = o; o = align16(o + sort_cap * 4);
     s.hpage = o; o = align16(o + hcap * 4);
@@ -82,6 +82,7 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
     s.top = o; o = align16(o + kSelWarps * kTopK * 12);
     s.ring = s.keys;  // the scan's copy ring, dead before the candidates are written
     if (o < s.ring + kRingB) o = s.ring + kRingB;
+    o = align128(o);
     s.free = o;
     const int Cp = align16((int)C);
     s.prio = o; o = align16(o + L * Cp);
@@ -778,8 +779,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         constexpr int EPC = 16 / (int)sizeof(T);  // elements per piece
         constexpr int CPR = kD / EPC;             // pieces per row
         constexpr int ROWB = kD * (int)sizeof(T);
-        unsigned char* stg = smem + lay.free;
-        const int half = min((smem_total - lay.free) / (2 * ROWB), kSelThreads / 2);  // rows per half (two threads a row)
+        const int pad = pad_to_128(smem + lay.free);  // 0 when the window starts aligned
+        unsigned char* stg = smem + lay.free + pad;
+        const int half = min((smem_total - lay.free - pad) / (2 * ROWB), kSelThreads / 2);  // rows per half (two threads a row)
         const int nchunk = (ncand + half - 1) / half;
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = hcap - 1;

@@ -89,6 +89,7 @@ __host__ __device__ inline CluSmem clu_layout(long long C, const CluDims& d, int
     s.hub_part = o; o = align16(o + (fused ? K * (G * (kD + 2) + 4) * 4 : 0));
     s.qf = o; o = align16(o + (fused ? G * kD * 4 : 0));
     s.bm0 = o; o = align16(o + (L > 1 ? (int)((C + 31) / 32) * 4 : 0));
+    o = align128(o);  // the scan's copy ring starts here
     s.X = o;
     int a = o;  // scan
     s.ring = a; a = align16(a + kCRingB);
@@ -110,6 +111,7 @@ __host__ __device__ inline CluSmem clu_layout(long long C, const CluDims& d, int
     s.hkey = b; b = align16(b + d.hcap_l * 8);
     s.hcnt = b; b = align16(b + d.hcap_l * 4);
     s.top = b; b = align16(b + kCW * 32 * 12);
+    b = align128(b);
     s.stage = b;
     int g = o;  // ranking
     s.g_page = g; g = align16(g + d.gcap * 4);
@@ -794,8 +796,9 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         constexpr int EPC = 16 / (int)sizeof(T);
         constexpr int CPR = kD / EPC;
         constexpr int ROWB = kD * (int)sizeof(T);
-        unsigned char* stg = smem + lay.stage;
-        const int half = min((smem_total - lay.stage) / (2 * ROWB), kCT / 2);
+        const int pad = pad_to_128(smem + lay.stage);  // 0 when the window starts aligned
+        unsigned char* stg = smem + lay.stage + pad;
+        const int half = min((smem_total - lay.stage - pad) / (2 * ROWB), kCT / 2);
         const int nchunk = (ncand + half - 1) / half;
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = dm.hcap_l - 1;

@@ -13,6 +13,17 @@ namespace ice {
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // bounded barrier wait
 
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
+// Regions that asynchronous copies fill from global memory start on a 128-byte
+// boundary: a 128-byte line then lands in one 128-byte piece of shared memory
+// and travels as one request. A destination 16 bytes off splits every line
+// into several requests; over the host link that doubled the bytes read
+// (each partial request fetched more than it asked for).
+__host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
+
+// Bytes from p up to the next 128-byte boundary of the shared-memory window.
+__device__ __forceinline__ int pad_to_128(const void* p) {
+    return (int)((128u - ((unsigned)__cvta_generic_to_shared(p) & 127u)) & 127u);
+}
 
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
