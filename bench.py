@@ -34,6 +34,8 @@ WORKLOAD = "llama8b_36k"
 FUSED_KERNEL, FUSED_SRC = "select_kernel<fused>", "ice_select.cu"
 FLUSH_BYTES = 256 << 20
 INSERT_WORKLOAD = "mistral7b_gen8k"
+# the single-replica measurements after the headline, in the order they run
+EXTRAS = ("per_layer_serial", "insert", "host_kv", "reuse", "recall")
 
 
 def leaf_bytes(w):
@@ -276,6 +278,8 @@ def host_kv_run(ice, w, keys, values, q, flush, timed, args, st):
     import torch
     ix = ice.IceIndex.build(keys, values, page_size=w.page_size, n_q_heads=w.n_q_heads,
                             n_composite=w.n_composite, n_proj=w.n_proj, seed=w.seed, kv_host=True)
+    if args.cluster_size is not None:
+        ix.set_cluster_size(args.cluster_size)
     out = torch.empty_like(q)
     n = max(20, args.steps // 30)
     timed(lambda: ix.select_attn(q, w.budget, out), 3)
@@ -819,12 +823,25 @@ def run_ice(args):
                     "samples": n_w,
                     "note": "no L2 flush between steps; median of per-step event pairs"}
     if not args.no_extras and world == 1:  # single-replica extras (not part of scaling runs)
-        line["per_layer_serial"] = per_layer_serial(ice, w, keys, values, q, per_step, args,
-                                                    step_bytes, peak)
-        line["insert"] = insert_run(ice, synth, dev, flush, timed, args)
-        line["host_kv"] = host_kv_run(ice, w, keys, values, q, flush, timed, args, st)
-        line["reuse"] = reuse_run(ice, synth, ix, w, centers, flush, timed, args)
-        line["recall"] = recall_run(ice, w, keys, values, q, flush, timed, args)
+        runs = {
+            "per_layer_serial": lambda: per_layer_serial(ice, w, keys, values, q, per_step, args,
+                                                         step_bytes, peak),
+            "insert": lambda: insert_run(ice, synth, dev, flush, timed, args),
+            "host_kv": lambda: host_kv_run(ice, w, keys, values, q, flush, timed, args, st),
+            "reuse": lambda: reuse_run(ice, synth, ix, w, centers, flush, timed, args),
+            "recall": lambda: recall_run(ice, w, keys, values, q, flush, timed, args),
+        }
+        chosen = [e for e in args.extras.split(",") if e]
+        for name in chosen:
+            if name not in runs:
+                raise SystemExit(f"unknown extra {name!r}; choose from {','.join(EXTRAS)}")
+        for name in EXTRAS:
+            if name in chosen:
+                # an NVTX range per extra, so that a profiler can take the launches of one
+                torch.cuda.nvtx.range_push(name)
+                line[name] = runs[name]()
+                torch.cuda.synchronize()
+                torch.cuda.nvtx.range_pop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_units = sorted({0, U // 3, (2 * U) // 3, U - 1})
         ku = [keys.view(U, w.n_tokens, w.d)[u].cpu() for u in sample_units]
@@ -870,6 +887,8 @@ def main():
                     help="blocks per unit of the selection (0 automatic; profiling)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-layer-serial, insert and parallel-oracle measurements")
+    ap.add_argument("--extras", default=",".join(EXTRAS),
+                    help="comma list of the extras to run (profiling one of them): " + ",".join(EXTRAS))
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
