@@ -919,14 +919,27 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
             atomicAdd(&hubx0[3], ncand);
             atomicAdd(&hubx0[4], j1 - j0);
         }
-        unsigned long long tk;
-        int tv;
-        block_top32(ck, cpg, npl, reinterpret_cast<unsigned long long*>(smem + lay.top),
-                    reinterpret_cast<int*>(smem + lay.top + kCW * 32 * 8), tk, tv);
-        if (warp == 0 && lane < min(npl, n_sel)) {
-            uint4* pe0 = cluster.map_shared_rank(hub_pe, 0) + r * n_sel;
-            pe0[lane] = make_uint4((unsigned)tk, (unsigned)(tk >> 32), (unsigned)hpage[tv],
-                                   (unsigned)hcnt[tv]);
+        uint4* pe0 = cluster.map_shared_rank(hub_pe, 0) + r * n_sel;
+        if (npl <= kCT) {
+            // a page's place among this block's pages: the number with a smaller key
+            if (tid < npl) {
+                const unsigned long long key = ck[tid];
+                int rank = 0;
+                for (int j = 0; j < npl; ++j) rank += ck[j] < key ? 1 : 0;
+                if (rank < n_sel) {
+                    const int hh = cpg[tid];
+                    pe0[rank] = make_uint4((unsigned)key, (unsigned)(key >> 32), (unsigned)hpage[hh],
+                                           (unsigned)hcnt[hh]);
+                }
+            }
+        } else {
+            unsigned long long tk;
+            int tv;
+            block_top32(ck, cpg, npl, reinterpret_cast<unsigned long long*>(smem + lay.top),
+                        reinterpret_cast<int*>(smem + lay.top + kCW * 32 * 8), tk, tv);
+            if (warp == 0 && lane < min(npl, n_sel))
+                pe0[lane] = make_uint4((unsigned)tk, (unsigned)(tk >> 32), (unsigned)hpage[tv],
+                                       (unsigned)hcnt[tv]);
         }
     }
     clu_arrive();
