@@ -62,7 +62,7 @@ struct CluSmem {
     int X;  // phase region: scan tables, then candidates, then ranking, then attention staging
     int ring, prio, cnt, lid, tieb, hist, ghist, gpre, chosen, cmeta;  // scan
     int tl, toffc, skey, sval, hpage, hkey, hcnt, top, stage;     // candidates (stage: rows)
-    int g_page, g_key, g_cnt, gk, gp, gc;                         // ranking
+    int g_page, g_key, gk, gp;                                    // ranking
     int end;
 };
 
@@ -116,10 +116,8 @@ __host__ __device__ inline CluSmem clu_layout(long long C, const CluDims& d, int
     int g = o;  // ranking
     s.g_page = g; g = align16(g + d.gcap * 4);
     s.g_key = g; g = align16(g + d.gcap * 8);
-    s.g_cnt = g; g = align16(g + d.gcap * 4);
     s.gk = g; g = align16(g + K * n_sel * 8);
     s.gp = g; g = align16(g + K * n_sel * 4);
-    s.gc = g; g = align16(g + K * n_sel * 4);
     int e = a > b ? a : b;
     e = g > e ? g : e;
     s.end = e > min_total ? e : min_total;
@@ -950,10 +948,8 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     if (r == 0) {
         int* g_page = reinterpret_cast<int*>(smem + lay.g_page);
         unsigned long long* g_key = reinterpret_cast<unsigned long long*>(smem + lay.g_key);
-        int* g_cnt = reinterpret_cast<int*>(smem + lay.g_cnt);
-        unsigned long long* gk = reinterpret_cast<unsigned long long*>(smem + lay.gk);
-        int* gp = reinterpret_cast<int*>(smem + lay.gp);
-        int* gc = reinterpret_cast<int*>(smem + lay.gc);
+        unsigned long long* gk = reinterpret_cast<unsigned long long*>(smem + lay.gk);  // [K n_sel]
+        int* gslot = reinterpret_cast<int*>(smem + lay.gp);                            // [K n_sel]
         for (int i2 = tid; i2 < dm.gcap; i2 += kCT) {
             g_page[i2] = -1;
             g_key[i2] = ~0ull;
@@ -961,73 +957,72 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         if (tid == 0) s_gn = 0;
         __syncthreads();
         const int gmask = dm.gcap - 1;
-        for (int e = tid; e < K * n_sel; e += kCT) {
+        const int NE = K * n_sel;
+        // each entry takes its page's slot in the table and lowers the page's minimum
+        for (int e = tid; e < NE; e += kCT) {
             const int rr = e / n_sel;
-            if (e - rr * n_sel >= min(hubx[8 + rr], n_sel)) continue;
-            const uint4 x = hub_pe[e];
-            const unsigned long long key = ((unsigned long long)x.y << 32) | x.x;
-            const int pg = (int)x.z;
-            unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
-            for (int probe = 0; probe < dm.gcap; ++probe) {
-                const int old = atomicCAS(&g_page[hh], -1, pg);
-                if (old == -1 || old == pg) {
-                    if (old == -1) g_cnt[hh] = (int)x.w;
-                    atomicMin(&g_key[hh], key);
-                    break;
+            int slot = -1;
+            if (e - rr * n_sel < min(hubx[8 + rr], n_sel)) {
+                const uint4 x = hub_pe[e];
+                const unsigned long long key = ((unsigned long long)x.y << 32) | x.x;
+                const int pg = (int)x.z;
+                unsigned hh = ((unsigned)pg * 2654435761u) & (unsigned)gmask;
+                for (int probe = 0; probe < dm.gcap; ++probe) {
+                    const int old = atomicCAS(&g_page[hh], -1, pg);
+                    if (old == -1 || old == pg) {
+                        atomicMin(&g_key[hh], key);
+                        slot = (int)hh;
+                        break;
+                    }
+                    hh = (hh + 1) & (unsigned)gmask;
                 }
-                hh = (hh + 1) & (unsigned)gmask;
             }
+            gslot[e] = slot;
         }
         __syncthreads();
-        for (int h0 = warp * 32; h0 < dm.gcap; h0 += kCT) {  // warp-uniform
-            const int hh = h0 + lane;
-            const int pg = hh < dm.gcap ? g_page[hh] : -1;
-            const unsigned km = __ballot_sync(0xffffffffu, pg >= 0);
-            int base = 0;
-            if (lane == 0 && km) base = atomicAdd(&s_gn, __popc(km));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (pg >= 0) {
-                const int pos = base + __popc(km & ((1u << lane) - 1u));
-                gk[pos] = g_key[hh];
-                gp[pos] = pg;
-                gc[pos] = g_cnt[hh];
+        // an entry that holds its page's minimum keeps its key, every other entry ~0
+        for (int e = tid; e < NE; e += kCT) {
+            unsigned long long w = ~0ull;
+            if (gslot[e] >= 0) {
+                const uint4 x = hub_pe[e];
+                const unsigned long long key = ((unsigned long long)x.y << 32) | x.x;
+                if (g_key[gslot[e]] == key) w = key;
             }
+            gk[e] = w;
         }
         __syncthreads();
-        const int gn = s_gn;
-        const int taken = min(n_sel, gn);
-        // the rank of a page is the number of pages with a smaller key (keys are unique)
-        for (int i2 = tid; i2 < gn; i2 += kCT) {
-            const unsigned long long key = gk[i2];
+        // the rank of a page is the number of kept keys below its own (keys are unique);
+        // tpe adjacent threads share an entry's count and add their parts
+        const int tpe = NE <= kCT / 8 ? 8 : NE <= kCT / 4 ? 4 : NE <= kCT / 2 ? 2 : 1;
+        for (int base = 0; base < NE * tpe; base += kCT) {  // block-uniform
+            const int idx = base + tid;
+            const int e = idx / tpe, part = idx % tpe;
+            const bool live = idx < NE * tpe;
+            const unsigned long long key = live ? gk[e] : ~0ull;
             int rank = 0;
+            if (key != ~0ull) {
+                const int jlo = part * NE / tpe, jhi = (part + 1) * NE / tpe;
 #pragma unroll 8
-            for (int j2 = 0; j2 < gn; ++j2) rank += gk[j2] < key ? 1 : 0;
-            if (rank < n_sel) {
-                s_sel[rank] = gp[i2];
-                s_scnt[rank] = gc[i2];
+                for (int j2 = jlo; j2 < jhi; ++j2) rank += gk[j2] < key ? 1 : 0;
+            }
+            for (int o = 1; o < tpe; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+            if (key != ~0ull && part == 0) {
+                atomicAdd(&s_gn, 1);
+                if (rank < n_sel) {
+                    const uint4 x = hub_pe[e];
+                    s_sel[rank] = (int)x.z;
+                    s_scnt[rank] = (int)x.w;
+                }
             }
         }
+        __syncthreads();
+        const int taken = min(n_sel, s_gn);
         if (tid >= taken && tid < n_sel) {
             s_sel[tid] = -1;
             s_scnt[tid] = 0;
         }
         if (tid == 0) s_taken = taken;
         __syncthreads();
-        if (warp == 0) {
-            if (lane < n_sel) page_ids[(long long)u * n_sel + lane] = s_sel[lane];
-            int tok_sel = lane < taken ? s_scnt[lane] : 0;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
-            if (lane == 0) {
-                n_pages_out[u] = taken;
-                if (stats) {
-                    stats[4 * u + 0] = Nall;
-                    stats[4 * u + 1] = hubx[3];
-                    stats[4 * u + 2] = tok_sel;
-                    stats[4 * u + 3] = hubx[4];
-                }
-            }
-        }
         if (FUSED) {  // the selection to the other blocks
             for (int e = tid; e < (K - 1) * n_sel; e += kCT) {
                 const int rr = 1 + e / n_sel, i2 = e % n_sel;
@@ -1038,14 +1033,27 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         }
     }
     if (tid == 0 && ncand < s_ncand) set_status(v.status, ICE_ERR_CAPACITY);
-    if (!FUSED) {
-        // block 0 keeps its tables until every block has finished
-        clu_arrive();
-        clu_wait();
-        return;
-    }
     clu_arrive();
+    // block 0 writes the selection out while the barrier completes (block 0 keeps its
+    // tables until every block has passed it)
+    if (r == 0 && warp == 0) {
+        const int taken = s_taken;
+        if (lane < n_sel) page_ids[(long long)u * n_sel + lane] = s_sel[lane];
+        int tok_sel = lane < taken ? s_scnt[lane] : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
+        if (lane == 0) {
+            n_pages_out[u] = taken;
+            if (stats) {
+                stats[4 * u + 0] = Nall;
+                stats[4 * u + 1] = hubx[3];
+                stats[4 * u + 2] = tok_sel;
+                stats[4 * u + 3] = hubx[4];
+            }
+        }
+    }
     clu_wait();
+    if (!FUSED) return;
     const int taken = s_taken;
 
     // ---- 8. attention over this block's pages; the partials are merged in block 0 -----------
