@@ -316,6 +316,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     int head_div, const T* __restrict__ knew, const T* __restrict__ vnew) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float2 s_qp[kD / 2];  // (q_sel[e], q_sel[e + 64]), e < 64
+    __shared__ __align__(16) float s_qt[kD];        // q~, the normalised q_sel
     __shared__ int s_qcode[kMaxL][kM];
     __shared__ __align__(16) __half2 s_width[97 * 4];
     __shared__ int s_pstar[kMaxL], s_need[kMaxL], s_nch[kMaxL], s_tot[kMaxL];
@@ -383,10 +384,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     // ---- 1. leaf counts, query heads and directions requested together -------------------
     int N[kMaxL] = {0, 0};
     for (int l = 0; l < L; ++l) N[l] = v.n_leaf[v.ul(u, l)];
-    float qh[G][4];
+    float qh[G][4];  // warp 0 only
     const T* qu = q + (long long)row * G * kD;
+    if (warp == 0)
 #pragma unroll
-    for (int h = 0; h < G; ++h) load4(qu + (long long)h * kD + 4 * lane, qh[h]);
+        for (int h = 0; h < G; ++h) load4(qu + (long long)h * kD + 4 * lane, qh[h]);
     float wdir[4] = {0.f, 0.f, 0.f, 0.f};
     float wlast = 0.f;
     if (warp < L * kM) {
@@ -448,25 +450,23 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     for (int l = 0; l < L; ++l) N[l] = N[l] < 0 ? 0 : (N[l] > C ? (int)C : N[l]);
     const int Ntot = N[0] + N[1];
 
-    // query prep
+    // query prep: q_sel = the heads' sum in head order and q~ = q_sel / |q_sel| once
+    // (warp 0, into shared memory), then the codes (warp j: direction j)
     {
-        float qs[4] = {qh[0][0], qh[0][1], qh[0][2], qh[0][3]};
-#pragma unroll
-        for (int h = 1; h < G; ++h)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) qs[k] = __fadd_rn(qs[k], qh[h][k]);
-        const float nq = warp_dot_fixed(qs, qs);
-        float qt[4] = {0.f, 0.f, 0.f, 0.f};
-        if (nq > 0.0f) {
-            const float sn = __fsqrt_rn(nq);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) qt[k] = __fdiv_rn(qs[k], sn);
-        }
-        if (warp < L * kM) {
-            const float p = __fmaf_rn(wlast, 0.0f, warp_dot_fixed(wdir, qt));
-            if (lane == 0) s_qcode[warp / kM][warp % kM] = quantise_code(p);
-        }
         if (warp == 0) {
+            float qs[4] = {qh[0][0], qh[0][1], qh[0][2], qh[0][3]};
+#pragma unroll
+            for (int h = 1; h < G; ++h)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) qs[k] = __fadd_rn(qs[k], qh[h][k]);
+            const float nq = warp_dot_fixed(qs, qs);
+            float qt[4] = {0.f, 0.f, 0.f, 0.f};
+            if (nq > 0.0f) {
+                const float sn = __fsqrt_rn(nq);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) qt[k] = __fdiv_rn(qs[k], sn);
+            }
+            *reinterpret_cast<float4*>(s_qt + 4 * lane) = make_float4(qt[0], qt[1], qt[2], qt[3]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int e = 4 * lane + k;
@@ -480,6 +480,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 #pragma unroll
                     for (int k = 0; k < 4; ++k) qf[hh * kD + 4 * lane + k] = qh[hh][k];
             }
+        }
+        __syncthreads();
+        if (warp < L * kM) {
+            const float4 t4 = *reinterpret_cast<const float4*>(s_qt + 4 * lane);
+            const float qt[4] = {t4.x, t4.y, t4.z, t4.w};
+            const float p = __fmaf_rn(wlast, 0.0f, warp_dot_fixed(wdir, qt));
+            if (lane == 0) s_qcode[warp / kM][warp % kM] = quantise_code(p);
         }
     }
     __syncthreads();
@@ -807,84 +814,86 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             const unsigned char* stgc = stg + (ch & 1) * half * ROWB;
             asm volatile("cp.async.wait_group 1;" ::: "memory");  // chunk ch has landed
             __syncthreads();
-            // two threads per row: thread t of the pair owns the virtual lanes l with
-            // bit 1 of l equal to t, so the tree's levels 16, 8 and 4 stay inside
-            // the thread and level 2 is one exchange with the partner
-            const int r = tid >> 1, t = tid & 1;
-            const bool ok = r < nr;
-            const int sw = (r & (CPR / 2 - 1)) << 1;
-            int pg = -1;
-            unsigned long long key = ~0ull;
-            float s4[2] = {0.0f, 0.0f};
-            if (ok) {
-                const unsigned char* rowp = stgc + r * ROWB;
-                float s16[8];  // s16 of the owned lanes l < 16, in increasing order
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int l = ((j >> 1) << 2) | (t << 1) | (j & 1);  // 4(j/2) + 2t + (j mod 2)
-                    const int e0 = 4 * l, e1 = 4 * (l + 16);
-                    const int c0 = e0 / EPC, c1 = e1 / EPC;  // pieces holding the two groups
-                    float x0[EPC], x1[EPC];
-                    load_chunk<T>(rowp + 16 * (c0 ^ sw), x0);
-                    load_chunk<T>(rowp + 16 * (c1 ^ sw), x1);
-                    const int o0 = e0 % EPC, o1 = e1 % EPC;
-                    // the partials of lanes l and l + 16 (elements e0 + i and
-                    // e1 + i = e0 + 64 + i) as the two halves of a packed pair
-                    float2 ab = make_float2(0.0f, 0.0f);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        ab = __ffma2_rn(s_qp[e0 + i], make_float2(x0[o0 + i], x1[o1 + i]), ab);
-                    s16[j] = __fadd_rn(ab.x, ab.y);
-                }
-                // level 8: l + 8 is owned entry j + 4; level 4: l + 4 is entry j + 2
-#pragma unroll
-                for (int j = 0; j < 4; ++j) s16[j] = __fadd_rn(s16[j], s16[j + 4]);
-                s4[0] = __fadd_rn(s16[0], s16[2]);  // lane 2t
-                s4[1] = __fadd_rn(s16[1], s16[3]);  // lane 2t + 1
-            }
-            {
-                const float p0 = __shfl_xor_sync(0xffffffffu, s4[0], 1);
-                const float p1 = __shfl_xor_sync(0xffffffffu, s4[1], 1);
-                // level 2: lane 0 + lane 2, lane 1 + lane 3; level 1: their sum
-                const float a0 = t ? p0 : s4[0], a2 = t ? s4[0] : p0;
-                const float a1 = t ? p1 : s4[1], a3 = t ? s4[1] : p1;
-                const float sc = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
+            if (16 * warp < nr) {  // warp-uniform: warp w holds rows 16w .. 16w + 15
+                // two threads per row: thread t of the pair owns the virtual lanes l with
+                // bit 1 of l equal to t, so the tree's levels 16, 8 and 4 stay inside
+                // the thread and level 2 is one exchange with the partner
+                const int r = tid >> 1, t = tid & 1;
+                const bool ok = r < nr;
+                const int sw = (r & (CPR / 2 - 1)) << 1;
+                int pg = -1;
+                unsigned long long key = ~0ull;
+                float s4[2] = {0.0f, 0.0f};
                 if (ok) {
-                    pg = sval[rb0 + r] / P;
-                    key = ((unsigned long long)score_key_desc(sc) << 32) | (unsigned)skey[rb0 + r];
-                }
-            }
-            // rows of one page are adjacent in the candidate list: a segmented
-            // minimum over runs of equal pages (rows two lanes apart) leaves each
-            // run's minimum in its last row, which alone updates the table
-#pragma unroll
-            for (int o = 2; o < 32; o <<= 1) {
-                const int opg = __shfl_up_sync(0xffffffffu, pg, o);
-                const unsigned long long okey = __shfl_up_sync(0xffffffffu, key, o);
-                if (lane >= o && opg == pg && okey < key) key = okey;
-            }
-            const int next_pg = __shfl_down_sync(0xffffffffu, pg, 2);
-            bool fresh = false;
-            if (ok && t == 0 && (lane >= 30 || next_pg != pg)) {
-                unsigned h = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
-                for (int probe = 0; probe < hcap; ++probe) {
-                    const int old = atomicCAS(&hpage[h], -1, pg);
-                    if (old == -1 || old == pg) {
-                        fresh = old == -1;
-                        if (FUSED && fresh)  // the page's token count, for the attention tail
-                            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                                             smem_u32(hcnt + h)),
-                                         "l"(v.list_cnt + v.leaf_base(u, 0) + pg)
-                                         : "memory");
-                        atomicMin(&hkey[h], key);
-                        break;
+                    const unsigned char* rowp = stgc + r * ROWB;
+                    float s16[8];  // s16 of the owned lanes l < 16, in increasing order
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int l = ((j >> 1) << 2) | (t << 1) | (j & 1);  // 4(j/2) + 2t + (j mod 2)
+                        const int e0 = 4 * l, e1 = 4 * (l + 16);
+                        const int c0 = e0 / EPC, c1 = e1 / EPC;  // pieces holding the two groups
+                        float x0[EPC], x1[EPC];
+                        load_chunk<T>(rowp + 16 * (c0 ^ sw), x0);
+                        load_chunk<T>(rowp + 16 * (c1 ^ sw), x1);
+                        const int o0 = e0 % EPC, o1 = e1 % EPC;
+                        // the partials of lanes l and l + 16 (elements e0 + i and
+                        // e1 + i = e0 + 64 + i) as the two halves of a packed pair
+                        float2 ab = make_float2(0.0f, 0.0f);
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            ab = __ffma2_rn(s_qp[e0 + i], make_float2(x0[o0 + i], x1[o1 + i]), ab);
+                        s16[j] = __fadd_rn(ab.x, ab.y);
                     }
-                    h = (h + 1) & (unsigned)hmask;
+                    // level 8: l + 8 is owned entry j + 4; level 4: l + 4 is entry j + 2
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) s16[j] = __fadd_rn(s16[j], s16[j + 4]);
+                    s4[0] = __fadd_rn(s16[0], s16[2]);  // lane 2t
+                    s4[1] = __fadd_rn(s16[1], s16[3]);  // lane 2t + 1
                 }
-            }
-            {
-                const unsigned nf = __ballot_sync(0xffffffffu, fresh);
-                if (lane == 0 && nf) atomicAdd(&s_npg, __popc(nf));
+                {
+                    const float p0 = __shfl_xor_sync(0xffffffffu, s4[0], 1);
+                    const float p1 = __shfl_xor_sync(0xffffffffu, s4[1], 1);
+                    // level 2: lane 0 + lane 2, lane 1 + lane 3; level 1: their sum
+                    const float a0 = t ? p0 : s4[0], a2 = t ? s4[0] : p0;
+                    const float a1 = t ? p1 : s4[1], a3 = t ? s4[1] : p1;
+                    const float sc = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
+                    if (ok) {
+                        pg = sval[rb0 + r] / P;
+                        key = ((unsigned long long)score_key_desc(sc) << 32) | (unsigned)skey[rb0 + r];
+                    }
+                }
+                // rows of one page are adjacent in the candidate list: a segmented
+                // minimum over runs of equal pages (rows two lanes apart) leaves each
+                // run's minimum in its last row, which alone updates the table
+    #pragma unroll
+                for (int o = 2; o < 32; o <<= 1) {
+                    const int opg = __shfl_up_sync(0xffffffffu, pg, o);
+                    const unsigned long long okey = __shfl_up_sync(0xffffffffu, key, o);
+                    if (lane >= o && opg == pg && okey < key) key = okey;
+                }
+                const int next_pg = __shfl_down_sync(0xffffffffu, pg, 2);
+                bool fresh = false;
+                if (ok && t == 0 && (lane >= 30 || next_pg != pg)) {
+                    unsigned h = ((unsigned)pg * 2654435761u) & (unsigned)hmask;
+                    for (int probe = 0; probe < hcap; ++probe) {
+                        const int old = atomicCAS(&hpage[h], -1, pg);
+                        if (old == -1 || old == pg) {
+                            fresh = old == -1;
+                            if (FUSED && fresh)  // the page's token count, for the attention tail
+                                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                                 smem_u32(hcnt + h)),
+                                             "l"(v.list_cnt + v.leaf_base(u, 0) + pg)
+                                             : "memory");
+                            atomicMin(&hkey[h], key);
+                            break;
+                        }
+                        h = (h + 1) & (unsigned)hmask;
+                    }
+                }
+                {
+                    const unsigned nf = __ballot_sync(0xffffffffu, fresh);
+                    if (lane == 0 && nf) atomicAdd(&s_npg, __popc(nf));
+                }
             }
             __syncthreads();  // the chunk's rows are read before the next chunk lands there
             issue(ch + 2);
