@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(IndexView v, cons
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
                         const float mn = fmaxf(m[h], s[h]);
-                        const float corr = exp2f(m[h] - mn);
-                        const float p = exp2f(s[h] - mn);
+                        const float corr = exp2_approx(m[h] - mn);
+                        const float p = exp2_approx(s[h] - mn);
                         lsum[h] = lsum[h] * corr + p;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(p, vx[i], acc[h][i] * corr);
@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(IndexView v, cons
         const float mo = __shfl_xor_sync(0xffffffffu, m[h], 16);
         const float lo = __shfl_xor_sync(0xffffffffu, lsum[h], 16);
         const float mn = fmaxf(m[h], mo);
-        const float ca = mn == -INFINITY ? 0.0f : exp2f(m[h] - mn);
-        const float cb = mn == -INFINITY ? 0.0f : exp2f(mo - mn);
+        const float ca = mn == -INFINITY ? 0.0f : exp2_approx(m[h] - mn);
+        const float cb = mn == -INFINITY ? 0.0f : exp2_approx(mo - mn);
         lsum[h] = lsum[h] * ca + lo * cb;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(IndexView v, cons
             for (int w = 0; w < kAttnWarps; ++w) {
                 const float mw = s_part[w][h][kD];
                 if (mw == -INFINITY) continue;
-                const float cf = exp2f(mw - M);
+                const float cf = exp2_approx(mw - M);
                 Lt = fmaf(s_part[w][h][kD + 1], cf, Lt);
                 O = fmaf(s_part[w][h][dcol], cf, O);
             }

@@ -112,6 +112,15 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Act&&>(args)...);
 }
 
+// 2^x by the hardware approximation (ex2.approx: a few ulp; results below the
+// normal range flush to zero). The attention's softmax weights need far less
+// accuracy than the tolerance of its result.
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- status word -----------------------------------------------------------
 __device__ __forceinline__ void set_status(int* status, int code) {
     atomicCAS(status, 0, code);

@@ -241,8 +241,8 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
 #pragma unroll
                 for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 const float mn = fmaxf(m, s);
-                const float corr = exp2f(m - mn);
-                const float p = exp2f(s - mn);
+                const float corr = exp2_approx(m - mn);
+                const float p = exp2_approx(s - mn);
                 lsum = lsum * corr + p;
                 const float2 c2 = make_float2(corr, corr), p2 = make_float2(p, p);
 #pragma unroll
@@ -279,22 +279,32 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
         }
     }
     __syncthreads();
+    // the warps' weights 2^(m_w - M) per head and the head's softmax sum, once: warp hh,
+    // lane w holds warp w's (max, sum) of head hh
+    float* cfs = part + kSelWarps * G * (kD + 2);  // [G][kSelWarps] weights, then [G] sums
+    if (warp < G) {
+        const int hh = warp;
+        const float mw = lane < kSelWarps ? part[(lane * G + hh) * (kD + 2) + kD] : -INFINITY;
+        float M = mw;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float cf = (M == -INFINITY || mw == -INFINITY) ? 0.0f : exp2_approx(mw - M);
+        float Lt = lane < kSelWarps ? part[(lane * G + hh) * (kD + 2) + kD + 1] * cf : 0.0f;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
+        if (lane < kSelWarps) cfs[hh * kSelWarps + lane] = cf;
+        if (lane == 0) cfs[G * kSelWarps + hh] = *s_fail ? 0.0f : Lt;
+    }
+    __syncthreads();
     T* ou = out + (long long)u * G * kD;
     for (int e = tid; e < G * kD; e += kSelThreads) {
         const int hh = e / kD, dcol = e % kD;
-        float M = -INFINITY;
+        const float Lt = cfs[G * kSelWarps + hh];
+        float O = 0.0f;
+        if (Lt > 0.0f) {
 #pragma unroll
-        for (int w = 0; w < kSelWarps; ++w) M = fmaxf(M, part[(w * G + hh) * (kD + 2) + kD]);
-        float Lt = 0.0f, O = 0.0f;
-        if (M != -INFINITY && !*s_fail) {
-#pragma unroll
-            for (int w = 0; w < kSelWarps; ++w) {
-                const float* pw = part + (w * G + hh) * (kD + 2);
-                if (pw[kD] == -INFINITY) continue;
-                const float cf = exp2f(pw[kD] - M);
-                Lt = fmaf(pw[kD + 1], cf, Lt);
-                O = fmaf(pw[dcol], cf, O);
-            }
+            for (int w = 0; w < kSelWarps; ++w)
+                O = fmaf(part[(w * G + hh) * (kD + 2) + dcol], cfs[hh * kSelWarps + w], O);
         }
         ou[e] = from_f<T>(Lt > 0.0f ? O / Lt : 0.0f);
     }

@@ -284,8 +284,8 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
 #pragma unroll
                 for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 const float mn = fmaxf(m, s);
-                const float corr = exp2f(m - mn);
-                const float p = exp2f(s - mn);
+                const float corr = exp2_approx(m - mn);
+                const float p = exp2_approx(s - mn);
                 lsum = lsum * corr + p;
                 const float2 c2 = make_float2(corr, corr), p2 = make_float2(p, p);
 #pragma unroll
@@ -330,7 +330,7 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
             for (int w = 0; w < kCW; ++w) {
                 const float* pw = part + (w * G + hh) * (kD + 2);
                 if (pw[kD] == -INFINITY) continue;
-                const float cf = exp2f(pw[kD] - M);
+                const float cf = exp2_approx(pw[kD] - M);
                 Lt = fmaf(pw[kD + 1], cf, Lt);
                 O = fmaf(pw[dcol], cf, O);
             }
@@ -1081,7 +1081,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                         const float* cp = hub_part + rr * PW;
                         const float mr = cp[hh * (kD + 2) + kD];
                         if (mr == -INFINITY) continue;
-                        const float cf = exp2f(mr - M);
+                        const float cf = exp2_approx(mr - M);
                         Lt = fmaf(cp[hh * (kD + 2) + kD + 1], cf, Lt);
                         O = fmaf(cp[hh * (kD + 2) + dcol], cf, O);
                     }
