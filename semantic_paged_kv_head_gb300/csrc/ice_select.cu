@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     const int u = blockIdx.x / head_div, row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = v.L, P = v.P;
+    const int pshift = (P & (P - 1)) == 0 ? __ffs(P) - 1 : -1;  // page of a slot by a shift
     const long long C = v.C;
     const int Cp = align16((int)C);
     const SelSmem lay = sel_layout(C, L, n_cand, sort_cap, hcap, n_sel, 0);
@@ -606,8 +607,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         const unsigned* p32 = reinterpret_cast<const unsigned*>(prio + l * Cp);
         const uint4* lrec = recs + v.leaf_base(u, l);
         const int nw = (N[l] + 3) >> 2;
+        // a word with no priority <= ps holds nothing to take or mark: for ps < 128 the
+        // test is the borrow of a bytewise subtraction of ps + 1 (a byte below ps + 1
+        // borrows into its top bit, which its own value does not set)
+        const unsigned lim = 0x01010101u * (unsigned)(ps + 1);
         for (int w4 = tid; w4 < nw; w4 += kSelThreads) {
             const unsigned word = p32[w4];
+            if (ps < 128 && ((word - lim) & ~word & 0x80808080u) == 0u) continue;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int i = 4 * w4 + b;
@@ -761,7 +767,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                         keep = true;
                     } else {
                         loc = v.slot_loc1[v.loc1_base(u) + (long long)id * P + slot];
-                        const int pg = loc >= 0 ? loc / P : 0;
+                        const int pg = loc >= 0 ? (pshift >= 0 ? loc >> pshift : loc / P) : 0;
                         keep = tok >= 0 && loc >= 0 && pg < C && !((bm0[pg >> 5] >> (pg & 31)) & 1u);
                     }
                 }
@@ -868,7 +874,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                     const float a1 = t ? p1 : s4[1], a3 = t ? s4[1] : p1;
                     const float sc = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
                     if (ok) {
-                        pg = sval[rb0 + r] / P;
+                        pg = pshift >= 0 ? sval[rb0 + r] >> pshift : sval[rb0 + r] / P;
                         key = ((unsigned long long)score_key_desc(sc) << 32) | (unsigned)skey[rb0 + r];
                     }
                 }
