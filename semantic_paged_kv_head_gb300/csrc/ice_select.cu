@@ -101,8 +101,12 @@ __host__ __device__ inline SelSmem sel_layout(long long C, int L, int n_cand, in
 // pages (the fused tail). Pages are staged in rounds that fit the staging
 // region: lanes of warp 0 issue one bulk copy per page for K and one for V onto
 // one mbarrier; then every warp takes tokens w, w + 16, ... of the round. Lane
-// (h, g) holds query head h on dimensions [g*DPL, (g+1)*DPL), DPL = 4G; a token
-// costs one warp instruction per step and log2(32/G) shuffles per head.
+// l holds dimensions 4l..4l+3 of every head: a token's row is read once per
+// warp. The heads' partial scores are summed across the lanes by halving: at
+// each of the first log2 G exchange levels a lane keeps half of the heads it
+// holds and sends the other half, so that after the last level lane l holds
+// the score of head (l >> (5 - log2 G)). That lane keeps the head's softmax
+// state, and every lane takes the G (correction, weight) pairs by shuffles.
 template <typename T, int G>
 __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T* __restrict__ q,
                                               const float* s_q, const int* hpage, const int* hcnt,
@@ -110,12 +114,12 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
                                               int* s_ntok, unsigned char* stage,
                                               int stage_bytes, unsigned bar, int* s_fail,
                                               T* __restrict__ out) {
-    constexpr int LPH = 32 / G;     // lanes per head
-    constexpr int DPL = kD / LPH;   // dimensions per lane
+    constexpr int LG = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;  // log2 G
+    constexpr int HS = 5 - LG;  // lane l holds the score of head l >> HS
     constexpr int ROWB = kD * (int)sizeof(T);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = v.P;
-    const int h = lane / LPH, g = lane % LPH;
+    const int hl = lane >> HS;
     // token offsets of the selected pages (warp 0), counts read in parallel
     if (warp == 0) {
         int carry = 0;
@@ -154,20 +158,19 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
             *s_ntok = carry;
         }
     }
-    float qa[DPL];
+    float qa[G][4];
     {
         const float sc = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
-        if (s_q != nullptr) {  // the query rows kept in shared memory since the start
 #pragma unroll
-            for (int k = 0; k < DPL; ++k) qa[k] = s_q[h * kD + g * DPL + k] * sc;
-        } else {
-            const T* qh = q + ((long long)u * G + h) * kD + g * DPL;
+        for (int hh = 0; hh < G; ++hh) {
+            if (s_q != nullptr) {  // the query rows kept in shared memory since the start
 #pragma unroll
-            for (int k = 0; k < DPL; k += 4) {
+                for (int k = 0; k < 4; ++k) qa[hh][k] = s_q[hh * kD + 4 * lane + k] * sc;
+            } else {
                 float x[4];
-                load4(qh + k, x);
+                load4(q + ((long long)u * G + hh) * kD + 4 * lane, x);
 #pragma unroll
-                for (int z = 0; z < 4; ++z) qa[k + z] = x[z] * sc;
+                for (int k = 0; k < 4; ++k) qa[hh][k] = x[k] * sc;
             }
         }
     }
@@ -175,9 +178,11 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
     const int rows_cap = stage_bytes / (2 * ROWB);
     const T* sk = reinterpret_cast<const T*>(stage);
     const T* sv = reinterpret_cast<const T*>(stage + (size_t)rows_cap * ROWB);
-    float m = -INFINITY, lsum = 0.0f, acc[DPL];
+    float m = -INFINITY, lsum = 0.0f, acc[G][4];  // m, lsum: head hl
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[k] = 0.0f;
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[hh][k] = 0.0f;
     int p0 = 0, round = 0;
     while (p0 < npg) {  // every thread computes the same rounds
         int p1 = p0 + 1;
@@ -224,40 +229,50 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
         }
         if (ok) {
             for (int j = warp; j < nrow; j += kSelWarps) {  // warp-uniform
-                float kx[DPL];
+                float kx[4];
+                load4(sk + (size_t)j * kD + 4 * lane, kx);
+                float sv4[G];  // this lane's part of every head's score
 #pragma unroll
-                for (int k = 0; k < DPL; k += 4) {
-                    float x[4];
-                    load4(sk + (size_t)j * kD + g * DPL + k, x);
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) kx[k + z] = x[z];
+                for (int hh = 0; hh < G; ++hh) {
+                    float2 s2 = __fmul2_rn(make_float2(qa[hh][0], qa[hh][1]), make_float2(kx[0], kx[1]));
+                    s2 = __ffma2_rn(make_float2(qa[hh][2], qa[hh][3]), make_float2(kx[2], kx[3]), s2);
+                    sv4[hh] = s2.x + s2.y;
                 }
-                // even and odd dimensions in the two halves of packed fp32 pairs
-                float2 s2 = make_float2(0.0f, 0.0f);
+                // halving exchanges: lanes with bit b set keep the upper half of their heads
 #pragma unroll
-                for (int k = 0; k < DPL; k += 2)
-                    s2 = __ffma2_rn(make_float2(qa[k], qa[k + 1]), make_float2(kx[k], kx[k + 1]), s2);
-                float s = s2.x + s2.y;
+                for (int lv = 0; lv < LG; ++lv) {
+                    const int b = 4 - lv, half = G >> (lv + 1);
+                    const bool up = (lane >> b) & 1;
 #pragma unroll
-                for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                const float mn = fmaxf(m, s);
-                const float corr = exp2_approx(m - mn);
-                const float p = exp2_approx(s - mn);
-                lsum = lsum * corr + p;
-                const float2 c2 = make_float2(corr, corr), p2 = make_float2(p, p);
-#pragma unroll
-                for (int k = 0; k < DPL; k += 4) {
-                    float x[4];
-                    load4(sv + (size_t)j * kD + g * DPL + k, x);
-#pragma unroll
-                    for (int z = 0; z < 4; z += 2) {
-                        const float2 a = __ffma2_rn(p2, make_float2(x[z], x[z + 1]),
-                                                    __fmul2_rn(make_float2(acc[k + z], acc[k + z + 1]), c2));
-                        acc[k + z] = a.x;
-                        acc[k + z + 1] = a.y;
+                    for (int k = 0; k < half; ++k) {
+                        const float keep = up ? sv4[k + half] : sv4[k];
+                        const float send = up ? sv4[k] : sv4[k + half];
+                        sv4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << b);
                     }
                 }
+                float sc = sv4[0];
+#pragma unroll
+                for (int b = HS - 1; b >= 0; --b) sc += __shfl_xor_sync(0xffffffffu, sc, 1 << b);
+                const float mn = fmaxf(m, sc);
+                const float corr = exp2_approx(m - mn);
+                const float p = exp2_approx(sc - mn);
+                lsum = lsum * corr + p;
                 m = mn;
+                float vx[4];
+                load4(sv + (size_t)j * kD + 4 * lane, vx);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float ch = __shfl_sync(0xffffffffu, corr, hh << HS);
+                    const float ph = __shfl_sync(0xffffffffu, p, hh << HS);
+                    const float2 c2 = make_float2(ch, ch), p2 = make_float2(ph, ph);
+#pragma unroll
+                    for (int k = 0; k < 4; k += 2) {
+                        const float2 a2 = __ffma2_rn(p2, make_float2(vx[k], vx[k + 1]),
+                                                     __fmul2_rn(make_float2(acc[hh][k], acc[hh][k + 1]), c2));
+                        acc[hh][k] = a2.x;
+                        acc[hh][k + 1] = a2.y;
+                    }
+                }
             }
         }
         __syncthreads();  // the round's rows are consumed before the next copies land
@@ -270,10 +285,14 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
     // partials into the (now free) staging region: [warp][head][kD + 2]
     float* part = reinterpret_cast<float*>(stage);
     {
-        float* pw = part + (warp * G + h) * (kD + 2);
 #pragma unroll
-        for (int k = 0; k < DPL; ++k) pw[g * DPL + k] = acc[k];
-        if (g == 0) {
+        for (int hh = 0; hh < G; ++hh) {
+            float* pw = part + (warp * G + hh) * (kD + 2) + 4 * lane;  // rows of kD + 2: 8-byte aligned
+#pragma unroll
+            for (int k = 0; k < 4; ++k) pw[k] = acc[hh][k];
+        }
+        if ((lane & ((1 << HS) - 1)) == 0) {
+            float* pw = part + (warp * G + hl) * (kD + 2);
             pw[kD] = m;
             pw[kD + 1] = lsum;
         }
