@@ -182,13 +182,13 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
                                                int r, int K, int* s_toff, unsigned char* stage,
                                                int stage_bytes, unsigned bar, int* s_fail,
                                                float* dst) {
-    constexpr int LPH = 32 / G;
-    constexpr int DPL = kD / LPH;
+    constexpr int LG = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;  // log2 G
+    constexpr int HS = 5 - LG;  // lane l holds the score of head l >> HS
     constexpr int ROWB = kD * (int)sizeof(T);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = v.P;
     const long long C = v.C;
-    const int h = lane / LPH, g = lane % LPH;
+    const int hl = lane >> HS;
     const int npg = taken > r ? (taken - r + K - 1) / K : 0;
     if (warp == 0) {
         int carry = 0;
@@ -211,19 +211,23 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
         }
         if (lane == 0) s_toff[npg] = carry;
     }
-    float qa[DPL];
+    float qa[G][4];  // dimensions 4 lane .. 4 lane + 3 of every head
     {
         const float sc = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 #pragma unroll
-        for (int k = 0; k < DPL; ++k) qa[k] = s_q[h * kD + g * DPL + k] * sc;
+        for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) qa[hh][k] = s_q[hh * kD + 4 * lane + k] * sc;
     }
     __syncthreads();
     const int rows_cap = stage_bytes / (2 * ROWB);
     const T* sk = reinterpret_cast<const T*>(stage);
     const T* sv = reinterpret_cast<const T*>(stage + (size_t)rows_cap * ROWB);
-    float m = -INFINITY, lsum = 0.0f, acc[DPL];
+    float m = -INFINITY, lsum = 0.0f, acc[G][4];  // m, lsum: head hl
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[k] = 0.0f;
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[hh][k] = 0.0f;
     int p0 = 0, round = 0;
     while (p0 < npg) {  // block-uniform rounds
         int p1 = p0 + 1;
@@ -268,39 +272,50 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
         }
         if (ok) {
             for (int j = warp; j < nrow; j += kCW) {  // warp-uniform
-                float kx[DPL];
+                float kx[4];
+                load4(sk + (size_t)j * kD + 4 * lane, kx);
+                float sv4[G];  // this lane's part of every head's score
 #pragma unroll
-                for (int k = 0; k < DPL; k += 4) {
-                    float x[4];
-                    load4(sk + (size_t)j * kD + g * DPL + k, x);
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) kx[k + z] = x[z];
+                for (int hh = 0; hh < G; ++hh) {
+                    float2 s2 = __fmul2_rn(make_float2(qa[hh][0], qa[hh][1]), make_float2(kx[0], kx[1]));
+                    s2 = __ffma2_rn(make_float2(qa[hh][2], qa[hh][3]), make_float2(kx[2], kx[3]), s2);
+                    sv4[hh] = s2.x + s2.y;
                 }
-                float2 s2 = make_float2(0.0f, 0.0f);
+                // halving exchanges: lanes with bit b set keep the upper half of their heads
 #pragma unroll
-                for (int k = 0; k < DPL; k += 2)
-                    s2 = __ffma2_rn(make_float2(qa[k], qa[k + 1]), make_float2(kx[k], kx[k + 1]), s2);
-                float s = s2.x + s2.y;
+                for (int lv = 0; lv < LG; ++lv) {
+                    const int b = 4 - lv, half = G >> (lv + 1);
+                    const bool up = (lane >> b) & 1;
 #pragma unroll
-                for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                const float mn = fmaxf(m, s);
-                const float corr = exp2_approx(m - mn);
-                const float p = exp2_approx(s - mn);
-                lsum = lsum * corr + p;
-                const float2 c2 = make_float2(corr, corr), p2 = make_float2(p, p);
-#pragma unroll
-                for (int k = 0; k < DPL; k += 4) {
-                    float x[4];
-                    load4(sv + (size_t)j * kD + g * DPL + k, x);
-#pragma unroll
-                    for (int z = 0; z < 4; z += 2) {
-                        const float2 a = __ffma2_rn(p2, make_float2(x[z], x[z + 1]),
-                                                    __fmul2_rn(make_float2(acc[k + z], acc[k + z + 1]), c2));
-                        acc[k + z] = a.x;
-                        acc[k + z + 1] = a.y;
+                    for (int k = 0; k < half; ++k) {
+                        const float keep = up ? sv4[k + half] : sv4[k];
+                        const float send = up ? sv4[k] : sv4[k + half];
+                        sv4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << b);
                     }
                 }
+                float sc = sv4[0];
+#pragma unroll
+                for (int b = HS - 1; b >= 0; --b) sc += __shfl_xor_sync(0xffffffffu, sc, 1 << b);
+                const float mn = fmaxf(m, sc);
+                const float corr = exp2_approx(m - mn);
+                const float p = exp2_approx(sc - mn);
+                lsum = lsum * corr + p;
                 m = mn;
+                float vx[4];
+                load4(sv + (size_t)j * kD + 4 * lane, vx);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float ch = __shfl_sync(0xffffffffu, corr, hh << HS);
+                    const float ph = __shfl_sync(0xffffffffu, p, hh << HS);
+                    const float2 c2 = make_float2(ch, ch), p2 = make_float2(ph, ph);
+#pragma unroll
+                    for (int k = 0; k < 4; k += 2) {
+                        const float2 a2 = __ffma2_rn(p2, make_float2(vx[k], vx[k + 1]),
+                                                     __fmul2_rn(make_float2(acc[hh][k], acc[hh][k + 1]), c2));
+                        acc[hh][k] = a2.x;
+                        acc[hh][k + 1] = a2.y;
+                    }
+                }
             }
         }
         __syncthreads();  // the round's rows are consumed before the next copies land
@@ -310,10 +325,14 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
     }
     float* part = reinterpret_cast<float*>(stage);  // [warp][head][kD + 2]
     {
-        float* pw = part + (warp * G + h) * (kD + 2);
 #pragma unroll
-        for (int k = 0; k < DPL; ++k) pw[g * DPL + k] = acc[k];
-        if (g == 0) {
+        for (int hh = 0; hh < G; ++hh) {
+            float* pw = part + (warp * G + hh) * (kD + 2) + 4 * lane;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) pw[k] = acc[hh][k];
+        }
+        if ((lane & ((1 << HS) - 1)) == 0) {
+            float* pw = part + (warp * G + hl) * (kD + 2);
             pw[kD] = m;
             pw[kD + 1] = lsum;
         }
