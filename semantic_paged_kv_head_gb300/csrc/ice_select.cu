@@ -827,18 +827,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
         const int nchunk = (ncand + half - 1) / half;
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = hcap - 1;
+        // thread tid copies piece c = tid mod CPR of rows tid / CPR, + RSTEP, ...: the
+        // swizzled position of the piece is the same in all of them (the swizzle
+        // repeats every CPR / 2 rows), so only the row's source address changes per copy
+        constexpr int RSTEP = kSelThreads / CPR;
+        static_assert(RSTEP % (CPR / 2) == 0, "the swizzle must repeat every RSTEP rows");
+        const int cpc = tid % CPR, r_first = tid / CPR;
+        const int cpos = cpc ^ ((r_first & (CPR / 2 - 1)) << 1);
         auto issue = [&](int ch) {  // chunk ch into half ch & 1; every thread commits a group
             if (ch < nchunk) {
                 const int rb = ch * half, nr = min(half, ncand - rb);
-                unsigned char* buf = stg + (ch & 1) * half * ROWB;
-                for (int k = tid; k < nr * CPR; k += kSelThreads) {
-                    const int r = k / CPR, c = k % CPR;
-                    const int pos = c ^ ((r & (CPR / 2 - 1)) << 1);
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                                     smem_u32(buf + r * ROWB + 16 * pos)),
-                                 "l"(pk + (long long)sval[rb + r] * ROWB + 16 * c)
+                unsigned dst = smem_u32(stg + (ch & 1) * half * ROWB + r_first * ROWB + 16 * cpos);
+                const char* src = pk + 16 * cpc;
+                for (int r = r_first; r < nr; r += RSTEP, dst += RSTEP * ROWB)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                                 "l"(src + (long long)sval[rb + r] * ROWB)
                                  : "memory");
-                }
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
