@@ -819,16 +819,22 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         const int nchunk = (ncand + half - 1) / half;
         const char* pk = reinterpret_cast<const char*>(v.page_k) + (long long)u * C * P * ROWB;
         const int hmask = dm.hcap_l - 1;
+        // thread tid copies piece c = tid mod CPR of rows tid / CPR, + RSTEP, ...; when
+        // the swizzle repeats within RSTEP rows the piece's position stays fixed
+        constexpr int RSTEP = kCT / CPR;
+        constexpr bool kFixedPos = RSTEP % (CPR / 2) == 0;
+        const int cpc = tid % CPR, r_first = tid / CPR;
         auto issue = [&](int ch) {
             if (ch < nchunk) {
                 const int rb = ch * half, nr = min(half, ncand - rb);
-                unsigned char* buf = stg + (ch & 1) * half * ROWB;
-                for (int k = tid; k < nr * CPR; k += kCT) {
-                    const int rr = k / CPR, c = k % CPR;
-                    const int pos = c ^ ((rr & (CPR / 2 - 1)) << 1);
+                const unsigned buf = smem_u32(stg + (ch & 1) * half * ROWB);
+                const char* src = pk + 16 * cpc;
+                for (int rr = r_first; rr < nr; rr += RSTEP) {
+                    const int pos = kFixedPos ? (cpc ^ ((r_first & (CPR / 2 - 1)) << 1))
+                                              : (cpc ^ ((rr & (CPR / 2 - 1)) << 1));
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                                     smem_u32(buf + rr * ROWB + 16 * pos)),
-                                 "l"(pk + (long long)sval[rb + rr] * ROWB + 16 * c)
+                                     buf + rr * ROWB + 16 * pos),
+                                 "l"(src + (long long)sval[rb + rr] * ROWB)
                                  : "memory");
                 }
             }
