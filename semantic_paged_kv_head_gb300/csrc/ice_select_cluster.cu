@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     const int u = blockIdx.x / K;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = v.L, P = v.P;
+    const int pshift = (P & (P - 1)) == 0 ? __ffs(P) - 1 : -1;  // page of a slot by a shift
     const long long C = v.C;
     const int Kc = K / L, l = r / Kc, rc = r % Kc;
     const int n_cand = dm.n_cand;
@@ -628,8 +629,12 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         const int ps = s_pstar;
         const unsigned* p32 = reinterpret_cast<const unsigned*>(prio);
         const int nw = (nloc + 3) >> 2;
+        // a word with no priority <= ps holds nothing to take or mark: for ps < 128 the
+        // test is the borrow of a bytewise subtraction of ps + 1
+        const unsigned lim = 0x01010101u * (unsigned)(ps + 1);
         for (int w4 = tid; w4 < nw; w4 += kCT) {
             const unsigned word = p32[w4];
+            if (ps < 128 && ((word - lim) & ~word & 0x80808080u) == 0u) continue;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int i = 4 * w4 + b;
@@ -780,7 +785,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 } else {
                     // a composite-1 token whose page composite 0 took whole is a duplicate
                     loc = v.slot_loc1[v.loc1_base(u) + (long long)id * P + slot];
-                    const int pg = loc >= 0 ? loc / P : 0;
+                    const int pg = loc >= 0 ? (pshift >= 0 ? loc >> pshift : loc / P) : 0;
                     keep = tok >= 0 && loc >= 0 && pg < C && !((bm0[pg >> 5] >> (pg & 31)) & 1u);
                 }
             }
@@ -883,7 +888,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 const float a1 = t ? p1 : s4[1], a3 = t ? s4[1] : p1;
                 const float sc = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
                 if (ok) {
-                    pg = sval[rb0 + rr] / P;
+                    pg = pshift >= 0 ? sval[rb0 + rr] >> pshift : sval[rb0 + rr] / P;
                     key = ((unsigned long long)score_key_desc(sc) << 32) | (unsigned)skey[rb0 + rr];
                 }
             }
