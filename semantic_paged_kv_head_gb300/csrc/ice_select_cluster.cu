@@ -679,32 +679,41 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
                 const int y = __shfl_up_sync(0xffffffffu, inc, o);
                 if (lane >= o) inc += y;
             }
-            int acc = run + inc - tot, mine = 0;
-            unsigned take = 0u;
-            if (acc + tot <= need) {
-                take = bits;
-                mine = __popc(bits);
-            } else {
-                for (unsigned bb = bits; bb && acc < need; bb &= bb - 1u) {
-                    const int bit = __ffs(bb) - 1;
-                    take |= 1u << bit;
-                    acc += (int)((byte_word(cw, bit >> 2) >> (8 * (bit & 3))) & 0xFFu);
-                    ++mine;
-                }
-            }
+            const int acc = run + inc - tot;
+            const unsigned bt = boundary_take(bits, cw, acc, tot, need, lane);
+            const unsigned take = acc + tot <= need ? bits : (acc < need ? bt : 0u);
+            const int mine = __popc(take);
             int tinc = mine;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, tinc, o);
                 if (lane >= o) tinc += y;
             }
-            int slot = nbelow + ntaken + tinc - mine;
-            for (unsigned bb = take; bb; bb &= bb - 1u, ++slot)
-                if (slot < n_cand) {
-                    const int i = wi * 32 + __ffs(bb) - 1;
-                    chosen[slot] = i;
-                    cmeta[slot] = lid[i];
+            const int sbase = nbelow + ntaken + tinc - mine;
+            // one pass per word with ties taken (each lane one bit), or one pass per tie of
+            // the busiest lane, whichever is fewer
+            const unsigned nz = __ballot_sync(0xffffffffu, take != 0u);
+            if (__popc(nz) < __reduce_max_sync(0xffffffffu, (unsigned)mine)) {  // warp-uniform
+                for (unsigned z = nz; z; z &= z - 1u) {
+                    const int w = __ffs(z) - 1;
+                    const unsigned t = __shfl_sync(0xffffffffu, take, w);
+                    const int sb = __shfl_sync(0xffffffffu, sbase, w);
+                    const int slot = sb + __popc(t & ((1u << lane) - 1u));
+                    if (((t >> lane) & 1u) && slot < n_cand) {
+                        const int i = (w0 + w) * 32 + lane;
+                        chosen[slot] = i;
+                        cmeta[slot] = lid[i];
+                    }
                 }
+            } else {
+                int slot = sbase;
+                for (unsigned bb = take; bb; bb &= bb - 1u, ++slot)
+                    if (slot < n_cand) {
+                        const int i = wi * 32 + __ffs(bb) - 1;
+                        chosen[slot] = i;
+                        cmeta[slot] = lid[i];
+                    }
+            }
             ntaken += __shfl_sync(0xffffffffu, tinc, 31);
             run += __shfl_sync(0xffffffffu, inc, 31);
         }

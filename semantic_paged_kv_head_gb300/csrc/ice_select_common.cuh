@@ -113,6 +113,34 @@ __device__ __forceinline__ int leaf_priority(unsigned x, unsigned y, int t, cons
     return (int)(__half_as_ushort(b) & 0x3FFu);
 }
 
+// The ties taken from the boundary word of a tie walk: the one lane whose word
+// holds the tokens where the running count reaches `need` (acc < need < acc +
+// tot). Lane j looks at bit j of that word, a warp prefix sum of the tie counts
+// gives the tokens taken before it, and the tie is taken while that count is
+// below the need, as a walk over the word's bits in order would. Returns the
+// taken bits in every lane, 0 when no lane's word holds the boundary. All lanes
+// of the warp call it.
+__device__ __forceinline__ unsigned boundary_take(unsigned bits, const unsigned (&cw)[8], int acc,
+                                                  int tot, int need, int lane) {
+    const unsigned bl = __ballot_sync(0xffffffffu, bits != 0u && acc < need && acc + tot > need);
+    if (bl == 0u) return 0u;  // warp-uniform
+    const int b = __ffs(bl) - 1;
+    const unsigned wb = __shfl_sync(0xffffffffu, bits, b);
+    const int accb = __shfl_sync(0xffffffffu, acc, b);
+    unsigned cwb[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) cwb[q] = __shfl_sync(0xffffffffu, cw[q], b);
+    const bool has = (wb >> lane) & 1u;
+    const int c = has ? (int)((byte_word(cwb, lane >> 2) >> (8 * (lane & 3))) & 0xFFu) : 0;
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    return __ballot_sync(0xffffffffu, has && accb + inc - c < need);
+}
+
 // Byte store to shared memory through an explicit st.shared.u8. With a plain
 // C++ byte store of the fp16-derived priority, the priority table did not
 // receive the values in builds of this kernel for sm_103a with nvcc 13.0 (the
