@@ -833,10 +833,7 @@ def run_ice(args):
             "reuse": lambda: reuse_run(ice, synth, ix, w, centers, flush, timed, args),
             "recall": lambda: recall_run(ice, w, keys, values, q, flush, timed, args),
         }
-        chosen = [e for e in args.extras.split(",") if e]
-        for name in chosen:
-            if name not in runs:
-                raise SystemExit(f"unknown extra {name!r}; choose from {','.join(EXTRAS)}")
+        chosen = [e for e in args.extras.split(",") if e]  # names checked when parsing
         for name in EXTRAS:
             if name in chosen:
                 # an NVTX range per extra, so that a profiler can take the launches of one
@@ -892,6 +889,9 @@ def main():
     ap.add_argument("--extras", default=",".join(EXTRAS),
                     help="comma list of the extras to run (profiling one of them): " + ",".join(EXTRAS))
     args = ap.parse_args()
+    unknown = [e for e in args.extras.split(",") if e and e not in EXTRAS]
+    if unknown:
+        ap.error(f"unknown extra(s) {','.join(unknown)}; choose from {','.join(EXTRAS)}")
     if args.impl == "reference":
         return run_reference(args)
     return run_ice(args)

@@ -78,3 +78,13 @@ def test_binding_refuses_unpinned_cpu_memory():
         ice._dev_ptr(t, torch.bfloat16, "keys", host_ok=False)
     with pytest.raises(ValueError):
         ice._dev_ptr([1, 2, 3], None, "q")
+
+
+def test_unknown_extra_is_refused_before_any_work():
+    """A misspelt --extras name stops the benchmark while parsing its arguments (exit 2,
+    the names it accepts in the message), before any device work."""
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--extras", "host_kv,recal"],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2
+    assert "recal" in r.stderr and "per_layer_serial" in r.stderr
