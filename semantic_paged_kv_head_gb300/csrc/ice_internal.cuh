@@ -350,6 +350,9 @@ cudaError_t select_prepare();
 // per-device setup, and the launch (*launched false if clusters of that size
 // cannot be resident; nothing is launched then).
 int select_cluster_auto(int U, int L);
+cudaError_t launch_select_heads_cluster(const IndexView& v, const void* q, int n_sel, int n_cand,
+                                        int32_t* page_ids, int32_t* n_pages, cudaStream_t s,
+                                        bool* launched);
 int select_cluster_bytes(const IndexView& v, int K, int n_sel, int n_cand, bool fused);
 cudaError_t select_cluster_prepare();
 cudaError_t launch_select_cluster(const IndexView& v, int K, const void* q, int n_sel, int n_cand,

@@ -1135,10 +1135,17 @@ cudaError_t launch_select(const IndexView& v, const void* q, int n_sel, int n_ca
                                    knew, vnew, s);
 }
 
-// Per-query-head selection: one block per (unit, query head) selects with that
-// head's query alone (q_sel = q_h), through the single-head instantiation.
+// Per-query-head selection: every (unit, query head) selects with that head's query
+// alone (q_sel = q_h), through the single-head instantiations: a cluster of blocks per
+// row when the rows are few, else one block per row.
 cudaError_t launch_select_heads(const IndexView& v, const void* q, int n_sel, int n_cand,
                                 int32_t* page_ids, int32_t* n_pages, cudaStream_t s) {
+    {  // few rows: a cluster of blocks per (unit, head)
+        bool launched = false;
+        const cudaError_t e = launch_select_heads_cluster(v, q, n_sel, n_cand, page_ids, n_pages, s,
+                                                          &launched);
+        if (e != cudaSuccess || launched) return e;
+    }
     int sort_cap, hcap;
     select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
     const int bytes = select_smem_bytes(v.C, v.L, v.P, n_cand, n_sel, 1, false);

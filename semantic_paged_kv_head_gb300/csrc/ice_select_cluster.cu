@@ -367,7 +367,7 @@ template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, CluDims dm, int smem_total,
     int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
-    int32_t* __restrict__ stats, T* __restrict__ attn_out) {
+    int32_t* __restrict__ stats, T* __restrict__ attn_out, int head_div) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float2 s_qp[kD / 2];  // (q_sel[e], q_sel[e + 64]), e < 64
     __shared__ int s_qcode[kM];
@@ -379,7 +379,8 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     cg::cluster_group cluster = cg::this_cluster();
     const int K = (int)cluster.num_blocks();
     const int r = (int)cluster.block_rank();
-    const int u = blockIdx.x / K;
+    // head_div > 1: per-query-head selection, row = (unit, head) with the unit's tables
+    const int row = blockIdx.x / K, u = row / head_div;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = v.L, P = v.P;
     const int pshift = (P & (P - 1)) == 0 ? __ffs(P) - 1 : -1;  // page of a slot by a shift
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     if (r == 0)
         for (int ll = 0; ll < L; ++ll) Nall += max(0, min(v.n_leaf[v.ul(u, ll)], (int)C));
     float qh[G][4];
-    const T* qu = q + (long long)u * G * kD;
+    const T* qu = q + (long long)row * G * kD;
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) load4(qu + (long long)hh * kD + 4 * lane, qh[hh]);
     float wdir[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1077,17 +1078,17 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     // tables until every block has passed it)
     if (r == 0 && warp == 0) {
         const int taken = s_taken;
-        if (lane < n_sel) page_ids[(long long)u * n_sel + lane] = s_sel[lane];
+        if (lane < n_sel) page_ids[(long long)row * n_sel + lane] = s_sel[lane];
         int tok_sel = lane < taken ? s_scnt[lane] : 0;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) tok_sel += __shfl_xor_sync(0xffffffffu, tok_sel, o);
         if (lane == 0) {
-            n_pages_out[u] = taken;
+            n_pages_out[row] = taken;
             if (stats) {
-                stats[4 * u + 0] = Nall;
-                stats[4 * u + 1] = hubx[3];
-                stats[4 * u + 2] = tok_sel;
-                stats[4 * u + 3] = hubx[4];
+                stats[4 * row + 0] = Nall;
+                stats[4 * row + 1] = hubx[3];
+                stats[4 * row + 2] = tok_sel;
+                stats[4 * row + 3] = hubx[4];
             }
         }
     }
@@ -1104,7 +1105,7 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         clu_arrive();
         clu_wait();
         if (r == 0) {
-            T* ou = attn_out + (long long)u * G * kD;
+            T* ou = attn_out + (long long)row * G * kD;
             for (int e = tid; e < G * kD; e += kCT) {
                 const int hh = e / kD, dcol = e % kD;
                 float M = -INFINITY;
@@ -1175,10 +1176,10 @@ CluPlan clu_plan(const IndexView& v, int K, int n_sel, int n_cand, bool fused, i
 template <typename T, int G, bool F>
 cudaError_t clu_launch(const IndexView& v, const CluPlan& p, const void* q, int n_sel,
                        int32_t* page_ids, int32_t* n_pages, int32_t* stats, void* out,
-                       cudaStream_t s) {
+                       cudaStream_t s, int head_div = 1) {
     auto kern = select_cluster_kernel<T, G, F>;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(v.U * p.K));
+    cfg.gridDim = dim3((unsigned)(v.U * head_div * p.K));
     cfg.blockDim = dim3(kCT);
     cfg.dynamicSmemBytes = (size_t)p.bytes;
     cfg.stream = s;
@@ -1192,7 +1193,7 @@ cudaError_t clu_launch(const IndexView& v, const CluPlan& p, const void* q, int 
     cfg.attrs = at;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, v, (const T*)q, n_sel, p.d, p.bytes, page_ids, n_pages,
-                              stats, (T*)out);
+                              stats, (T*)out, head_div);
 }
 
 template <typename T, int G, bool F>
@@ -1314,6 +1315,28 @@ cudaError_t launch_select_cluster(const IndexView& v, int K, const void* q, int 
     cudaError_t e = clu_dispatch(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out, s, true, &fits);
     if (e != cudaSuccess || !fits) return e;
     e = clu_dispatch(v, p, q, n_sel, n_cand, page_ids, n_pages, stats, out, s, false, &fits);
+    if (e == cudaSuccess) *launched = true;
+    return e;
+}
+
+// Per-query-head selection (one row per (unit, query head), the head's query alone)
+// with a cluster of blocks per row. Sets *launched when it ran; leaves the launch to
+// the one-block kernel when the rows are many or a cluster cannot hold them.
+cudaError_t launch_select_heads_cluster(const IndexView& v, const void* q, int n_sel, int n_cand,
+                                        int32_t* page_ids, int32_t* n_pages, cudaStream_t s,
+                                        bool* launched) {
+    *launched = false;
+    const int rows = v.U * v.G;
+    const int K = v.cluster_k > 0 ? v.cluster_k : select_cluster_auto(rows, v.L);
+    if (K < 2 || select_cluster_bytes(v, K, n_sel, n_cand, false) < 0) return cudaSuccess;
+    const CluPlan p = clu_plan(v, K, n_sel, n_cand, false, clu_target_bytes(rows * K));
+    const bool fits = v.dtype == ICE_BF16 ? clu_fits<__nv_bfloat16, 1, false>(v, p)
+                                          : clu_fits<float, 1, false>(v, p);
+    if (!fits) return cudaSuccess;
+    const cudaError_t e =
+        v.dtype == ICE_BF16
+            ? clu_launch<__nv_bfloat16, 1, false>(v, p, q, n_sel, page_ids, n_pages, nullptr, nullptr, s, v.G)
+            : clu_launch<float, 1, false>(v, p, q, n_sel, page_ids, n_pages, nullptr, nullptr, s, v.G);
     if (e == cudaSuccess) *launched = true;
     return e;
 }
