@@ -95,7 +95,10 @@ __device__ __forceinline__ void cell_widths(int t, __half2 (&w)[4]) {
 
 // L-infinity distance (code units) between the query codes q (biased fp16x2,
 // directions 2k, 2k+1 in word k) and the cell of a leaf: lower corner codes 0-3
-// in x and 4-7 in y (one byte each), prefix length t.
+// in x and 4-7 in y (one byte each), prefix length t. Per direction, with
+// d = q - lo and the cell's width w, the distance to [lo, lo + w] is the larger
+// of lo - q = -d and q - (lo + w) = d - w (one of them is <= 0); every value is
+// an integer of magnitude below 2048, exact in fp16.
 __device__ __forceinline__ int leaf_priority(unsigned x, unsigned y, int t, const __half2 (&q)[4],
                                              const __half2* widths /* [97][4] */) {
     const __half2 lo[4] = {bytes_to_h2(x, 0x4140u), bytes_to_h2(x, 0x4342u),
@@ -104,8 +107,8 @@ __device__ __forceinline__ int leaf_priority(unsigned x, unsigned y, int t, cons
     __half2 m[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const __half2 hi = __hadd2(lo[k], widths[t * 4 + k]);
-        m[k] = __hmax2(__hsub2(lo[k], q[k]), __hsub2(q[k], hi));  // one of them is <= 0
+        const __half2 d = __hsub2(q[k], lo[k]);
+        m[k] = __hmax2(__hneg2(d), __hsub2(d, widths[t * 4 + k]));
     }
     const __half2 r = __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
     const __half d = __hmax(__hmax(__low2half(r), __high2half(r)), __float2half(0.0f));
