@@ -567,7 +567,11 @@ int ice_sparse_attn(ice_index* ix, const void* q, const int32_t* page_ids, const
     ICE_KERNEL_ADDR(page_ids);
     ICE_KERNEL_ADDR(n_pages);
     ICE_KERNEL_ADDR(out);
-    cudaError_t e = launch_attn(ix->v, q, page_ids, n_pages, page_stride, out, (cudaStream_t)stream);
+    // pages in device memory are staged by bulk copies while the units fit one block per
+    // SM; a host pool, and launches of more units, take the plain-load kernel
+    cudaError_t e = ix->p.kv_location == ICE_KV_DEVICE && ix->U <= kAttnStagedMaxUnits
+                        ? launch_attn_staged(ix->v, q, page_ids, n_pages, page_stride, out, (cudaStream_t)stream)
+                        : launch_attn(ix->v, q, page_ids, n_pages, page_stride, out, (cudaStream_t)stream);
     return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
 }
 

@@ -15,6 +15,7 @@ namespace ice {
 constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kTokUnr = 4;  // token pairs requested ahead per warp (8 rows of K and V)
+static_assert(2 * kAttnThreads >= 512, "two list slots per thread cover the longest list");
 
 // 8 consecutive elements as floats.
 template <typename T> struct Row8;
@@ -50,19 +51,31 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(IndexView v, cons
     __shared__ float s_part[kAttnWarps][G][kD + 2];  // per-warp {acc[kD], m, l}
     __shared__ int s_pid[512];
     __shared__ int s_cnt[512];
+    pdl_wait_then_release();
     const int u = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = v.P;
 
     // ---- page list and counts, all pages at once --------------------------------------
+    // the list length, the allocated page count and every slot of the list's row are
+    // read together (page_stride <= 2 * kAttnThreads), then the counts of the pages
     int np = n_pages[u];
+    const int nalloc = v.next_id[v.ul(u, 0)];
+    int pids[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + k * kAttnThreads;
+        pids[k] = i < page_stride ? page_ids[(long long)u * page_stride + i] : -1;
+    }
     if (np < 0 || np > page_stride) {
         if (tid == 0) set_status(v.status, ICE_ERR_BOUNDS);
         np = np < 0 ? 0 : page_stride;
     }
-    const int nalloc = v.next_id[v.ul(u, 0)];
-    for (int i = tid; i < np; i += kAttnThreads) {
-        const int pid = page_ids[(long long)u * page_stride + i];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + k * kAttnThreads;
+        if (i >= np) continue;
+        const int pid = pids[k];
         int c = 0;
         if (pid < 0 || pid >= nalloc || pid >= v.C) {
             set_status(v.status, ICE_ERR_BOUNDS);
@@ -208,13 +221,12 @@ static cudaError_t launch_attn_dt(const IndexView& v, const void* q, const int32
     const T* qq = (const T*)q;
     T* oo = (T*)out;
     switch (v.G) {
-        case 1: attn_kernel<T, 1><<<v.U, kAttnThreads, 0, s>>>(v, qq, page_ids, n_pages, page_stride, oo); break;
-        case 2: attn_kernel<T, 2><<<v.U, kAttnThreads, 0, s>>>(v, qq, page_ids, n_pages, page_stride, oo); break;
-        case 4: attn_kernel<T, 4><<<v.U, kAttnThreads, 0, s>>>(v, qq, page_ids, n_pages, page_stride, oo); break;
-        case 8: attn_kernel<T, 8><<<v.U, kAttnThreads, 0, s>>>(v, qq, page_ids, n_pages, page_stride, oo); break;
+        case 1: return launch_pdl(attn_kernel<T, 1>, dim3(v.U), dim3(kAttnThreads), 0, s, v, qq, page_ids, n_pages, page_stride, oo);
+        case 2: return launch_pdl(attn_kernel<T, 2>, dim3(v.U), dim3(kAttnThreads), 0, s, v, qq, page_ids, n_pages, page_stride, oo);
+        case 4: return launch_pdl(attn_kernel<T, 4>, dim3(v.U), dim3(kAttnThreads), 0, s, v, qq, page_ids, n_pages, page_stride, oo);
+        case 8: return launch_pdl(attn_kernel<T, 8>, dim3(v.U), dim3(kAttnThreads), 0, s, v, qq, page_ids, n_pages, page_stride, oo);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_attn(const IndexView& v, const void* q, const int32_t* page_ids,

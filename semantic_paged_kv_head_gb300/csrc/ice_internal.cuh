@@ -384,7 +384,16 @@ cudaError_t launch_union(int U, int G, int n_sel, const int32_t* head_ids, const
 // selection, and the reuse age); writes reselect[U] and updates codes/age.
 cudaError_t launch_reuse(const IndexView& v, const void* q, int r, unsigned char* codes, int* age,
                          int32_t* reselect, cudaStream_t s);
+// Plain-load attention (any pool; the path for a pool in pinned host memory).
 cudaError_t launch_attn(const IndexView& v, const void* q, const int32_t* page_ids,
                         const int32_t* n_pages, int page_stride, void* out, cudaStream_t s);
+// Attention with the pages staged by bulk copies (a pool in device memory). Up to
+// one block per SM of the 152 it is faster than the plain-load kernel (8 units:
+// 12.3 against 14.3 us per call); with more units the plain kernel, two blocks per
+// SM with loads in flight during the arithmetic, is faster (256 units: 18.4 against
+// 20.5 us).
+constexpr int kAttnStagedMaxUnits = 152;
+cudaError_t launch_attn_staged(const IndexView& v, const void* q, const int32_t* page_ids,
+                               const int32_t* n_pages, int page_stride, void* out, cudaStream_t s);
 
 }  // namespace ice

@@ -282,33 +282,31 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
         p0 = p1;
         ++round;
     }
-    // partials into the (now free) staging region: [warp][head][kD + 2]
+    // partials into the (now free) staging region: rows [warp][head] of PR floats, the
+    // accumulator, then m and the sum. Rows of 16-byte multiples take one 16-byte store per
+    // lane and head, where scalar stores 16 bytes apart would conflict four ways in the banks
+    constexpr int PR = kD + 4;
     float* part = reinterpret_cast<float*>(stage);
     {
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            float* pw = part + (warp * G + hh) * (kD + 2) + 4 * lane;  // rows of kD + 2: 8-byte aligned
-#pragma unroll
-            for (int k = 0; k < 4; ++k) pw[k] = acc[hh][k];
-        }
-        if ((lane & ((1 << HS) - 1)) == 0) {
-            float* pw = part + (warp * G + hl) * (kD + 2);
-            pw[kD] = m;
-            pw[kD + 1] = lsum;
-        }
+        for (int hh = 0; hh < G; ++hh)
+            *reinterpret_cast<float4*>(part + (warp * G + hh) * PR + 4 * lane) =
+                make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+        if ((lane & ((1 << HS) - 1)) == 0)
+            *reinterpret_cast<float2*>(part + (warp * G + hl) * PR + kD) = make_float2(m, lsum);
     }
     __syncthreads();
     // the warps' weights 2^(m_w - M) per head and the head's softmax sum, once: warp hh,
     // lane w holds warp w's (max, sum) of head hh
-    float* cfs = part + kSelWarps * G * (kD + 2);  // [G][kSelWarps] weights, then [G] sums
+    float* cfs = part + kSelWarps * G * PR;  // [G][kSelWarps] weights, then [G] sums
     if (warp < G) {
         const int hh = warp;
-        const float mw = lane < kSelWarps ? part[(lane * G + hh) * (kD + 2) + kD] : -INFINITY;
+        const float mw = lane < kSelWarps ? part[(lane * G + hh) * PR + kD] : -INFINITY;
         float M = mw;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         const float cf = (M == -INFINITY || mw == -INFINITY) ? 0.0f : exp2_approx(mw - M);
-        float Lt = lane < kSelWarps ? part[(lane * G + hh) * (kD + 2) + kD + 1] * cf : 0.0f;
+        float Lt = lane < kSelWarps ? part[(lane * G + hh) * PR + kD + 1] * cf : 0.0f;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) Lt += __shfl_xor_sync(0xffffffffu, Lt, o);
         if (lane < kSelWarps) cfs[hh * kSelWarps + lane] = cf;
@@ -323,7 +321,7 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
         if (Lt > 0.0f) {
 #pragma unroll
             for (int w = 0; w < kSelWarps; ++w)
-                O = fmaf(part[(w * G + hh) * (kD + 2) + dcol], cfs[hh * kSelWarps + w], O);
+                O = fmaf(part[(w * G + hh) * PR + dcol], cfs[hh * kSelWarps + w], O);
         }
         ou[e] = from_f<T>(Lt > 0.0f ? O / Lt : 0.0f);
     }
@@ -1050,6 +1048,81 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
                             smem_total - lay.keys, smem_u32(&s_bar), &s_fail, attn_out);
 }
 
+// Sparse attention over a given page list ("IceCache", Figure 2 step 3), for a
+// page pool in device memory: the fused kernel's attention tail on its own. One
+// 512-thread block per unit stages the pages' K and V rows with one bulk copy
+// per page and row kind, so a round of pages costs one memory latency. A page id
+// that is negative, not allocated or past the list capacity marks the status
+// ICE_ERR_BOUNDS and contributes nothing, as does a list length outside
+// [0, page_stride].
+constexpr int kAttnStagedSmem = 104 * 1024;  // two blocks per SM with the static arrays
+constexpr int kAttnMaxPages = 512;
+static_assert(kAttnMaxPages <= kSelThreads, "one list slot per thread");
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kSelThreads, 2) attn_staged_kernel(
+    IndexView v, const T* __restrict__ q, const int32_t* __restrict__ page_ids,
+    const int32_t* __restrict__ n_pages, int page_stride, T* __restrict__ out) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_sel[kAttnMaxPages];
+    __shared__ int s_toff[kAttnMaxPages + 1];
+    __shared__ int s_ntok, s_fail;
+    __shared__ __align__(8) unsigned long long s_bar;
+    pdl_wait_then_release();
+    const int u = blockIdx.x, tid = threadIdx.x;
+    // the list length, the allocated page count and every slot of the list's row are read
+    // together (page_stride <= kSelThreads): one memory latency
+    int np = n_pages[u];
+    const int nalloc = v.next_id[v.ul(u, 0)];
+    int pid = tid < page_stride ? page_ids[(long long)u * page_stride + tid] : -1;
+    if (np < 0 || np > page_stride) {
+        if (tid == 0) set_status(v.status, ICE_ERR_BOUNDS);
+        np = np < 0 ? 0 : page_stride;
+    }
+    if (tid < np) {
+        if (pid < 0 || pid >= nalloc || pid >= v.C) {
+            set_status(v.status, ICE_ERR_BOUNDS);
+            pid = -1;  // no rows
+        }
+        s_sel[tid] = pid;
+    }
+    if (tid == 0) {
+        s_fail = 0;
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int pad = pad_to_128(smem);
+    attend_staged<T, G>(v, u, q, nullptr, nullptr, nullptr, 0, np, s_sel, s_toff, &s_ntok, smem + pad,
+                        kAttnStagedSmem - pad, smem_u32(&s_bar), &s_fail, out);
+}
+
+template <typename T>
+static cudaError_t launch_attn_staged_dt(const IndexView& v, const void* q, const int32_t* page_ids,
+                                         const int32_t* n_pages, int page_stride, void* out,
+                                         cudaStream_t s) {
+    const T* qq = (const T*)q;
+    T* oo = (T*)out;
+    const size_t b = kAttnStagedSmem;
+    switch (v.G) {
+        case 1: return launch_pdl(attn_staged_kernel<T, 1>, dim3(v.U), dim3(kSelThreads), b, s, v, qq, page_ids, n_pages, page_stride, oo);
+        case 2: return launch_pdl(attn_staged_kernel<T, 2>, dim3(v.U), dim3(kSelThreads), b, s, v, qq, page_ids, n_pages, page_stride, oo);
+        case 4: return launch_pdl(attn_staged_kernel<T, 4>, dim3(v.U), dim3(kSelThreads), b, s, v, qq, page_ids, n_pages, page_stride, oo);
+        // eight heads hold 64 registers of query and output per lane, the whole bound of
+        // two 512-thread blocks per SM: the plain-load kernel, without that bound
+        case 8: return launch_attn(v, q, page_ids, n_pages, page_stride, out, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_attn_staged(const IndexView& v, const void* q, const int32_t* page_ids,
+                               const int32_t* n_pages, int page_stride, void* out, cudaStream_t s) {
+    if (page_stride < 1 || page_stride > kAttnMaxPages) return cudaErrorInvalidValue;
+    if (v.dtype == ICE_BF16)
+        return launch_attn_staged_dt<__nv_bfloat16>(v, q, page_ids, n_pages, page_stride, out, s);
+    return launch_attn_staged_dt<float>(v, q, page_ids, n_pages, page_stride, out, s);
+}
+
 static void select_caps(int L, int P, int n_cand, int* sort_cap, int* hcap) {
     const int cand_cap = L * (n_cand + P - 1);
     int c = 1;
@@ -1170,7 +1243,10 @@ cudaError_t select_prepare() {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
     if (e == cudaSuccess)                                                                         \
         e = cudaFuncSetAttribute(select_kernel<T, G, true>,                                       \
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
+    if (e == cudaSuccess && G < 8)                                                                \
+        e = cudaFuncSetAttribute(attn_staged_kernel<T, (G < 8 ? G : 4)>,                          \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnStagedSmem);
     ICE_SET_SMEM(__nv_bfloat16, 1) ICE_SET_SMEM(__nv_bfloat16, 2) ICE_SET_SMEM(__nv_bfloat16, 4)
     ICE_SET_SMEM(__nv_bfloat16, 8) ICE_SET_SMEM(float, 1) ICE_SET_SMEM(float, 2)
     ICE_SET_SMEM(float, 4) ICE_SET_SMEM(float, 8)

@@ -124,7 +124,10 @@ __host__ __device__ inline CluSmem clu_layout(long long C, const CluDims& d, int
     return s;
 }
 
+// The .aligned cluster barrier expects every thread of a warp to execute it together:
+// the warp is reconverged first.
 __device__ __forceinline__ void clu_arrive() {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void clu_wait() {
@@ -323,31 +326,29 @@ __device__ __forceinline__ void attend_partial(const IndexView& v, int u, const 
         p0 = p1;
         ++round;
     }
-    float* part = reinterpret_cast<float*>(stage);  // [warp][head][kD + 2]
+    // rows [warp][head] of PR floats (accumulator, m, sum): one 16-byte store per lane and
+    // head, where scalar stores 16 bytes apart would conflict four ways in the banks
+    constexpr int PR = kD + 4;
+    float* part = reinterpret_cast<float*>(stage);
     {
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            float* pw = part + (warp * G + hh) * (kD + 2) + 4 * lane;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) pw[k] = acc[hh][k];
-        }
-        if ((lane & ((1 << HS) - 1)) == 0) {
-            float* pw = part + (warp * G + hl) * (kD + 2);
-            pw[kD] = m;
-            pw[kD + 1] = lsum;
-        }
+        for (int hh = 0; hh < G; ++hh)
+            *reinterpret_cast<float4*>(part + (warp * G + hh) * PR + 4 * lane) =
+                make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+        if ((lane & ((1 << HS) - 1)) == 0)
+            *reinterpret_cast<float2*>(part + (warp * G + hl) * PR + kD) = make_float2(m, lsum);
     }
     __syncthreads();
     for (int e = tid; e < G * kD; e += kCT) {
         const int hh = e / kD, dcol = e % kD;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) M = fmaxf(M, part[(w * G + hh) * (kD + 2) + kD]);
+        for (int w = 0; w < kCW; ++w) M = fmaxf(M, part[(w * G + hh) * PR + kD]);
         float Lt = 0.0f, O = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kCW; ++w) {
-                const float* pw = part + (w * G + hh) * (kD + 2);
+                const float* pw = part + (w * G + hh) * PR;
                 if (pw[kD] == -INFINITY) continue;
                 const float cf = exp2_approx(pw[kD] - M);
                 Lt = fmaf(pw[kD + 1], cf, Lt);
@@ -1167,7 +1168,7 @@ CluPlan clu_plan(const IndexView& v, int K, int n_sel, int n_cand, bool fused, i
     need = std::max(need, lay.stage + 2 * 2 * kD * es);
     if (fused) {
         need = std::max(need, lay.X + 2 * P * kD * es);
-        need = std::max(need, lay.X + kCW * v.G * (kD + 2) * 4);
+        need = std::max(need, lay.X + kCW * v.G * (kD + 4) * 4);  // partial rows of kD + 4
     }
     p.bytes = need > kCluSmemMax ? need : std::min(std::max(need, target_bytes), kCluSmemMax);
     return p;
