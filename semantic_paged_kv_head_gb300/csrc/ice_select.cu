@@ -1058,6 +1058,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 constexpr int kAttnStagedSmem = 104 * 1024;  // two blocks per SM with the static arrays
 constexpr int kAttnMaxPages = 512;
 static_assert(kAttnMaxPages <= kSelThreads, "one list slot per thread");
+static_assert(kAttnStagedSmem - 128 >= 2 * kMaxP * kD * 4, "a page's f32 K and V rows fit one round");
+static_assert(kAttnStagedSmem - 128 >= kSelWarps * 4 * (kD + 4) * 4 + 4 * (kSelWarps + 1) * 4,
+              "the partials of four heads fit the staging region");
 
 template <typename T, int G>
 __global__ void __launch_bounds__(kSelThreads, 2) attn_staged_kernel(
