@@ -36,10 +36,33 @@ struct ice_index {
     int* reuse_age = nullptr;              // [U] reuses since that selection; -1 = none
     int32_t* reuse_flag = nullptr;         // [U] 1 where this step selects
     int reuse_budget = -1;
+    // the stream of the last launch that wrote index tables (an insert), until a selection
+    // on that stream has waited for it; until then a selection on that stream reads the
+    // index only after its wait on the previous kernel
+    void* write_stream = nullptr;
+    bool write_pending = false;
     IndexView v;
 };
 
 namespace {
+
+// The view a selection launch on `stream` gets: the index may be read before the wait on
+// the stream's previous kernel unless that kernel may have written it.
+IndexView select_view(const ice_index* ix, void* stream) {
+    IndexView vv = ix->v;
+    vv.early_index = (ix->write_pending && ix->write_stream == stream) ? 0 : 1;
+    return vv;
+}
+
+// A selection was launched on `stream`: it waits for the write pending there.
+void select_issued(ice_index* ix, void* stream) {
+    if (ix->write_pending && ix->write_stream == stream) ix->write_pending = false;
+}
+
+void index_written(ice_index* ix, void* stream) {
+    ix->write_pending = true;
+    ix->write_stream = stream;
+}
 
 // splitmix64 (Steele, Lea & Flood 2014), the generator of the directions.
 uint64_t sm64(uint64_t& s) {
@@ -360,6 +383,7 @@ int ice_insert(ice_index* ix, const void* k, const void* v, void* stream) {
     if (ix->n_tok >= ix->v.max_tokens) return ICE_ERR_CAPACITY;
     cudaError_t e = launch_insert(ix->v, k, v, (cudaStream_t)stream);
     if (e != cudaSuccess) return ICE_ERR_CUDA;
+    index_written(ix, stream);
     ix->n_tok += 1;
     return ICE_OK;
 }
@@ -408,9 +432,11 @@ static int select_common(ice_index* ix, const void* q, int32_t token_budget, int
     const int P = ix->p.page_size;
     const int n_sel = token_budget / P;
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
-    cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, stats, out, reselect,
-                                  (cudaStream_t)stream);
-    return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
+    cudaError_t e = launch_select(select_view(ix, stream), q, n_sel, n_cand, page_ids, n_pages, stats,
+                                  out, reselect, (cudaStream_t)stream);
+    if (e != cudaSuccess) return ICE_ERR_CUDA;
+    select_issued(ix, stream);
+    return ICE_OK;
 }
 
 int ice_select(ice_index* ix, const void* q, int32_t token_budget, int32_t* page_ids,
@@ -507,17 +533,21 @@ int ice_decode_step(ice_index* ix, const void* k, const void* v, const void* q,
     if (ix->p.kv_location == ICE_KV_DEVICE && Kc >= 2 &&
         select_cluster_bytes(ix->v, Kc, n_sel, n_cand, true) >= 0) {
         if (launch_insert(ix->v, k, v, (cudaStream_t)stream) != cudaSuccess) return ICE_ERR_CUDA;
+        index_written(ix, stream);
         ix->n_tok += 1;
-        cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, nullptr, out,
-                                      nullptr, (cudaStream_t)stream);
-        return e == cudaSuccess ? ICE_OK : ICE_ERR_CUDA;
+        cudaError_t e = launch_select(select_view(ix, stream), q, n_sel, n_cand, page_ids, n_pages,
+                                      nullptr, out, nullptr, (cudaStream_t)stream);
+        if (e != cudaSuccess) return ICE_ERR_CUDA;
+        select_issued(ix, stream);
+        return ICE_OK;
     }
     if (ix->p.kv_location == ICE_KV_DEVICE &&
         select_insert_fits(ix->C, ix->p.n_composite, P, n_cand, n_sel, es)) {
         // one launch: every block inserts its unit's token, then selects and attends
-        cudaError_t e = launch_select(ix->v, q, n_sel, n_cand, page_ids, n_pages, nullptr, out,
-                                      nullptr, (cudaStream_t)stream, k, v);
+        cudaError_t e = launch_select(select_view(ix, stream), q, n_sel, n_cand, page_ids, n_pages,
+                                      nullptr, out, nullptr, (cudaStream_t)stream, k, v);
         if (e != cudaSuccess) return ICE_ERR_CUDA;
+        index_written(ix, stream);  // its blocks insert before they select
         ix->n_tok += 1;
         return ICE_OK;
     }
@@ -541,8 +571,10 @@ int ice_select_heads(ice_index* ix, const void* q, int32_t token_budget, int32_t
     if (ix->G * n_sel > 512) return ICE_ERR_UNSUPPORTED;  // the attention's page-list bound
     const int n_cand = ix->p.n_cand > 0 ? ix->p.n_cand : token_budget;
     cudaStream_t st = (cudaStream_t)stream;
-    if (launch_select_heads(ix->v, q, n_sel, n_cand, head_page_ids, head_n_pages, st) != cudaSuccess)
+    if (launch_select_heads(select_view(ix, stream), q, n_sel, n_cand, head_page_ids, head_n_pages,
+                            st) != cudaSuccess)
         return ICE_ERR_CUDA;
+    select_issued(ix, stream);
     if (launch_union(ix->U, ix->G, n_sel, head_page_ids, head_n_pages, page_ids, n_pages, st) !=
         cudaSuccess)
         return ICE_ERR_CUDA;

@@ -75,6 +75,10 @@ struct IndexView {
     int* n_tok;  // [U] tokens in each unit (build + inserts), advanced by the insert kernel
     int debug;  // ICE_DEBUG_* flags (tests only), 0 in normal use
     int cluster_k;  // blocks per unit of the selection: 0 automatic, 1, 2, 4, 8 or 16
+    // 1 when the previous kernel of the launch's stream wrote no index table: the cluster
+    // selection then reads the index before it waits on that kernel (programmatic
+    // dependent launch), so those reads overlap the previous kernel
+    int early_index;
 
     __host__ __device__ long long ul(int u, int l) const { return (long long)u * L + l; }
     __host__ __device__ long long leaf_base(int u, int l) const { return ul(u, l) * C; }

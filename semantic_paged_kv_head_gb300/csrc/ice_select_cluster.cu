@@ -376,7 +376,6 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     __shared__ int s_pstar, s_need, s_nch, s_base, s_ncand, s_cmp, s_fail, s_gn, s_taken, s_nl[kMaxL];
     __shared__ __align__(8) unsigned long long s_bar;
 
-    pdl_wait_then_release();
     cg::cluster_group cluster = cg::this_cluster();
     const int K = (int)cluster.num_blocks();
     const int r = (int)cluster.block_rank();
@@ -404,14 +403,25 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
     int* hubx0 = cluster.map_shared_rank(hubx, 0);
 
     // ---- 1. leaf count, query heads and directions requested together ------------------
+    // The query may be the previous kernel's output: it is read after the wait on that
+    // kernel (programmatic dependent launch). The index tables are read before the wait
+    // when that kernel wrote none of them (early): the leaf counts, the directions and the
+    // scan's first copies then overlap the previous kernel.
+    const bool early = v.early_index != 0;
+    float qh[G][4];
+    const T* qu = q + (long long)row * G * kD;
+    auto load_query = [&]() {
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) load4(qu + (long long)hh * kD + 4 * lane, qh[hh]);
+    };
+    if (!early) {
+        pdl_wait_then_release();
+        load_query();
+    }
     int Nl = v.n_leaf[v.ul(u, l)];
     int Nall = 0;
     if (r == 0)
         for (int ll = 0; ll < L; ++ll) Nall += max(0, min(v.n_leaf[v.ul(u, ll)], (int)C));
-    float qh[G][4];
-    const T* qu = q + (long long)row * G * kD;
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) load4(qu + (long long)hh * kD + 4 * lane, qh[hh]);
     float wdir[4] = {0.f, 0.f, 0.f, 0.f};
     float wlast = 0.f;
     if (warp < kM) {
@@ -469,6 +479,10 @@ __global__ void __launch_bounds__(kCT, 2) select_cluster_kernel(
         const int k = warp + sidx * kCW;
         if (k < nck) ring_issue(k, sidx);
         asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    if (early) {
+        pdl_wait_then_release();
+        load_query();
     }
     // query prep: q_sel = sum of the heads in head order, q~ = q_sel / |q_sel|,
     // codes of this block's composite (warp j: direction j)
