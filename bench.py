@@ -32,6 +32,18 @@ METRIC = "decode-step select+attn latency (µs/layer) & achieved HBM GB/s vs pea
 UNIT = "us/layer"
 WORKLOAD = "llama8b_36k"
 FUSED_KERNEL, FUSED_SRC = "select_kernel<fused>", "ice_select.cu"
+CLUSTER_KERNEL, CLUSTER_SRC = "select_cluster_kernel<fused>", "ice_select_cluster.cu"
+
+
+def fused_kernel_of(units, n_composite, cluster_size=None):
+    """The kernel of ice_select_attn for a launch of `units` units, by the rule that
+    ice_set_cluster_size documents: 8, 4 or 2 blocks per unit (a cluster) up to 19, 38
+    or 76 units, one block per unit above, unless a size is set."""
+    k = cluster_size if cluster_size else (8 if units <= 19 else 4 if units <= 38 else
+                                           2 if units <= 76 else 1)
+    if k < n_composite:
+        k = 1
+    return (CLUSTER_KERNEL, CLUSTER_SRC) if k >= 2 else (FUSED_KERNEL, FUSED_SRC)
 FLUSH_BYTES = 256 << 20
 INSERT_WORKLOAD = "mistral7b_gen8k"
 # the single-replica measurements after the headline, in the order they run
@@ -202,9 +214,10 @@ def run_reference(args):
 # --------------------------------------------------------------------------------------
 # the GPU arm
 # --------------------------------------------------------------------------------------
-def _traffic_for(kernel, src_file):
+def _traffic_for(kernel, src_file, workload, units):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+    the current source of the kernel and describes this workload at this number of
+    units per launch (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -215,7 +228,7 @@ def _traffic_for(kernel, src_file):
         return None
     with open(os.path.join(ROOT, "semantic_paged_kv_head_gb300", "csrc", src_file), "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()[:16]
-    if ent.get("source_sha") != h:
+    if ent.get("source_sha") != h or ent.get("workload") != workload or ent.get("units") != units:
         return None
     return ent.get("dram_bytes_per_launch_full")
 
@@ -770,7 +783,8 @@ def run_ice(args):
     att_gbs = attn_bytes / (ms_att * 1e-3) / 1e9
     # the reported path is always the fused call; it is one kernel, so the roofline
     # kernel is that kernel and its time is the step's
-    dom, dom_bytes, dom_ms, src = FUSED_KERNEL, step_bytes, ms_fused, FUSED_SRC
+    dom, src = fused_kernel_of(U, w.n_composite, args.cluster_size)
+    dom_bytes, dom_ms = step_bytes, ms_fused
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
     # every rank runs its own replica of the workload: the job processes
     # world x n_layers layers per step
@@ -787,7 +801,7 @@ def run_ice(args):
         "step_us": {"median": round(ms_fused * 1e3, 3), "p10": round(fused_p10 * 1e3, 3),
                     "p90": round(fused_p90 * 1e3, 3), "samples": n_steps,
                     "loop_crosscheck": round(ms_loop * 1e3, 3), "loop_steps": n_x},
-        "kernels": {FUSED_KERNEL: {"us": round(ms_fused * 1e3, 3),
+        "kernels": {dom: {"us": round(ms_fused * 1e3, 3),
                                              "bytes": int(step_bytes),
                                              "gbs": round(step_bytes / (ms_fused * 1e-3) / 1e9, 1)},
                     "separate_calls": {"us": round(ms_sep * 1e3, 3),
@@ -798,7 +812,7 @@ def run_ice(args):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
-                     "traffic": _traffic_for(dom, src), "algorithmic_bytes": int(dom_bytes)},
+                     "traffic": _traffic_for(dom, src, w.name, U), "algorithmic_bytes": int(dom_bytes)},
         "e2e": {"value": round(us_per_layer(ms_e2e, w, world), 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(q.numel() * q.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),

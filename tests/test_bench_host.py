@@ -58,14 +58,30 @@ def test_traffic_record_only_for_its_source(tmp_path, monkeypatch):
     shutil.copy(os.path.join(ROOT, src_rel), tmp_path / src_rel)
     import hashlib
     sha = hashlib.sha256((tmp_path / src_rel).read_bytes()).hexdigest()[:16]
-    rec = {"select_kernel<fused>": {"source_sha": sha, "dram_bytes_per_launch_full": 12345}}
+    rec = {"select_kernel<fused>": {"source_sha": sha, "dram_bytes_per_launch_full": 12345,
+                                    "workload": "llama8b_36k", "units": 256}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench._traffic_for("select_kernel<fused>", "ice_select.cu") == 12345
-    assert bench._traffic_for("attn_kernel", "ice_select.cu") is None
+    assert bench._traffic_for("select_kernel<fused>", "ice_select.cu", "llama8b_36k", 256) == 12345
+    assert bench._traffic_for("attn_kernel", "ice_select.cu", "llama8b_36k", 256) is None
+    # another workload or another launch size: the record does not describe it
+    assert bench._traffic_for("select_kernel<fused>", "ice_select.cu", "qwen3_4b_250k", 256) is None
+    assert bench._traffic_for("select_kernel<fused>", "ice_select.cu", "llama8b_36k", 16) is None
     with open(tmp_path / src_rel, "a") as f:
         f.write("\n// changed\n")
-    assert bench._traffic_for("select_kernel<fused>", "ice_select.cu") is None
+    assert bench._traffic_for("select_kernel<fused>", "ice_select.cu", "llama8b_36k", 256) is None
+
+
+def test_fused_kernel_follows_the_documented_cluster_rule():
+    bench = _bench()
+    # launches of up to 76 units run the cluster kernel, larger ones one block per unit
+    assert bench.fused_kernel_of(8, 2)[0] == bench.CLUSTER_KERNEL
+    assert bench.fused_kernel_of(76, 2)[0] == bench.CLUSTER_KERNEL
+    assert bench.fused_kernel_of(77, 2)[0] == bench.FUSED_KERNEL
+    assert bench.fused_kernel_of(256, 2)[0] == bench.FUSED_KERNEL
+    assert bench.fused_kernel_of(8, 2, cluster_size=1)[0] == bench.FUSED_KERNEL
+    assert bench.fused_kernel_of(256, 2, cluster_size=2)[0] == bench.CLUSTER_KERNEL
+    assert bench.fused_kernel_of(60, 4)[0] == bench.FUSED_KERNEL  # 2 blocks < 4 composites
 
 
 def test_binding_refuses_unpinned_cpu_memory():
