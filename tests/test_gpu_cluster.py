@@ -118,3 +118,49 @@ def test_forced_timeout_in_a_cluster(ice):
     assert gix.get_error() == 0
     assert torch.equal(out2, ref)
     gix.destroy()
+
+
+def test_selection_reads_the_index_after_an_insert(ice):
+    """The cluster selection reads the index before its wait on the previous kernel of
+    the stream, except right after an insert on that stream. A selection right after
+    an insert must see the inserted token; one right after another selection reads
+    early and must agree with it; a decode step (insert, then selection) and the
+    selection after it agree too. No synchronisation between the calls: only the
+    stream orders them. Page ids follow the oracle after every insert."""
+    from semantic_paged_kv_head_gb300 import synth
+    w = synth.scaled(synth.WORKLOADS["mistral7b_gen8k"], n_kv_heads=2, n_tokens=600,
+                     n_insert=24, n_centers=12, seed=17)
+    keys, values, centers = synth.make_kv(w)
+    deltas = synth.make_drift(w, centers)
+    gix = ice.IceIndex.build(keys.cuda(), values.cuda(), page_size=w.page_size,
+                             n_q_heads=w.n_q_heads, n_composite=w.n_composite, seed=w.seed,
+                             max_tokens=w.n_tokens + w.n_insert)
+    U, G, n_sel = gix.n_units, w.group, w.budget // w.page_size
+    orcs = [oracle_for_unit(w, keys, values, u) for u in range(U)]
+    results = []
+    for s in range(w.n_insert):
+        k, v = synth.make_insert_token(w, centers, deltas, s)
+        q = synth.make_queries(w, centers, step=s, drift_deltas=deltas).cuda()
+        if s % 2 == 0:
+            gix.insert(k.cuda(), v.cuda())
+            first = gix.select_attn(q, w.budget)   # right after the insert: waits first
+        else:
+            ids = torch.empty((U, n_sel), dtype=torch.int32, device="cuda")
+            npg = torch.empty((U,), dtype=torch.int32, device="cuda")
+            out = torch.empty_like(q)
+            gix.decode_step(k.cuda(), v.cuda(), q, w.budget, ids, npg, out)
+            first = (out, ids, npg)
+        second = gix.select_attn(q, w.budget)      # right after a selection: reads early
+        for u in range(U):
+            orcs[u].insert(k.view(-1, w.d)[u], v.view(-1, w.d)[u])
+        results.append((s, q, first, second))
+    torch.cuda.synchronize()
+    assert gix.get_error() == 0
+    for s, q, (o1, i1, n1), (o2, i2, n2) in results:
+        assert torch.equal(i1, i2) and torch.equal(n1, n2), s
+        assert torch.equal(o1, o2), s
+    # the last step against the oracle (the index holds every insert by then)
+    s, q, (o1, i1, n1), _ = results[-1]
+    for u in range(U):
+        check_select_attn(w, orcs[u], q_of_unit(w, q.cpu(), u), i1[u], n1[u],
+                          o1.view(-1, G, w.d)[u], None, f"step {s} unit {u}")
