@@ -335,6 +335,44 @@ __device__ __noinline__ void insert_unit_call(const IndexView& v, int u, const T
     insert_unit<T, kSelThreads>(v, u, kin, vin, rows);
 }
 
+// More than kTopK pages to select: a block-wide bitonic sort of the compacted
+// (key, page) pairs, the first n_sel in order. Out of line (rarely taken), so that
+// the selection's own code path stays contiguous.
+__device__ __noinline__ void block_sort_select(unsigned long long* skey, int* sval, int npg, int n_sel,
+                                               int taken, int32_t* out, int* s_sel) {
+    const int tid = threadIdx.x;
+    int npow = 1;
+    while (npow < npg) npow <<= 1;
+    for (int c = npg + tid; c < npow; c += kSelThreads) {
+        skey[c] = ~0ull;
+        sval[c] = -1;
+    }
+    __syncthreads();
+    for (int k = 2; k <= npow; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < npow; i += kSelThreads) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const unsigned long long a = skey[i], b = skey[ixj];
+                    if ((a > b) == ((i & k) == 0)) {
+                        skey[i] = b;
+                        skey[ixj] = a;
+                        const int t = sval[i];
+                        sval[i] = sval[ixj];
+                        sval[ixj] = t;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int r = tid; r < n_sel; r += kSelThreads) {
+        const int pg = r < taken ? sval[r] : -1;
+        out[r] = pg;
+        s_sel[r] = pg;
+    }
+}
+
 template <typename T, int G, bool FUSED>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
@@ -995,37 +1033,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
             s_sel[lane] = pg;
         }
     } else {
-        // a block-wide bitonic sort of the compacted pairs
-        int npow = 1;
-        while (npow < npg) npow <<= 1;
-        for (int c = npg + tid; c < npow; c += kSelThreads) {
-            skey[c] = ~0ull;
-            sval[c] = -1;
-        }
-        __syncthreads();
-        for (int k = 2; k <= npow; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int i = tid; i < npow; i += kSelThreads) {
-                    const int ixj = i ^ j;
-                    if (ixj > i) {
-                        const unsigned long long a = skey[i], b = skey[ixj];
-                        if ((a > b) == ((i & k) == 0)) {
-                            skey[i] = b;
-                            skey[ixj] = a;
-                            const int t = sval[i];
-                            sval[i] = sval[ixj];
-                            sval[ixj] = t;
-                        }
-                    }
-                }
-                __syncthreads();
-            }
-        }
-        for (int r = tid; r < n_sel; r += kSelThreads) {
-            const int pg = r < taken ? sval[r] : -1;
-            out[r] = pg;
-            s_sel[r] = pg;
-        }
+        block_sort_select(skey, sval, npg, n_sel, taken, out, s_sel);
     }
     __syncthreads();
     if (tid == 0) n_pages_out[row] = taken;
