@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 
     // the unit keeps the pages it selected before (reuse across steps): no
     // selection, and the fused call attends over the pages in page_ids
-    if (reselect != nullptr && reselect[u] == 0) {  // block-uniform
+    if (__builtin_expect(reselect != nullptr && reselect[u] == 0, 0)) {  // block-uniform, rare
         if (FUSED) {
             const int taken = min(max(n_pages_out[u], 0), n_sel);
             for (int i = tid; i < taken; i += kSelThreads) s_sel[i] = page_ids[(long long)u * n_sel + i];
