@@ -254,23 +254,39 @@ __device__ __forceinline__ void attend_staged(const IndexView& v, int u, const T
 #pragma unroll
                 for (int b = HS - 1; b >= 0; --b) sc += __shfl_xor_sync(0xffffffffu, sc, 1 << b);
                 const float mn = fmaxf(m, sc);
-                const float corr = exp2_approx(m - mn);
                 const float p = exp2_approx(sc - mn);
-                lsum = lsum * corr + p;
-                m = mn;
                 float vx[4];
                 load4(sv + (size_t)j * kD + 4 * lane, vx);
+                if (__any_sync(0xffffffffu, mn != m)) {  // a head's maximum rose: rescale
+                    const float corr = exp2_approx(m - mn);
+                    lsum = lsum * corr + p;
+                    m = mn;
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float ch = __shfl_sync(0xffffffffu, corr, hh << HS);
-                    const float ph = __shfl_sync(0xffffffffu, p, hh << HS);
-                    const float2 c2 = make_float2(ch, ch), p2 = make_float2(ph, ph);
+                    for (int hh = 0; hh < G; ++hh) {
+                        const float ch = __shfl_sync(0xffffffffu, corr, hh << HS);
+                        const float ph = __shfl_sync(0xffffffffu, p, hh << HS);
+                        const float2 c2 = make_float2(ch, ch), p2 = make_float2(ph, ph);
 #pragma unroll
-                    for (int k = 0; k < 4; k += 2) {
-                        const float2 a2 = __ffma2_rn(p2, make_float2(vx[k], vx[k + 1]),
-                                                     __fmul2_rn(make_float2(acc[hh][k], acc[hh][k + 1]), c2));
-                        acc[hh][k] = a2.x;
-                        acc[hh][k + 1] = a2.y;
+                        for (int k = 0; k < 4; k += 2) {
+                            const float2 a2 = __ffma2_rn(p2, make_float2(vx[k], vx[k + 1]),
+                                                         __fmul2_rn(make_float2(acc[hh][k], acc[hh][k + 1]), c2));
+                            acc[hh][k] = a2.x;
+                            acc[hh][k + 1] = a2.y;
+                        }
+                    }
+                } else {  // every maximum held: the correction is 2^0 = 1
+                    lsum += p;
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        const float ph = __shfl_sync(0xffffffffu, p, hh << HS);
+                        const float2 p2 = make_float2(ph, ph);
+#pragma unroll
+                        for (int k = 0; k < 4; k += 2) {
+                            const float2 a2 = __ffma2_rn(p2, make_float2(vx[k], vx[k + 1]),
+                                                         make_float2(acc[hh][k], acc[hh][k + 1]));
+                            acc[hh][k] = a2.x;
+                            acc[hh][k + 1] = a2.y;
+                        }
                     }
                 }
             }
