@@ -130,12 +130,27 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
     uint4 pr = make_uint4(0u, 0u, 0u, 0u);
     if (in_group) pstep = probe(0, s_N[gl], pi, pk, pr);
 
-    // ---- key of the new token: frozen scale, projections, codes (warp 0) ----------
-    if (warp == 0) {
+    // ---- key of the new token: frozen scale, projections, codes. The L * kM direction
+    //      dots are spread over the warps (each warp forms the scaled key itself, in the
+    //      same fixed order), and one thread per composite interleaves the codes --------
+    {
+        constexpr int NW = NT / 32;
+        constexpr int kPerWarp = (kMaxL * kM + NW - 1) / NW;
+        __shared__ int s_code[kMaxL * kM];
         float k4[4];
         load4(kin + 4 * lane, k4);
-        const float nrm2 = warp_dot_fixed(k4, k4);
         const int e = v.e_unit[u];
+        float w[kPerWarp][4], wl[kPerWarp];  // this warp's directions, requested together
+#pragma unroll
+        for (int i = 0; i < kPerWarp; ++i) {
+            const int dj = warp + i * NW;
+            if (dj < v.L * kM) {
+                const float* ud = v.dirs + (long long)dj * kDirStride;
+                load4(ud + 4 * lane, w[i]);
+                wl[i] = ud[kD];
+            }
+        }
+        const float nrm2 = warp_dot_fixed(k4, k4);
         const float sc = ldexpf(1.0f, -e), sc2 = ldexpf(1.0f, -2 * e);
         float kt[4];
 #pragma unroll
@@ -143,17 +158,20 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
         float r = __fsub_rn(1.0f, __fmul_rn(nrm2, sc2));
         r = r > 0.0f ? r : 0.0f;
         const float tail = __fsqrt_rn(r);
-        for (int l = 0; l < v.L; ++l) {
+#pragma unroll
+        for (int i = 0; i < kPerWarp; ++i) {
+            const int dj = warp + i * NW;
+            if (dj < v.L * kM) {  // warp-uniform
+                const float p = __fmaf_rn(wl[i], tail, warp_dot_fixed(w[i], kt));
+                if (lane == 0) s_code[dj] = quantise_code(p);
+            }
+        }
+        __syncthreads();
+        if (tid < v.L) {
             int c[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float* ud = v.dirs + (long long)(l * kM + j) * kDirStride;
-                float w[4];
-                load4(ud + 4 * lane, w);
-                const float p = __fmaf_rn(ud[kD], tail, warp_dot_fixed(w, kt));
-                c[j] = quantise_code(p);
-            }
-            if (lane == 0) s_mk[l] = morton8(c);
+            for (int j = 0; j < 8; ++j) c[j] = s_code[tid * kM + j];
+            s_mk[tid] = morton8(c);
         }
     }
     __syncthreads();
