@@ -79,6 +79,7 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
     __shared__ unsigned int e_t[kMaxP + 1];
     __shared__ int e_slot[kMaxP + 1];  // original slot (P = the new token)
     __shared__ int s_sorted[kMaxP + 1];
+    __shared__ int s_ts1[kMaxP + 1];  // composite-1 slots of a splitting leaf's tokens
     __shared__ int s_cnt, s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -89,6 +90,13 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
     if (tok < 0 || tok >= v.max_tokens) {  // block-uniform
         if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
         return;
+    }
+
+    // the new token's K and V rows, staged as row P of the split's staging: the append,
+    // the split and the new leaf copy them from there, with no memory latency of their own
+    for (int i = tid; i < kD; i += NT) {
+        rows_k[(size_t)P * kD + i] = kin[i];
+        rows_v[(size_t)P * kD + i] = vin[i];
     }
 
     // ---- the search for the new key's leaf runs for all composites at once: thread
@@ -267,8 +275,8 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                 T* pk = reinterpret_cast<T*>(v.page_k) + v.page_row(u, id, cnt) * kD;
                 T* pv = reinterpret_cast<T*>(v.page_v) + v.page_row(u, id, cnt) * kD;
                 for (int i = tid; i < kD; i += NT) {
-                    pk[i] = kin[i];
-                    pv[i] = vin[i];
+                    pk[i] = rows_k[(size_t)P * kD + i];
+                    pv[i] = rows_v[(size_t)P * kD + i];
                 }
             }
             __syncthreads();
@@ -287,21 +295,32 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                 }
                 e_slot[j] = j;
             }
-            if (l == 0) {  // stage the P old rows and the new row, K and V
+            if (l == 0) {  // stage the P old rows, K and V (row P holds the new token's)
                 const T* pk = reinterpret_cast<const T*>(v.page_k) + v.page_row(u, id, 0) * kD;
                 const T* pv = reinterpret_cast<const T*>(v.page_v) + v.page_row(u, id, 0) * kD;
-                for (int i = tid; i < (P + 1) * kD; i += NT) {
+                for (int i = tid; i < P * kD; i += NT) {
                     const int r = i / kD, c = i % kD;
-                    rows_k[i] = r < P ? pk[(long long)r * kD + c] : kin[c];
-                    rows_v[i] = r < P ? pv[(long long)r * kD + c] : vin[c];
+                    rows_k[i] = pk[(long long)r * kD + c];
+                    rows_v[i] = pv[(long long)r * kD + c];
                 }
             }
             __syncthreads();
-            // rank of each key among the P+1 (keys are distinct)
+            // rank of each key among the P+1 (keys are distinct); meanwhile the upper half of
+            // the block requests the composite-1 slots of the leaf's tokens, which follow
+            // them to their new rows below (stored to shared memory in the next step)
             for (int j = tid; j <= P; j += NT) {
                 int r = 0;
                 for (int k = 0; k <= P; ++k) r += key_less(e_m[k], e_t[k], e_m[j], e_t[j]);
                 s_sorted[r] = j;
+            }
+            const bool fetch_s1 = l == 0 && v.tok_slot1 != nullptr && tid >= NT / 2;
+            int ts1[(kMaxP + 1 + NT / 2 - 1) / (NT / 2)];
+            if (fetch_s1) {
+#pragma unroll
+                for (int q2 = 0; q2 < (kMaxP + 1 + NT / 2 - 1) / (NT / 2); ++q2) {
+                    const int j = tid - NT / 2 + q2 * (NT / 2);
+                    ts1[q2] = j <= P ? v.tok_slot1[(long long)u * v.max_tokens + e_t[j]] : -1;
+                }
             }
             __syncthreads();
             const int f = s_sorted[0], g = s_sorted[P];
@@ -310,6 +329,13 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                 int nl = 0;
                 for (int r = 0; r <= P; ++r) nl += key_bit96(e_m[s_sorted[r]], e_t[s_sorted[r]], lam) == 0;
                 s_cnt = nl;
+            }
+            if (fetch_s1) {
+#pragma unroll
+                for (int q2 = 0; q2 < (kMaxP + 1 + NT / 2 - 1) / (NT / 2); ++q2) {
+                    const int j = tid - NT / 2 + q2 * (NT / 2);
+                    if (j <= P) s_ts1[j] = ts1[q2];
+                }
             }
             __syncthreads();
             const int nl = s_cnt, nr = P + 1 - nl;
@@ -324,7 +350,7 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                     v.tok_loc[(long long)u * v.max_tokens + e_t[j]] = dst * P + slot;
                     // the token's composite-1 slot follows it to its new row
                     if (v.tok_slot1 != nullptr) {
-                        const int s1 = v.tok_slot1[(long long)u * v.max_tokens + e_t[j]];
+                        const int s1 = s_ts1[j];
                         if (s1 >= 0) v.slot_loc1[v.loc1_base(u) + s1] = dst * P + slot;
                     }
                 }
@@ -397,8 +423,8 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
                 T* pk = reinterpret_cast<T*>(v.page_k) + v.page_row(u, nidl, 0) * kD;
                 T* pv = reinterpret_cast<T*>(v.page_v) + v.page_row(u, nidl, 0) * kD;
                 for (int i = tid; i < kD; i += NT) {
-                    pk[i] = kin[i];
-                    pv[i] = vin[i];
+                    pk[i] = rows_k[(size_t)P * kD + i];
+                    pv[i] = rows_v[(size_t)P * kD + i];
                 }
             }
             shift_right<NT>(lk, lr, llo, ltc, pos + 1, N);
