@@ -84,9 +84,41 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = v.P;
+    // Every request that depends on nothing else goes out first, together: the token
+    // count, the leaf counts and next list ids, the new token's rows, its key for the
+    // projections, the unit's exponent and the directions of this warp's projections
+    // (the L * kM direction dots are spread over the warps; each warp forms the scaled
+    // key itself, in the same fixed order). The addresses are valid whatever the count.
+    static_assert(NT >= kD, "one element of the new rows per thread");
+    constexpr int NW = NT / 32;
+    constexpr int kPerWarp = (kMaxL * kM + NW - 1) / NW;
     // the new token's index is the unit's count, kept on the device (so that a
     // captured CUDA graph of inserts advances it on every replay)
     const int tok = v.n_tok[u];
+    const int Lc = v.L;
+    int n_l = 0, nid_l = 0;
+    if (tid < Lc) {
+        n_l = v.n_leaf[v.ul(u, tid)];
+        nid_l = v.next_id[v.ul(u, tid)];
+    }
+    T kin_i{}, vin_i{};
+    if (tid < kD) {
+        kin_i = kin[tid];
+        vin_i = vin[tid];
+    }
+    float k4[4];
+    load4(kin + 4 * lane, k4);
+    const int e = v.e_unit[u];
+    float w[kPerWarp][4], wl[kPerWarp];  // this warp's directions
+#pragma unroll
+    for (int i = 0; i < kPerWarp; ++i) {
+        const int dj = warp + i * NW;
+        if (dj < v.L * kM) {
+            const float* ud = v.dirs + (long long)dj * kDirStride;
+            load4(ud + 4 * lane, w[i]);
+            wl[i] = ud[kD];
+        }
+    }
     if (tok < 0 || tok >= v.max_tokens) {  // block-uniform
         if (tid == 0) set_status(v.status, ICE_ERR_CAPACITY);
         return;
@@ -94,21 +126,20 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
 
     // the new token's K and V rows, staged as row P of the split's staging: the append,
     // the split and the new leaf copy them from there, with no memory latency of their own
-    for (int i = tid; i < kD; i += NT) {
-        rows_k[(size_t)P * kD + i] = kin[i];
-        rows_v[(size_t)P * kD + i] = vin[i];
+    if (tid < kD) {
+        rows_k[(size_t)P * kD + tid] = kin_i;
+        rows_v[(size_t)P * kD + tid] = vin_i;
     }
 
     // ---- the search for the new key's leaf runs for all composites at once: thread
-    //      group l (NT / L threads) searches composite l. The leaf counts come first;
-    //      the first probes are requested while warp 0 forms the new key's codes.
+    //      group l (NT / L threads) searches composite l. The first probes are requested
+    //      while the warps form the new key's codes.
     __shared__ int s_N[kMaxL], s_nid[kMaxL], s_lo2[kMaxL], s_hi2[kMaxL], s_a[kMaxL], s_fin[kMaxL];
     __shared__ LeafKey s_pk[kMaxL];
     __shared__ uint4 s_pr[kMaxL];
-    const int Lc = v.L;
     if (tid < Lc) {
-        s_N[tid] = v.n_leaf[v.ul(u, tid)];
-        s_nid[tid] = v.next_id[v.ul(u, tid)];
+        s_N[tid] = n_l;
+        s_nid[tid] = nid_l;
         s_lo2[tid] = 0;
         s_a[tid] = -1;
         s_fin[tid] = 0;
@@ -138,26 +169,10 @@ __device__ void insert_unit(const IndexView& v, int u, const T* __restrict__ kin
     uint4 pr = make_uint4(0u, 0u, 0u, 0u);
     if (in_group) pstep = probe(0, s_N[gl], pi, pk, pr);
 
-    // ---- key of the new token: frozen scale, projections, codes. The L * kM direction
-    //      dots are spread over the warps (each warp forms the scaled key itself, in the
-    //      same fixed order), and one thread per composite interleaves the codes --------
+    // ---- key of the new token: frozen scale, projections, codes; one thread per
+    //      composite interleaves the codes ------------------------------------------------
     {
-        constexpr int NW = NT / 32;
-        constexpr int kPerWarp = (kMaxL * kM + NW - 1) / NW;
         __shared__ int s_code[kMaxL * kM];
-        float k4[4];
-        load4(kin + 4 * lane, k4);
-        const int e = v.e_unit[u];
-        float w[kPerWarp][4], wl[kPerWarp];  // this warp's directions, requested together
-#pragma unroll
-        for (int i = 0; i < kPerWarp; ++i) {
-            const int dj = warp + i * NW;
-            if (dj < v.L * kM) {
-                const float* ud = v.dirs + (long long)dj * kDirStride;
-                load4(ud + 4 * lane, w[i]);
-                wl[i] = ud[kD];
-            }
-        }
         const float nrm2 = warp_dot_fixed(k4, k4);
         const float sc = ldexpf(1.0f, -e), sc2 = ldexpf(1.0f, -2 * e);
         float kt[4];
