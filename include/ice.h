@@ -35,8 +35,13 @@
  *  - Return value: ICE_OK (0) or a negative ICE_ERR_* code. Argument errors
  *    are found on the host before anything is launched. Errors that only the
  *    GPU can see (a page id out of range, an exhausted capacity) are recorded
- *    in a per-index device status word that ice_get_error() returns; kernels
- *    never trap and never wait on other blocks.
+ *    in a per-index device status word that ice_get_error() returns. Kernels
+ *    never trap; the only waits between blocks are the barriers of one
+ *    thread-block cluster, whose blocks run together.
+ *  - One handle is used by one host thread at a time: the calls keep host-side
+ *    state (the token count, the stream of the last insert). Separate handles
+ *    are independent. Calls on one stream run in order; calls on different
+ *    streams that touch one handle must be ordered by the caller (events).
  *  - Element type of keys, values, queries and outputs is the index's dtype
  *    (ICE_BF16 or ICE_F32); rows of d elements are contiguous.
  */
