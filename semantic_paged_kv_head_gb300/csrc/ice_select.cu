@@ -389,7 +389,10 @@ __device__ __noinline__ void block_sort_select(unsigned long long* skey, int* sv
     }
 }
 
-template <typename T, int G, bool FUSED>
+// INSERT: the one-launch decode step, whose blocks insert their unit's token first. It
+// is a separate instantiation: the out-of-line insert call in the kernel slowed the
+// plain fused selection, which never takes it, by 1.3 us on the 32-layer step.
+template <typename T, int G, bool FUSED, bool INSERT = false>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
     int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     const uint4* recs = v.leaf_rec;
 
     // the fused decode step: this block first inserts its unit's new token
-    if constexpr (FUSED) {
+    if constexpr (FUSED && INSERT) {
         if (knew != nullptr) {  // block-uniform
             insert_unit_call<T>(v, u, knew + (long long)u * kD, vnew + (long long)u * kD,
                                 smem + lay.free);
@@ -1186,6 +1189,10 @@ static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel,
     select_caps(v.L, v.P, n_cand, &sort_cap, &hcap);
     const bool fused = out != nullptr;
     const int bytes = select_smem_bytes(v.C, v.L, v.P, n_cand, n_sel, G, fused);
+    if (fused && knew != nullptr)
+        return launch_pdl(select_kernel<T, G, true, true>, dim3(v.U), dim3(kSelThreads), (size_t)bytes, s,
+                          v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats,
+                          (T*)out, reselect, 1, (const T*)knew, (const T*)vnew);
     if (fused)
         return launch_pdl(select_kernel<T, G, true>, dim3(v.U), dim3(kSelThreads), (size_t)bytes, s, v,
                           (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats,
@@ -1270,6 +1277,9 @@ cudaError_t select_prepare() {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
     if (e == cudaSuccess)                                                                         \
         e = cudaFuncSetAttribute(select_kernel<T, G, true>,                                       \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
+    if (e == cudaSuccess)                                                                         \
+        e = cudaFuncSetAttribute(select_kernel<T, G, true, true>,                                 \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
     if (e == cudaSuccess && G < 8)                                                                \
         e = cudaFuncSetAttribute(attn_staged_kernel<T, (G < 8 ? G : 4)>,                          \

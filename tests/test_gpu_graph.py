@@ -105,6 +105,9 @@ def test_fused_decode_step_equals_separate_calls(ice, dtype):
 
     U, n_sel = w.n_units, w.budget // w.page_size
     fused, sep = index(), index()
+    # one block per unit: with few units the automatic choice is the cluster selection,
+    # which runs the decode step as an insert launch and a selection launch
+    fused.set_cluster_size(1)
     orcs = [oracle_for_unit(w, keys, values, u) for u in range(U)]
     ids_f = torch.empty((U, n_sel), dtype=torch.int32, device="cuda")
     npg_f = torch.empty((U,), dtype=torch.int32, device="cuda")
