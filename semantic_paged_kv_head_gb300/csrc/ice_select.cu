@@ -389,10 +389,11 @@ __device__ __noinline__ void block_sort_select(unsigned long long* skey, int* sv
     }
 }
 
-// INSERT: the one-launch decode step, whose blocks insert their unit's token first. It
-// is a separate instantiation: the out-of-line insert call in the kernel slowed the
-// plain fused selection, which never takes it, by 1.3 us on the 32-layer step.
-template <typename T, int G, bool FUSED, bool INSERT = false>
+// INSERT: the one-launch decode step, whose blocks insert their unit's token first.
+// KEEP: selection reuse, where a unit may keep its pages and only attend. Both are
+// separate instantiations: the out-of-line insert call in the kernel slowed the plain
+// fused selection, which never takes it, by 1.3 us on the 32-layer step.
+template <typename T, int G, bool FUSED, bool INSERT = false, bool KEEP = false>
 __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
     IndexView v, const T* __restrict__ q, int n_sel, int n_cand, int sort_cap, int hcap,
     int smem_total, int32_t* __restrict__ page_ids, int32_t* __restrict__ n_pages_out,
@@ -449,7 +450,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_kernel(
 
     // the unit keeps the pages it selected before (reuse across steps): no
     // selection, and the fused call attends over the pages in page_ids
-    if (__builtin_expect(reselect != nullptr && reselect[u] == 0, 0)) {  // block-uniform, rare
+    if (KEEP && reselect != nullptr && reselect[u] == 0) {  // block-uniform
         if (FUSED) {
             const int taken = min(max(n_pages_out[u], 0), n_sel);
             for (int i = tid; i < taken; i += kSelThreads) s_sel[i] = page_ids[(long long)u * n_sel + i];
@@ -1193,6 +1194,16 @@ static cudaError_t launch_select_g(const IndexView& v, const void* q, int n_sel,
         return launch_pdl(select_kernel<T, G, true, true>, dim3(v.U), dim3(kSelThreads), (size_t)bytes, s,
                           v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats,
                           (T*)out, reselect, 1, (const T*)knew, (const T*)vnew);
+    if (reselect != nullptr) {
+        if (fused)
+            return launch_pdl(select_kernel<T, G, true, false, true>, dim3(v.U), dim3(kSelThreads),
+                              (size_t)bytes, s, v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes,
+                              page_ids, n_pages, stats, (T*)out, reselect, 1, (const T*)nullptr,
+                              (const T*)nullptr);
+        return launch_pdl(select_kernel<T, G, false, false, true>, dim3(v.U), dim3(kSelThreads),
+                          (size_t)bytes, s, v, (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids,
+                          n_pages, stats, (T*)nullptr, reselect, 1, (const T*)nullptr, (const T*)nullptr);
+    }
     if (fused)
         return launch_pdl(select_kernel<T, G, true>, dim3(v.U), dim3(kSelThreads), (size_t)bytes, s, v,
                           (const T*)q, n_sel, n_cand, sort_cap, hcap, bytes, page_ids, n_pages, stats,
@@ -1280,6 +1291,12 @@ cudaError_t select_prepare() {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
     if (e == cudaSuccess)                                                                         \
         e = cudaFuncSetAttribute(select_kernel<T, G, true, true>,                                 \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
+    if (e == cudaSuccess)                                                                         \
+        e = cudaFuncSetAttribute(select_kernel<T, G, true, false, true>,                          \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
+    if (e == cudaSuccess)                                                                         \
+        e = cudaFuncSetAttribute(select_kernel<T, G, false, false, true>,                         \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim);               \
     if (e == cudaSuccess && G < 8)                                                                \
         e = cudaFuncSetAttribute(attn_staged_kernel<T, (G < 8 ? G : 4)>,                          \
