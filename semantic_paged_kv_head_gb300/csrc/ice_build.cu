@@ -312,10 +312,13 @@ constexpr int kTcThreads = 128;              // one thread per token row, 4 warp
 constexpr int kTcTileB = kTcRows * kD * 2;   // 32 KB
 constexpr int kTcHalfB = kTcTileB / 2;       // one 64-dimension box
 constexpr int kTcDirB = 16 * kD * 2;         // 16 directions x 128 bf16
-constexpr int kTcStages = 3;                 // tiles in shared memory (two copies ahead)
+constexpr int kTcStages = 2;                 // tiles in shared memory (one copy ahead)
 constexpr int kTcSmem = 1024 + kTcStages * kTcTileB + kTcDirB;  // + alignment slack
-constexpr int kTcBlocksPerSm = 2;
+constexpr int kTcBlocksPerSm = 3;            // 3 x 70.6 KB of shared memory, 3 x 32 tensor-memory columns
 constexpr int kTcTmemCols = 32;
+static_assert(kTcBlocksPerSm * (kTcSmem + 1024 + 64) <= 228 * 1024,
+              "the blocks' shared memory (each with its 1 KB reserve and static part) fits one SM");
+static_assert(kTcBlocksPerSm * kTcTmemCols <= 512, "the blocks' tensor-memory columns fit one SM");
 
 // Shared-memory matrix descriptor of a K-major operand with the 128-byte
 // swizzle: start address >> 4 (bits 0-13), leading offset 16 B (unused with
